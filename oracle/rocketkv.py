@@ -1,0 +1,299 @@
+"""Plain fp64 CPU oracle for the RocketKV hot path (SnapKV++ eviction + hybrid sparse decode).
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product path may import this module: only the tests,
+``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py``
+call it. It shares no code with the CUDA library and never imports it.
+
+Every function takes float64 numpy arrays that hold the exact values of the bf16 inputs and
+computes in float64. It is deliberately slow and literal: each step follows the method's text in
+the order the pages give it, with numpy library primitives (matmul, exp, sort) as the only
+building blocks.
+
+Sources (the pages, cited by title and section):
+  [P1] "RocketKV: Accelerating Long-Context LLM Inference via Two-Stage KV Cache Compression",
+       summarizepaper.com summary of arXiv 2502.14051v1 -- "Key points", "Summary".
+  [P3] the same title on paperhub.cn (OpenReview author responses) -- paragraphs
+       "Novelty: RocketKV is SnapKV + QUEST", "Potential Sensitivity to Kernel Size in SnapKV++",
+       "Lack of Direct Latency Comparison", "Is Needle Among Evicted Tokens",
+       "Explanation of Calculating Approximate Attention Scores", "Measurement of Exact-TopK",
+       "Are Different KV Tokens Retrieved at Each Decoding Step?",
+       "Is Page Always Divided Into 4?", "Novelty of SnapKV++".
+  [P4] the same title on pith.science (abstract v3).
+
+Readings taken where the pages leave a step open (each restated at its function):
+  R1  stage-1 keep N1 = min(L, B * p * d / c) (the 128K / 512 worked example in
+      "Is Page Always Divided Into 4?" gives 8192 = 16 * 512 with p = 4, c = d / 4).
+  R2  stage-1 scores are softmax probabilities (logits scaled by `scale`, normalised over every key
+      visible to that window query: the prefix plus the causal part of the window), summed over the
+      window rows and over the query heads of the KV head's group. Only prefix columns are ranked;
+      the window tokens are always kept.
+  R3  adaptive pooling kernel: L <= 8192 -> 7, L <= 32768 -> 15, else 31 ("longer -> larger").
+  R4  max pooling, stride 1, same length, window clipped at both ends.
+  R5  top-k order: larger key first, equal keys -> lower index. Kept indices stored ascending, then
+      the window positions.
+  R6  N1 >= L keeps everything; a cache of len <= B is attended densely (no approximation).
+  R7  channel pick on sum_h |q_h|; score and Kmin/Kmax sign choice on q_g = sum_h q_h.
+  R8  q_g[i] >= 0 reads Kmax (the product is 0 at q_g[i] == 0 either way).
+  R9  approximate scores are unscaled.
+  R10 S = floor((B/2) / p) whole pages are selected; a partial last page counts its valid tokens.
+  R11 the summary of a partial last page is over its valid tokens only.
+  R12 decode appends (when given) happen before attending; the new token is selectable.
+  R13 attention scale as given (1/sqrt(d) by default); output kept in float64.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "plan", "adaptive_kernel_size", "window_scores", "pool_max", "topk_desc",
+    "snapkv_compress", "page_summaries", "channel_pick", "approx_scores", "page_select",
+    "attention", "dense_decode", "hybrid_decode", "group_topk_attention", "append_token",
+]
+
+
+# --------------------------------------------------------------------------------------------
+# Planning: the compression-ratio decomposition
+# --------------------------------------------------------------------------------------------
+def adaptive_kernel_size(ctx: int) -> int:
+    """Pooling kernel from the prompt length (reading R3).
+
+    [P3] "Potential Sensitivity to Kernel Size in SnapKV++": the kernel size is chosen from the
+    sequence length, larger for longer inputs; [P1] "Key points" ties kernel size to sequence
+    length. The table itself is not on the pages: 7 up to 8K tokens, 15 up to 32K, 31 beyond.
+    """
+    if ctx <= 8192:
+        return 7
+    if ctx <= 32768:
+        return 15
+    return 31
+
+
+def plan(ctx: int, budget: int, head_dim: int, page: int = 0, channels: int = 0):
+    """Resolve (keep N1, page size p, channels c, pooling kernel) for one sequence.
+
+    [P3] "Is Page Always Divided Into 4?": the overall ratio ctx/B is split evenly between the two
+    stages, and the second stage's share evenly between the sequence dimension (page size) and the
+    head dimension (channels kept); 128K / 512 -> 256x -> 16x per stage -> page 4 and 4x fewer
+    channels. [P3] "Novelty: RocketKV is SnapKV + QUEST": ratio 16 split as 4 x 4.
+    Reading R1: p defaults to 4 and c to d/4, and N1 = min(ctx, B * p * d / c), so that the
+    approximation step reads exactly as many bytes as B/2 tokens of K and V.
+    """
+    if page == 0:
+        page = 4
+    if channels == 0:
+        channels = head_dim // 4
+    keep = min(ctx, budget * page * head_dim // channels)
+    return keep, page, channels, adaptive_kernel_size(ctx)
+
+
+# --------------------------------------------------------------------------------------------
+# Stage 1: SnapKV++ eviction
+# --------------------------------------------------------------------------------------------
+def window_scores(k: np.ndarray, q_win: np.ndarray, scale: float, return_lse: bool = False,
+                  all_columns: bool = False):
+    """Observation-window scores of the prefix, summed over the window and the GQA group.
+
+    k: [L, d] keys of one (sequence, layer, KV head); q_win: [G, W, d], the last W queries of the
+    G query heads that share this KV head. Window row j sits at absolute position L - W + j and
+    sees keys 0 .. L - W + j. Returns score[i] for the L - W prefix positions (reading R2):
+        score[i] = sum_h sum_j softmax_row(h, j)[i]
+    (all L column sums when `all_columns`; those add up to G * W).
+    [P1] "Key points" (SnapKV with the grouped-query enhancement); [P3] "Novelty of SnapKV++"
+    (the enhancement scores each KV head once from its whole group).
+    """
+    L, d = k.shape
+    G, W, _ = q_win.shape
+    rows = q_win.reshape(G * W, d)
+    logits = (rows @ k.T) * scale                      # [G*W, L]
+    pos = (L - W) + np.tile(np.arange(W), G)           # absolute position of each row
+    visible = np.arange(L)[None, :] <= pos[:, None]
+    logits = np.where(visible, logits, -np.inf)
+    m = logits.max(axis=1, keepdims=True)
+    e = np.exp(logits - m)
+    denom = e.sum(axis=1, keepdims=True)
+    probs = e / denom
+    score = probs.sum(axis=0) if all_columns else probs[:, : L - W].sum(axis=0)
+    if return_lse:
+        return score, (m[:, 0] + np.log(denom[:, 0])).reshape(G, W)
+    return score
+
+
+def pool_max(x: np.ndarray, kernel: int) -> np.ndarray:
+    """1-D max pooling, stride 1, same length, window clipped at the ends (reading R4).
+
+    [P3] "Potential Sensitivity to Kernel Size in SnapKV++" (pooling with an adaptive size).
+    """
+    assert kernel % 2 == 1 and kernel >= 1
+    r = kernel // 2
+    n = x.shape[0]
+    out = np.empty_like(x)
+    for i in range(n):
+        out[i] = x[max(0, i - r): min(n, i + r + 1)].max()
+    return out
+
+
+def topk_desc(keys: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest keys; equal keys -> lower index first (reading R5).
+
+    Returned in selection order (largest first). A full stable sort, nothing clever.
+    """
+    idx = np.arange(keys.shape[0])
+    order = np.lexsort((idx, -keys))                    # primary: -key, secondary: index
+    return order[:k]
+
+
+def snapkv_compress(k: np.ndarray, v: np.ndarray, q_win: np.ndarray, keep: int, kernel: int,
+                    scale: float):
+    """SnapKV++ for one (sequence, layer, KV head): score, pool, top-k, gather.
+
+    [P3] "Is Needle Among Evicted Tokens": eviction is independent per head and per layer.
+    [P3] "Measurement of Exact-TopK": SnapKV prunes the prompt by a one-time top-k filter.
+    Returns (kept_idx ascending prefix then window, K_kept, V_kept, prefix scores, pooled scores).
+    Reading R6: keep >= L keeps every token (scores are still returned).
+    """
+    L = k.shape[0]
+    W = q_win.shape[1]
+    score = window_scores(k, q_win, scale)
+    pooled = pool_max(score, kernel)
+    if keep >= L:
+        kept = np.arange(L)
+    else:
+        prefix = np.sort(topk_desc(pooled, keep - W))
+        kept = np.concatenate([prefix, np.arange(L - W, L)])
+    return kept, k[kept], v[kept], score, pooled
+
+
+# --------------------------------------------------------------------------------------------
+# Stage 2: hybrid sparse decode attention
+# --------------------------------------------------------------------------------------------
+def page_summaries(kc: np.ndarray, length: int, page: int):
+    """Element-wise Kmin / Kmax per page of consecutive tokens, channel-major [d, P].
+
+    [P3] "Explanation of Calculating Approximate Attention Scores": K is split into pages of
+    consecutive tokens and each page records its element-wise min and max. Reading R11: the last
+    page covers only its valid tokens.
+    """
+    d = kc.shape[1]
+    P = (length + page - 1) // page
+    kmin = np.empty((d, P))
+    kmax = np.empty((d, P))
+    for pg in range(P):
+        rows = kc[pg * page: min(length, (pg + 1) * page)]
+        kmin[:, pg] = rows.min(axis=0)
+        kmax[:, pg] = rows.max(axis=0)
+    return kmin, kmax
+
+
+def channel_pick(q: np.ndarray, channels: int):
+    """Top-|q| channels of a GQA group; returns (channels ascending, q_g = sum_h q_h).
+
+    [P3] "Explanation of Calculating Approximate Attention Scores": only head-dim positions where
+    |q| is large are used, and for GQA the selection uses the group sum of q or |q| so that all
+    heads of a group select alike. Reading R7: |q| summed for the pick, signed q for the score.
+    """
+    mag = np.abs(q).sum(axis=0)
+    chosen = np.sort(topk_desc(mag, channels))
+    return chosen, q.sum(axis=0)
+
+
+def approx_scores(q_g: np.ndarray, chosen: np.ndarray, kmin: np.ndarray, kmax: np.ndarray):
+    """Approximate page score: sum over the kept channels of max(q*Kmin, q*Kmax).
+
+    [P3] "Explanation of Calculating Approximate Attention Scores": per page, max(q x Kmin,
+    q x Kmax) bounds the highest score inside the page, and only one of Kmin / Kmax is fetched per
+    position, chosen by the sign of q. Reading R8 (q >= 0 -> Kmax), R9 (unscaled).
+    """
+    P = kmin.shape[1]
+    total = np.zeros(P)
+    for i in chosen:
+        row = kmax[i] if q_g[i] >= 0 else kmin[i]
+        total += q_g[i] * row
+    return total
+
+
+def page_select(scores: np.ndarray, n_select: int) -> np.ndarray:
+    """The n_select pages with the highest approximate score, ascending (reading R5, R10).
+
+    [P3] "Explanation of Calculating Approximate Attention Scores": "select pages with higher
+    scores".
+    """
+    return np.sort(topk_desc(scores, min(n_select, scores.shape[0])))
+
+
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float) -> np.ndarray:
+    """Softmax attention of G query heads [G, d] over T tokens k, v [T, d] -> [G, d]."""
+    logits = (q @ k.T) * scale
+    m = logits.max(axis=1, keepdims=True)
+    e = np.exp(logits - m)
+    return (e / e.sum(axis=1, keepdims=True)) @ v
+
+
+def dense_decode(q: np.ndarray, k: np.ndarray, v: np.ndarray, length: int, scale: float):
+    """Full-KV decode attention, the baseline the pages compare against ([P1] "Key points")."""
+    return attention(q, k[:length], v[:length], scale)
+
+
+def hybrid_decode(q: np.ndarray, kc: np.ndarray, vc: np.ndarray, length: int,
+                  kmin: np.ndarray, kmax: np.ndarray, budget: int, page: int, channels: int,
+                  scale: float):
+    """One hybrid decode step for one (sequence, layer, KV head) and its G query heads.
+
+    [P3] "Lack of Direct Latency Comparison": half the token budget is spent on the approximation
+    (steps 1, 2) and half on sparse attention (step 3). [P3] "Explanation of Calculating
+    Approximate Attention Scores": steps 1-2 (channel pick, approximate score, page select).
+    [P3] "Are Different KV Tokens Retrieved at Each Decoding Step?": the selection is redone per
+    step. Reading R6: length <= budget attends densely over every token.
+    Returns a dict with out [G, d], chosen channels, approx scores, selected pages, token ids.
+    """
+    if length <= budget:
+        tokens = np.arange(length)
+        return {"out": attention(q, kc[tokens], vc[tokens], scale), "tokens": tokens,
+                "channels": None, "scores": None, "pages": None}
+    chosen, q_g = channel_pick(q, channels)
+    P = (length + page - 1) // page
+    scores = approx_scores(q_g, chosen, kmin[:, :P], kmax[:, :P])
+    pages = page_select(scores, (budget // 2) // page)
+    tokens = np.concatenate([np.arange(pg * page, min(length, (pg + 1) * page)) for pg in pages])
+    return {"out": attention(q, kc[tokens], vc[tokens], scale), "tokens": tokens,
+            "channels": chosen, "scores": scores, "pages": pages}
+
+
+def group_topk_attention(q: np.ndarray, kc: np.ndarray, vc: np.ndarray, length: int, k: int,
+                         scale: float):
+    """Exact top-k attention shared by a GQA group: rank tokens by the true group logit sum.
+
+    [P3] "Measurement of Exact-TopK": the oracle top-k scheme picks the top-k tokens by their true
+    scores at every step. With the selection shared per group ([P3] "Explanation of Calculating
+    Approximate Attention Scores"), the true group score of token t is sum_h q_h . k_t.
+    Written independently of `hybrid_decode`: it is what that function must reduce to with page
+    size 1 and all channels kept.
+    """
+    true_scores = kc[:length] @ q.sum(axis=0)
+    tokens = np.sort(topk_desc(true_scores, min(k, length)))
+    return attention(q, kc[tokens], vc[tokens], scale), tokens
+
+
+def append_token(kc: np.ndarray, vc: np.ndarray, length: int, kmin: np.ndarray,
+                 kmax: np.ndarray, new_k: np.ndarray, new_v: np.ndarray, page: int):
+    """Append one decode token and update the page it lands in (reading R12, R11).
+
+    Arrays are modified in place; returns the new length. A token that opens a page sets that
+    page's Kmin = Kmax = new_k; otherwise the page's min / max absorb it.
+    """
+    kc[length] = new_k
+    vc[length] = new_v
+    pg = length // page
+    if length % page == 0:
+        kmin[:, pg] = new_k
+        kmax[:, pg] = new_k
+    else:
+        kmin[:, pg] = np.minimum(kmin[:, pg], new_k)
+        kmax[:, pg] = np.maximum(kmax[:, pg], new_k)
+    return length + 1
+
+
+def default_scale(head_dim: int) -> float:
+    """1 / sqrt(d) (reading R13)."""
+    return 1.0 / math.sqrt(head_dim)
