@@ -1,0 +1,182 @@
+/*
+ * rkv.h -- C ABI of the RocketKV hot path on GB300 (sm_103a): SnapKV++ prefill eviction and
+ * hybrid sparse decode attention, plus a dense decode used as the full-KV timing reference.
+ *
+ * The method is described in "RocketKV: Accelerating Long-Context LLM Inference via Two-Stage KV
+ * Cache Compression" (Behnam et al., arXiv 2502.14051). Sections cited below are those of the
+ * authors' OpenReview responses on paperhub.cn (same title), which hold the method's details:
+ *   [LAT]   "Lack of Direct Latency Comparison"           -- token budget split half / half
+ *   [APPROX]"Explanation of Calculating Approximate Attention Scores" -- pages, Kmin/Kmax,
+ *                                                             top-|q| channels, GQA group sums
+ *   [PAGE]  "Is Page Always Divided Into 4?"              -- ratio decomposition, page size
+ *   [EVICT] "Is Needle Among Evicted Tokens"              -- eviction per head and per layer
+ *   [KSIZE] "Potential Sensitivity to Kernel Size in SnapKV++" -- adaptive pooling size
+ *   [STEP]  "Are Different KV Tokens Retrieved at Each Decoding Step?" -- selection per step
+ *   [SNAP++]"Novelty of SnapKV++"                          -- GQA-aware SnapKV scoring
+ * and [KEYPTS] = "Key points" of the summarizepaper.com summary (full-KV baseline, SnapKV++).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every tensor pointer is DEVICE memory owned by the caller. The library allocates nothing
+ *    and keeps no state between calls. bf16 tensors are passed as void* and must be 16-byte
+ *    aligned. All integer tensors are int32.
+ *  - n counts independent problems (batch x layers flattened; "unit" below = one of the n).
+ *    Query heads of unit u: Hq = n_kv * gqa, query head h belongs to KV head h / gqa.
+ *  - head_dim must be 128 (RKV_ERR_UNSUPPORTED otherwise).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL = legacy
+ *    default stream). Arguments are validated on the host before any launch; an invalid
+ *    argument returns RKV_ERR_INVALID_ARG / RKV_ERR_UNSUPPORTED / RKV_ERR_WORKSPACE and launches
+ *    nothing. A failed launch returns RKV_ERR_CUDA.
+ *  - ws / ws_bytes: scratch owned by the caller, at least the size the matching
+ *    *_workspace_bytes() returns. Its first 256 bytes hold a device status word that kernels set
+ *    when they detect an inconsistency in device-resident data (e.g. a length beyond capacity,
+ *    a bounded wait that ran out). It must be zero before first use (allocate it zeroed).
+ *    rkv_check_status() synchronises the stream, reads and clears it. Kernels never trap.
+ *  - Two calls that share one workspace must not overlap on the GPU (same stream is fine).
+ */
+#ifndef RKV_H_
+#define RKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RKV_OK = 0,
+  RKV_ERR_INVALID_ARG = 1,
+  RKV_ERR_UNSUPPORTED = 2,
+  RKV_ERR_WORKSPACE = 3,
+  RKV_ERR_CUDA = 4,
+  RKV_ERR_DEVICE_STATUS = 5
+} rkv_status;
+
+/* Device status bits (reported by rkv_check_status through *bits). */
+#define RKV_DEV_LEN_OVER_CAP   0x1u  /* a length exceeds cap / page_cap (work for it skipped) */
+#define RKV_DEV_BAD_WINDOW     0x2u  /* a sequence shorter than the window (unit skipped)     */
+#define RKV_DEV_WAIT_TIMEOUT   0x4u  /* a bounded mbarrier wait ran out (unit abandoned)      */
+#define RKV_DEV_SELECT_FAILED  0x8u  /* a top-k selection produced the wrong count            */
+
+/* Human-readable name of a status code (static string). */
+const char* rkv_status_string(rkv_status s);
+
+/* Synchronise `stream`, read the device status word in `ws`, clear it, and return RKV_OK if it
+ * was zero or RKV_ERR_DEVICE_STATUS otherwise (bits in *bits when bits != NULL). */
+rkv_status rkv_check_status(void* ws, void* stream, uint32_t* bits);
+
+/* Pure host planner ([PAGE], [LAT], [KSIZE]). The overall ratio ctx / budget is split between
+ * the two stages, and stage 2's share between the sequence dimension (page) and the head
+ * dimension (head_dim / channels). page = 0 picks 4 and channels = 0 picks head_dim / 4; the
+ * stage-1 keep is then min(ctx, budget * page * head_dim / channels), which makes the
+ * approximation read exactly as many bytes as budget / 2 tokens of K and V. kernel_size: 7 for
+ * ctx <= 8192, 15 for ctx <= 32768, else 31 (larger pooling for longer prompts). Any output
+ * pointer may be NULL. Errors: RKV_ERR_INVALID_ARG for non-positive sizes, channels > head_dim,
+ * budget odd or budget / 2 < page. */
+rkv_status rkv_plan(int ctx, int budget, int head_dim, int page, int channels,
+                    int* keep, int* page_out, int* channels_out, int* kernel_size);
+
+/* ------------------------------------------------------------------------------------------ */
+/* Stage 1: SnapKV++ eviction ([SNAP++], [EVICT], [KSIZE], [KEYPTS])                            */
+/* ------------------------------------------------------------------------------------------ */
+size_t rkv_snapkv_workspace_bytes(int n, int n_kv, int gqa, int max_len, int window);
+
+/* For each unit u and KV head g: score every prefix position i < L_u - window with the window
+ * queries -- softmax(q . k / sqrt-scale) over all keys visible to each window query (the prefix
+ * plus the causal part of the window), summed over the window and over the gqa query heads of
+ * the group -- max-pool the scores with an odd kernel (stride 1, same length, clipped ends), keep
+ * the keep - window highest (ties -> lower position) and append the window, then gather those
+ * rows of K and V into the compact cache.
+ *   k, v      [n][n_kv][max_len][128] bf16, rows >= L_u ignored
+ *   seq_lens  [n] int32 on device, window <= L_u <= max_len
+ *   q_win     [n][n_kv*gqa][window][128] bf16 -- the last `window` queries of every head
+ *   window    1 <= window, gqa * window <= 256
+ *   kernel_size odd >= 1, or 0 to pick it per sequence from L_u (7 / 15 / 31 as rkv_plan)
+ *   keep      tokens kept per (unit, KV head) including the window; window < keep <= cap.
+ *             A sequence with L_u <= keep keeps all L_u tokens.
+ *   scale     logit scale (1/sqrt(128) for the usual attention)
+ *   k_out, v_out [n][n_kv][cap][128] bf16: rows 0 .. out_len[u]-1 written (kept positions in
+ *             ascending order, the window last)
+ *   kept_idx  [n][n_kv][keep] int32: original positions of the kept rows; -1 past out_len[u]
+ *   out_len   [n] int32: min(L_u, keep)
+ *   scores_out NULL or [n][n_kv][max_len - window] fp32: the un-pooled prefix scores
+ */
+rkv_status rkv_snapkv_compress(const void* k, const void* v, const int32_t* seq_lens,
+                               const void* q_win, int n, int n_kv, int gqa, int head_dim,
+                               int max_len, int window, int kernel_size, int keep, float scale,
+                               void* k_out, void* v_out, int cap, int32_t* kept_idx,
+                               int32_t* out_len, float* scores_out, void* ws, size_t ws_bytes,
+                               void* stream);
+
+/* ------------------------------------------------------------------------------------------ */
+/* Stage 2: page summaries ([APPROX])                                                          */
+/* ------------------------------------------------------------------------------------------ */
+size_t rkv_summaries_workspace_bytes(void);
+
+/* Element-wise min and max of K over pages of `page` consecutive cache rows, stored
+ * channel-major so that one channel of all pages is one contiguous row:
+ *   k_cache [n][n_kv][cap][128] bf16, len [n] int32 (device)
+ *   kmin, kmax [n][n_kv][128][page_cap] bf16; page p of unit u covers rows p*page ..
+ *   min(len_u, (p+1)*page) - 1 (a partial last page uses its valid rows only).
+ *   Pages from first_token / page up to the last page are (re)computed; first_token = 0
+ *   rebuilds everything. page is a power of two <= 64; page_cap is a multiple of 8 and
+ *   page_cap * page >= the largest len (checked on device: RKV_DEV_LEN_OVER_CAP).
+ */
+rkv_status rkv_build_page_summaries(const void* k_cache, const int32_t* len, int n, int n_kv,
+                                    int head_dim, int cap, int page, int page_cap,
+                                    int first_token, void* kmin, void* kmax, void* ws,
+                                    size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------------ */
+/* Stage 2: hybrid sparse decode ([APPROX], [LAT], [STEP], [PAGE])                              */
+/* ------------------------------------------------------------------------------------------ */
+size_t rkv_hybrid_decode_workspace_bytes(int n, int n_kv, int gqa, int page_cap, int budget,
+                                         int page);
+
+/* One decode step. If new_k / new_v are given, token len_u is first appended to every KV head
+ * of unit u (cache rows and the page summary it lands in) and len[u] is incremented; the new
+ * token can be selected in this step. Then, per (unit, KV head g):
+ *   len_u <= budget: exact attention over every cached token;
+ *   otherwise: the `channels` channels with the largest sum over the group of |q_h| (ties ->
+ *   lower channel) are kept; with q_g = sum_h q_h, each page scores
+ *   sum_{kept i} q_g[i] * (q_g[i] >= 0 ? Kmax[i][page] : Kmin[i][page]) (unscaled); the
+ *   (budget/2)/page best pages (ties -> lower page) are selected and all gqa query heads attend
+ *   exactly over their valid tokens.
+ *   q        [n][n_kv*gqa][128] bf16
+ *   new_k, new_v NULL (no append) or [n][n_kv][128] bf16
+ *   k_cache, v_cache [n][n_kv][cap][128] bf16; len [n] int32 (device)
+ *   kmin, kmax [n][n_kv][128][page_cap] bf16, as built by rkv_build_page_summaries
+ *   budget    even, budget/2 >= page; page a power of two <= 64; 1 <= channels <= 128
+ *   gqa       1, 2, 4 or 8
+ *   out       [n][n_kv*gqa][128] bf16
+ *   sel_channels NULL or [n][n_kv][channels] int32 (ascending; -1 on the dense path)
+ *   sel_pages NULL or [n][n_kv][(budget/2)/page] int32 (ascending; -1 where unused)
+ *   approx_scores NULL or [n][n_kv][page_cap] fp32 (pages >= ceil(len_u/page) untouched)
+ */
+rkv_status rkv_hybrid_decode(const void* q, const void* new_k, const void* new_v,
+                             void* k_cache, void* v_cache, int32_t* len, void* kmin, void* kmax,
+                             int n, int n_kv, int gqa, int head_dim, int cap, int page_cap,
+                             int budget, int page, int channels, float scale, void* out,
+                             int32_t* sel_channels, int32_t* sel_pages, float* approx_scores,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------------ */
+/* Full-KV decode attention, the baseline the method is compared against ([KEYPTS])            */
+/* ------------------------------------------------------------------------------------------ */
+size_t rkv_dense_decode_workspace_bytes(int n, int n_kv, int gqa, int max_len);
+
+/* out[u][h] = softmax(scale * q[u][h] . K[u][g]^T) V[u][g] over the len_u cached tokens
+ * (g = h / gqa), split over the sequence across thread blocks and merged.
+ *   q [n][n_kv*gqa][128] bf16; k, v [n][n_kv][max_len][128] bf16; len [n] int32 (device,
+ *   1 <= len_u <= max_len); out [n][n_kv*gqa][128] bf16; gqa 1, 2, 4 or 8.
+ */
+rkv_status rkv_dense_decode(const void* q, const void* k, const void* v, const int32_t* len,
+                            int n, int n_kv, int gqa, int head_dim, int max_len, float scale,
+                            void* out, void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RKV_H_ */

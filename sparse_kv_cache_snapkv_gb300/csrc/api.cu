@@ -1,0 +1,276 @@
+// C ABI of the RocketKV library: argument validation, workspace carving, kernel launches.
+// Declarations and the contract of every entry point are in include/rkv.h.
+#include <cuda_runtime.h>
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/rkv.h"
+#include "rkv_internal.h"
+
+using namespace rkv;
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+inline uint32_t* status_ptr(void* ws) { return reinterpret_cast<uint32_t*>(ws); }
+inline rkv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA; }
+inline bool gqa_ok(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace
+
+extern "C" {
+
+const char* rkv_status_string(rkv_status s) {
+  switch (s) {
+    case RKV_OK: return "ok";
+    case RKV_ERR_INVALID_ARG: return "invalid argument";
+    case RKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case RKV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case RKV_ERR_CUDA: return "CUDA launch or runtime error";
+    case RKV_ERR_DEVICE_STATUS: return "kernel reported inconsistent device data";
+  }
+  return "unknown status";
+}
+
+rkv_status rkv_check_status(void* ws, void* stream, uint32_t* bits) {
+  if (!ws) return RKV_ERR_INVALID_ARG;
+  cudaStream_t s = as_stream(stream);
+  uint32_t h = 0;
+  cudaError_t e = cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return RKV_ERR_CUDA;
+  if (bits) *bits = h;
+  if (h == 0) return RKV_OK;
+  e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e == cudaSuccess ? RKV_ERR_DEVICE_STATUS : RKV_ERR_CUDA;
+}
+
+rkv_status rkv_plan(int ctx, int budget, int head_dim, int page, int channels, int* keep,
+                    int* page_out, int* channels_out, int* kernel_size) {
+  if (ctx <= 0 || budget <= 0 || head_dim <= 0 || page < 0 || channels < 0)
+    return RKV_ERR_INVALID_ARG;
+  if (page == 0) page = 4;
+  if (channels == 0) channels = head_dim / 4;
+  if (channels < 1 || channels > head_dim || budget % 2 != 0 || budget / 2 < page)
+    return RKV_ERR_INVALID_ARG;
+  const long long want = (long long)budget * page * head_dim / channels;
+  if (keep) *keep = (int)(want < ctx ? want : ctx);
+  if (page_out) *page_out = page;
+  if (channels_out) *channels_out = channels;
+  if (kernel_size) *kernel_size = ctx <= 8192 ? 7 : (ctx <= 32768 ? 15 : 31);
+  return RKV_OK;
+}
+
+// ------------------------------------------------------------------------------- stage 1
+size_t rkv_snapkv_workspace_bytes(int n, int n_kv, int gqa, int max_len, int window) {
+  if (n <= 0 || n_kv <= 0 || gqa <= 0 || max_len <= window || window <= 0) return 0;
+  return kStatusBytes + snapkv_scratch_bytes(n, n_kv, gqa, max_len, window);
+}
+
+rkv_status rkv_snapkv_compress(const void* k, const void* v, const int32_t* seq_lens,
+                               const void* q_win, int n, int n_kv, int gqa, int head_dim,
+                               int max_len, int window, int kernel_size, int keep, float scale,
+                               void* k_out, void* v_out, int cap, int32_t* kept_idx,
+                               int32_t* out_len, float* scores_out, void* ws, size_t ws_bytes,
+                               void* stream) {
+  if (head_dim != kHeadDim) return RKV_ERR_UNSUPPORTED;
+  if (!k || !v || !seq_lens || !q_win || !k_out || !v_out || !kept_idx || !out_len)
+    return RKV_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(q_win) || !aligned16(k_out) ||
+      !aligned16(v_out) || (scores_out && !aligned16(scores_out)))
+    return RKV_ERR_INVALID_ARG;
+  if (n <= 0 || n_kv <= 0 || gqa <= 0 || window <= 0 || max_len <= window || keep <= window ||
+      keep > cap || cap <= 0 || !(scale > 0.f) || !std::isfinite(scale))
+    return RKV_ERR_INVALID_ARG;
+  if (kernel_size < 0 || (kernel_size > 0 && kernel_size % 2 == 0)) return RKV_ERR_INVALID_ARG;
+  if (gqa * window > 256) return RKV_ERR_UNSUPPORTED;
+  const size_t need = rkv_snapkv_workspace_bytes(n, n_kv, gqa, max_len, window);
+  if (!ws || !aligned16(ws) || ws_bytes < need) return RKV_ERR_WORKSPACE;
+
+  SnapArgs a{};
+  a.k = static_cast<const bf16*>(k);
+  a.v = static_cast<const bf16*>(v);
+  a.seq_lens = seq_lens;
+  a.q_win = static_cast<const bf16*>(q_win);
+  a.n = n;
+  a.n_kv = n_kv;
+  a.gqa = gqa;
+  a.max_len = max_len;
+  a.window = window;
+  a.kernel_size = kernel_size;
+  a.keep = keep;
+  a.cap = cap;
+  a.scale_log2 = scale * kLog2e;
+  a.k_out = static_cast<bf16*>(k_out);
+  a.v_out = static_cast<bf16*>(v_out);
+  a.kept_idx = kept_idx;
+  a.out_len = out_len;
+  snapkv_plan(n, n_kv, gqa, max_len, window, &a.nsplit, &a.tokens_per_split, &a.rows_pad);
+  // workspace carve: [status][pooled][scores (if not given)][split partials]
+  unsigned char* p = static_cast<unsigned char*>(ws) + kStatusBytes;
+  const size_t plen = align_up((size_t)n * n_kv * (max_len - window) * 4, 256);
+  a.pooled = reinterpret_cast<float*>(p);
+  p += plen;
+  if (scores_out) {
+    a.scores = scores_out;
+  } else {
+    a.scores = reinterpret_cast<float*>(p);
+  }
+  p += plen;
+  a.part_ml = reinterpret_cast<float*>(p);
+  a.status = status_ptr(ws);
+  return from_cuda(launch_snapkv(a, as_stream(stream)));
+}
+
+// ------------------------------------------------------------------------------- summaries
+size_t rkv_summaries_workspace_bytes(void) { return kStatusBytes; }
+
+rkv_status rkv_build_page_summaries(const void* k_cache, const int32_t* len, int n, int n_kv,
+                                    int head_dim, int cap, int page, int page_cap,
+                                    int first_token, void* kmin, void* kmax, void* ws,
+                                    size_t ws_bytes, void* stream) {
+  if (head_dim != kHeadDim) return RKV_ERR_UNSUPPORTED;
+  if (!k_cache || !len || !kmin || !kmax) return RKV_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(kmin) || !aligned16(kmax)) return RKV_ERR_INVALID_ARG;
+  if (n <= 0 || n_kv <= 0 || cap <= 0 || !pow2(page) || page > 64 || page_cap <= 0 ||
+      page_cap % 8 != 0 || first_token < 0)
+    return RKV_ERR_INVALID_ARG;
+  if (!ws || !aligned16(ws) || ws_bytes < kStatusBytes) return RKV_ERR_WORKSPACE;
+  SummaryArgs a{};
+  a.k_cache = static_cast<const bf16*>(k_cache);
+  a.len = len;
+  a.kmin = static_cast<bf16*>(kmin);
+  a.kmax = static_cast<bf16*>(kmax);
+  a.n = n;
+  a.n_kv = n_kv;
+  a.cap = cap;
+  a.page = page;
+  a.page_cap = page_cap;
+  a.first_token = first_token;
+  a.status = status_ptr(ws);
+  return from_cuda(launch_summaries(a, as_stream(stream)));
+}
+
+// ------------------------------------------------------------------------------- hybrid
+size_t rkv_hybrid_decode_workspace_bytes(int n, int n_kv, int gqa, int page_cap, int budget,
+                                         int page) {
+  (void)n;
+  (void)n_kv;
+  (void)gqa;
+  (void)page_cap;
+  (void)budget;
+  (void)page;
+  return kStatusBytes;
+}
+
+rkv_status rkv_hybrid_decode(const void* q, const void* new_k, const void* new_v,
+                             void* k_cache, void* v_cache, int32_t* len, void* kmin, void* kmax,
+                             int n, int n_kv, int gqa, int head_dim, int cap, int page_cap,
+                             int budget, int page, int channels, float scale, void* out,
+                             int32_t* sel_channels, int32_t* sel_pages, float* approx_scores,
+                             void* ws, size_t ws_bytes, void* stream) {
+  if (head_dim != kHeadDim) return RKV_ERR_UNSUPPORTED;
+  if (!gqa_ok(gqa)) return RKV_ERR_UNSUPPORTED;
+  if (!q || !k_cache || !v_cache || !len || !kmin || !kmax || !out) return RKV_ERR_INVALID_ARG;
+  if ((new_k == nullptr) != (new_v == nullptr)) return RKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(kmin) ||
+      !aligned16(kmax) || !aligned16(out))
+    return RKV_ERR_INVALID_ARG;
+  if (n <= 0 || n_kv <= 0 || cap <= 0 || page_cap <= 0 || page_cap % 8 != 0 || !pow2(page) ||
+      page > 64 || budget <= 0 || budget % 2 != 0 || budget / 2 < page || channels < 1 ||
+      channels > kHeadDim || !(scale > 0.f) || !std::isfinite(scale))
+    return RKV_ERR_INVALID_ARG;
+  const size_t smem = hybrid_smem_bytes(gqa, page_cap, budget, page);
+  if (smem > 200 * 1024) return RKV_ERR_UNSUPPORTED;
+  if (!ws || !aligned16(ws) ||
+      ws_bytes < rkv_hybrid_decode_workspace_bytes(n, n_kv, gqa, page_cap, budget, page))
+    return RKV_ERR_WORKSPACE;
+  cudaStream_t s = as_stream(stream);
+  if (new_k) {
+    AppendArgs ap{};
+    ap.new_k = static_cast<const bf16*>(new_k);
+    ap.new_v = static_cast<const bf16*>(new_v);
+    ap.k_cache = static_cast<bf16*>(k_cache);
+    ap.v_cache = static_cast<bf16*>(v_cache);
+    ap.len = len;
+    ap.kmin = static_cast<bf16*>(kmin);
+    ap.kmax = static_cast<bf16*>(kmax);
+    ap.n = n;
+    ap.n_kv = n_kv;
+    ap.cap = cap;
+    ap.page_cap = page_cap;
+    ap.page = page;
+    ap.status = status_ptr(ws);
+    cudaError_t e = launch_append(ap, s);
+    if (e != cudaSuccess) return RKV_ERR_CUDA;
+  }
+  HybridArgs a{};
+  a.q = static_cast<const bf16*>(q);
+  a.k_cache = static_cast<const bf16*>(k_cache);
+  a.v_cache = static_cast<const bf16*>(v_cache);
+  a.len = len;
+  a.kmin = static_cast<const bf16*>(kmin);
+  a.kmax = static_cast<const bf16*>(kmax);
+  a.n = n;
+  a.n_kv = n_kv;
+  a.gqa = gqa;
+  a.cap = cap;
+  a.page_cap = page_cap;
+  a.budget = budget;
+  a.page = page;
+  a.channels = channels;
+  a.scale_log2 = scale * kLog2e;
+  a.out = static_cast<bf16*>(out);
+  a.sel_channels = sel_channels;
+  a.sel_pages = sel_pages;
+  a.approx = approx_scores;
+  a.status = status_ptr(ws);
+  return from_cuda(launch_hybrid(a, s));
+}
+
+// ------------------------------------------------------------------------------- dense
+size_t rkv_dense_decode_workspace_bytes(int n, int n_kv, int gqa, int max_len) {
+  if (n <= 0 || n_kv <= 0 || gqa <= 0 || max_len <= 0) return 0;
+  return kStatusBytes + dense_partials_bytes(n, n_kv, gqa, max_len);
+}
+
+rkv_status rkv_dense_decode(const void* q, const void* k, const void* v, const int32_t* len,
+                            int n, int n_kv, int gqa, int head_dim, int max_len, float scale,
+                            void* out, void* ws, size_t ws_bytes, void* stream) {
+  if (head_dim != kHeadDim) return RKV_ERR_UNSUPPORTED;
+  if (!gqa_ok(gqa)) return RKV_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !len || !out) return RKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return RKV_ERR_INVALID_ARG;
+  if (n <= 0 || n_kv <= 0 || max_len <= 0 || !(scale > 0.f) || !std::isfinite(scale))
+    return RKV_ERR_INVALID_ARG;
+  const size_t need = rkv_dense_decode_workspace_bytes(n, n_kv, gqa, max_len);
+  if (!ws || !aligned16(ws) || ws_bytes < need) return RKV_ERR_WORKSPACE;
+  DenseArgs a{};
+  a.q = static_cast<const bf16*>(q);
+  a.k = static_cast<const bf16*>(k);
+  a.v = static_cast<const bf16*>(v);
+  a.len = len;
+  a.n = n;
+  a.n_kv = n_kv;
+  a.gqa = gqa;
+  a.max_len = max_len;
+  dense_plan(n, n_kv, max_len, &a.nsplit, &a.tokens_per_split);
+  a.scale_log2 = scale * kLog2e;
+  const size_t rows = (size_t)n * n_kv * gqa * a.nsplit;
+  unsigned char* p = static_cast<unsigned char*>(ws) + kStatusBytes;
+  a.part_m = reinterpret_cast<float*>(p);
+  p += align_up(rows * 4, 256);
+  a.part_l = reinterpret_cast<float*>(p);
+  p += align_up(rows * 4, 256);
+  a.part_o = reinterpret_cast<float*>(p);
+  a.out = static_cast<bf16*>(out);
+  a.status = status_ptr(ws);
+  return from_cuda(launch_dense(a, as_stream(stream)));
+}
+
+}  // extern "C"

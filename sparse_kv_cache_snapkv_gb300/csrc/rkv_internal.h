@@ -1,0 +1,107 @@
+// Internal launch interface between the C ABI (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace rkv {
+
+constexpr int kHeadDim = 128;
+constexpr size_t kStatusBytes = 256;     // device status word + padding at the start of ws
+constexpr int kDecodeThreads = 256;      // 8 warps per decode CTA
+constexpr int kChunkTokens = 64;         // tokens per shared-memory stage in decode attention
+constexpr int kStages = 3;               // stages in flight per decode CTA
+
+typedef __nv_bfloat16 bf16;
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------- decode side
+struct HybridArgs {
+  const bf16* q;
+  const bf16* k_cache;
+  const bf16* v_cache;
+  const int32_t* len;
+  const bf16* kmin;
+  const bf16* kmax;
+  int n, n_kv, gqa, cap, page_cap, budget, page, channels;
+  float scale_log2;  // scale * log2(e)
+  bf16* out;
+  int32_t* sel_channels;
+  int32_t* sel_pages;
+  float* approx;
+  uint32_t* status;
+};
+
+struct AppendArgs {
+  const bf16* new_k;
+  const bf16* new_v;
+  bf16* k_cache;
+  bf16* v_cache;
+  int32_t* len;
+  bf16* kmin;
+  bf16* kmax;
+  int n, n_kv, cap, page_cap, page;
+  uint32_t* status;
+};
+
+struct SummaryArgs {
+  const bf16* k_cache;
+  const int32_t* len;
+  bf16* kmin;
+  bf16* kmax;
+  int n, n_kv, cap, page, page_cap, first_token;
+  uint32_t* status;
+};
+
+struct DenseArgs {
+  const bf16* q;
+  const bf16* k;
+  const bf16* v;
+  const int32_t* len;
+  int n, n_kv, gqa, max_len, nsplit, tokens_per_split;
+  float scale_log2;
+  float* part_m;  // [n*Hq][nsplit]
+  float* part_l;  // [n*Hq][nsplit]
+  float* part_o;  // [n*Hq][nsplit][128]
+  bf16* out;
+  uint32_t* status;
+};
+
+// split plan for dense decode, shared by the workspace query and the launch
+void dense_plan(int n, int n_kv, int max_len, int* nsplit, int* tokens_per_split);
+size_t dense_partials_bytes(int n, int n_kv, int gqa, int max_len);
+
+size_t hybrid_smem_bytes(int gqa, int page_cap, int budget, int page);
+cudaError_t launch_hybrid(const HybridArgs& a, cudaStream_t s);
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+cudaError_t launch_summaries(const SummaryArgs& a, cudaStream_t s);
+cudaError_t launch_dense(const DenseArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------------------- prefill side
+struct SnapArgs {
+  const bf16* k;
+  const bf16* v;
+  const int32_t* seq_lens;
+  const bf16* q_win;
+  int n, n_kv, gqa, max_len, window, kernel_size, keep, cap;
+  float scale_log2;
+  bf16* k_out;
+  bf16* v_out;
+  int32_t* kept_idx;
+  int32_t* out_len;
+  float* scores;       // [n][n_kv][max_len - window] (caller's buffer or workspace)
+  float* pooled;       // workspace, same shape
+  float* part_ml;      // workspace: [n*n_kv][nsplit][rows_pad][2] (max, sum) per split
+  int nsplit, tokens_per_split, rows_pad;
+  uint32_t* status;
+};
+
+void snapkv_plan(int n, int n_kv, int gqa, int max_len, int window, int* nsplit,
+                 int* tokens_per_split, int* rows_pad);
+size_t snapkv_scratch_bytes(int n, int n_kv, int gqa, int max_len, int window);
+cudaError_t launch_snapkv(const SnapArgs& a, cudaStream_t s);
+
+}  // namespace rkv

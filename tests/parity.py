@@ -1,0 +1,54 @@
+"""GPU-vs-oracle acceptance rules shared by the parity tests.
+
+* Index sets (kept tokens, channels, pages): equal to the oracle's, except that elements whose
+  oracle key lies within the tie band around the k-th key, |s_i - s_k| <= 1e-4 * |s_k|, may be
+  exchanged for one another.
+* Approximate page scores: |gpu - ref| <= 1e-3 * max(|ref|, sum_i |q_g[i] * K_sel[i]|).
+* Attention outputs (bf16): |gpu - ref| <= 2e-3 + 1e-2 * |ref|, ref in float64 over the GPU's
+  own selection when that differs from the oracle's inside the tie band.
+"""
+import numpy as np
+
+BAND_REL = 1e-4
+APPROX_REL = 1e-3
+OUT_ABS = 2e-3
+OUT_REL = 1e-2
+
+
+def check_selection(gpu_sel, keys, k, what="selection"):
+    """gpu_sel: selected indices (any order); keys: oracle fp64 keys; k: number selected."""
+    gpu = np.sort(np.asarray(gpu_sel, dtype=np.int64))
+    assert gpu.shape[0] == k, f"{what}: {gpu.shape[0]} selected, expected {k}"
+    assert np.unique(gpu).shape[0] == k, f"{what}: duplicate indices"
+    assert gpu.min() >= 0 and gpu.max() < keys.shape[0], f"{what}: index out of range"
+    order = np.lexsort((np.arange(keys.shape[0]), -keys))
+    ref = np.sort(order[:k])
+    if np.array_equal(gpu, ref):
+        return 0
+    sk = keys[order[k - 1]]
+    band = BAND_REL * abs(sk)
+    must = np.nonzero(keys > sk + band)[0]
+    never = np.nonzero(keys < sk - band)[0]
+    gset = set(gpu.tolist())
+    missing = [i for i in must if i not in gset]
+    extra = [i for i in never if i in gset]
+    assert not missing and not extra, (
+        f"{what}: outside the tie band: missing {missing[:8]} (keys {keys[missing[:8]]}), "
+        f"extra {extra[:8]} (keys {keys[extra[:8]]}), k-th key {sk}")
+    return len(set(ref.tolist()) ^ gset) // 2
+
+
+def check_output(gpu_out, ref_out, what="output"):
+    gpu = np.asarray(gpu_out, dtype=np.float64)
+    err = np.abs(gpu - ref_out)
+    tol = OUT_ABS + OUT_REL * np.abs(ref_out)
+    bad = err > tol
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside tolerance; worst err "
+                           f"{err.max():.3e} at ref {ref_out.flat[np.argmax(err - tol)]:.4f}")
+
+
+def check_approx(gpu_scores, ref_scores, magnitude, what="approx scores"):
+    err = np.abs(np.asarray(gpu_scores, dtype=np.float64) - ref_scores)
+    tol = APPROX_REL * np.maximum(np.abs(ref_scores), magnitude)
+    bad = err > tol
+    assert not bad.any(), f"{what}: {bad.sum()} outside tolerance; worst {err.max():.3e}"

@@ -1,0 +1,114 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports every symbol that
+include/rkv.h declares; the planner matches the oracle; invalid arguments are rejected on the host
+before any launch. No GPU needed."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle import rocketkv as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_kv_cache_snapkv_gb300 import _build, rkv
+    _build.build()
+    return rkv.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "rkv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(rkv_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 11
+    for name in names:
+        assert hasattr(lib, name), name
+    from sparse_kv_cache_snapkv_gb300 import rkv
+    assert set(rkv.SYMBOLS) <= set(names)
+
+
+@pytest.mark.parametrize("ctx", [300, 4096, 8192, 32768, 50000, 131072])
+@pytest.mark.parametrize("budget", [256, 512, 1024, 4096])
+def test_plan_matches_oracle(lib, ctx, budget):
+    from sparse_kv_cache_snapkv_gb300 import rkv
+    assert rkv.rkv_plan(ctx, budget) == O.plan(ctx, budget, 128)
+    assert rkv.rkv_plan(ctx, budget, 128, 16, 128) == O.plan(ctx, budget, 128, 16, 128)
+
+
+def test_plan_rejects(lib):
+    out = [ctypes.c_int() for _ in range(4)]
+    refs = [ctypes.byref(o) for o in out]
+    assert lib.rkv_plan(4096, 255, 128, 0, 0, *refs) == 1      # odd budget
+    assert lib.rkv_plan(4096, 256, 128, 0, 129, *refs) == 1    # channels > d
+    assert lib.rkv_plan(0, 256, 128, 0, 0, *refs) == 1
+    assert lib.rkv_plan(4096, 4, 128, 4, 0, *refs) == 1        # budget / 2 < page
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.rkv_status_string(code)
+
+
+FAKE = ctypes.c_void_p(1 << 20)   # aligned, non-null, never dereferenced: calls fail validation
+
+
+def test_validation_rejects_before_launch(lib):
+    vp = FAKE
+    # hybrid: unsupported head_dim, gqa, bad page, odd budget, null pointer, small workspace
+    common = (vp, None, None, vp, vp, vp, vp, vp)
+    assert lib.rkv_hybrid_decode(*common, 1, 1, 4, 64, 64, 16, 256, 4, 32, 0.1, vp, None, None,
+                                 None, vp, 256, None) == 2
+    assert lib.rkv_hybrid_decode(*common, 1, 1, 3, 128, 64, 16, 256, 4, 32, 0.1, vp, None, None,
+                                 None, vp, 256, None) == 2
+    assert lib.rkv_hybrid_decode(*common, 1, 1, 4, 128, 64, 16, 256, 3, 32, 0.1, vp, None, None,
+                                 None, vp, 256, None) == 1
+    assert lib.rkv_hybrid_decode(*common, 1, 1, 4, 128, 64, 16, 255, 4, 32, 0.1, vp, None, None,
+                                 None, vp, 256, None) == 1
+    assert lib.rkv_hybrid_decode(*common, 1, 1, 4, 128, 64, 12, 256, 4, 32, 0.1, vp, None, None,
+                                 None, vp, 256, None) == 1                      # page_cap % 8
+    assert lib.rkv_hybrid_decode(None, None, None, vp, vp, vp, vp, vp, 1, 1, 4, 128, 64, 16, 256,
+                                 4, 32, 0.1, vp, None, None, None, vp, 256, None) == 1
+    assert lib.rkv_hybrid_decode(*common, 1, 1, 4, 128, 64, 16, 256, 4, 32, 0.1, vp, None, None,
+                                 None, vp, 8, None) == 3
+    assert lib.rkv_hybrid_decode(vp, vp, None, vp, vp, vp, vp, vp, 1, 1, 4, 128, 64, 16, 256, 4,
+                                 32, 0.1, vp, None, None, None, vp, 256, None) == 1  # new_v missing
+    misaligned = ctypes.c_void_p((1 << 20) + 8)
+    assert lib.rkv_hybrid_decode(misaligned, None, None, vp, vp, vp, vp, vp, 1, 1, 4, 128, 64, 16,
+                                 256, 4, 32, 0.1, vp, None, None, None, vp, 256, None) == 1
+    # dense
+    assert lib.rkv_dense_decode(vp, vp, vp, vp, 1, 1, 4, 128, 100, 0.1, vp, vp, 16, None) == 3
+    assert lib.rkv_dense_decode(vp, vp, vp, vp, 1, 1, 4, 128, 100, -1.0, vp, vp, 1 << 20,
+                                None) == 1
+    # summaries
+    assert lib.rkv_build_page_summaries(vp, vp, 1, 1, 128, 64, 3, 16, 0, vp, vp, vp, 256,
+                                        None) == 1
+    assert lib.rkv_build_page_summaries(vp, vp, 1, 1, 128, 64, 4, 16, 0, vp, vp, vp, 4,
+                                        None) == 3
+    # snapkv: even kernel, keep <= window, gqa * window > 256, small workspace
+    args = (vp, vp, vp, vp, 1, 2, 4, 128, 4096, 32)
+    assert lib.rkv_snapkv_compress(*args, 6, 256, 0.1, vp, vp, 256, vp, vp, None, vp, 1 << 30,
+                                   None) == 1
+    assert lib.rkv_snapkv_compress(*args, 7, 32, 0.1, vp, vp, 256, vp, vp, None, vp, 1 << 30,
+                                   None) == 1
+    assert lib.rkv_snapkv_compress(*args, 7, 512, 0.1, vp, vp, 256, vp, vp, None, vp, 1 << 30,
+                                   None) == 1                                  # keep > cap
+    assert lib.rkv_snapkv_compress(vp, vp, vp, vp, 1, 2, 16, 128, 4096, 32, 7, 256, 0.1, vp, vp,
+                                   256, vp, vp, None, vp, 1 << 30, None) == 2
+    assert lib.rkv_snapkv_compress(*args, 7, 256, 0.1, vp, vp, 256, vp, vp, None, vp, 64,
+                                   None) == 3
+
+
+def test_workspace_sizes_monotone(lib):
+    a = lib.rkv_dense_decode_workspace_bytes(32, 8, 4, 32768)
+    b = lib.rkv_dense_decode_workspace_bytes(32, 8, 4, 131072)
+    assert 256 < a <= b
+    assert lib.rkv_snapkv_workspace_bytes(1, 8, 4, 131072, 64) > \
+        lib.rkv_snapkv_workspace_bytes(1, 8, 4, 4096, 32)
+    assert lib.rkv_hybrid_decode_workspace_bytes(32, 8, 4, 1024, 256, 4) >= 256

@@ -1,0 +1,278 @@
+"""Parity of the stage-2 kernels (page summaries, hybrid decode, append, dense decode) against
+the CPU oracle, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import rocketkv as O
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+
+
+def _lib():
+    from sparse_kv_cache_snapkv_gb300 import rkv
+    rkv.load()
+    return rkv
+
+
+def _f64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def _page_cap(cap, page):
+    return ((cap + page - 1) // page + 7) // 8 * 8
+
+
+def _make_cache(n, n_kv, cap, lens, seed):
+    from sparse_kv_cache_snapkv_gb300 import synthetic as S
+    k, v = S.random_cache(n, n_kv, cap, D, seed)
+    for u, L in enumerate(lens):
+        k[u, :, L:] = 0
+        v[u, :, L:] = 0
+    return k.cuda(), v.cuda()
+
+
+def _summaries(rkv, k, lens_t, page, page_cap):
+    n, n_kv = k.shape[:2]
+    kmin = torch.zeros(n, n_kv, D, page_cap, dtype=torch.bfloat16, device="cuda")
+    kmax = torch.zeros_like(kmin)
+    ws = rkv.rkv_build_page_summaries(k, lens_t, page, kmin, kmax)
+    rkv.rkv_check_status(ws)
+    return kmin, kmax
+
+
+@pytest.mark.parametrize("page", [1, 4, 16])
+def test_summaries_bit_exact(page):
+    rkv = _lib()
+    lens = [4093, 257, 1030]
+    cap = 4096
+    k, _ = _make_cache(3, 2, cap, lens, seed=11 + page)
+    page_cap = _page_cap(cap, page)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    kmin, kmax = _summaries(rkv, k, lens_t, page, page_cap)
+    for u, L in enumerate(lens):
+        for g in range(2):
+            rmin, rmax = O.page_summaries(_f64(k[u, g]), L, page)
+            P = rmin.shape[1]
+            assert np.array_equal(_f64(kmin[u, g, :, :P]), rmin)
+            assert np.array_equal(_f64(kmax[u, g, :, :P]), rmax)
+
+
+def test_summaries_incremental_first_token():
+    rkv = _lib()
+    cap, page = 2048, 4
+    lens = [1999, 2048]
+    k, _ = _make_cache(2, 2, cap, lens, seed=5)
+    page_cap = _page_cap(cap, page)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    kmin, kmax = _summaries(rkv, k, lens_t, page, page_cap)
+    full_min, full_max = kmin.clone(), kmax.clone()
+    # scribble over the tail pages, then rebuild only from token 1500 on
+    kmin[..., 375:] = 0
+    kmax[..., 375:] = 0
+    ws = rkv.rkv_build_page_summaries(k, lens_t, page, kmin, kmax, first_token=1500)
+    rkv.rkv_check_status(ws)
+    for u, L in enumerate(lens):
+        P = (L + page - 1) // page
+        assert torch.equal(kmin[u, :, :, :P], full_min[u, :, :, :P])
+        assert torch.equal(kmax[u, :, :, :P], full_max[u, :, :, :P])
+
+
+def _hybrid_case(n, n_kv, gqa, lens, cap, budget, page, channels, seed, steps=2):
+    rkv = _lib()
+    k, v = _make_cache(n, n_kv, cap, lens, seed)
+    page_cap = _page_cap(cap, page)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    kmin, kmax = _summaries(rkv, k, lens_t, page, page_cap)
+    scale = 1.0 / math.sqrt(D)
+    S = (budget // 2) // page
+    g_ = torch.Generator().manual_seed(seed + 1)
+    kk, vv = _f64(k), _f64(v)
+    for step in range(steps):
+        q = torch.randn(n, n_kv * gqa, D, generator=g_).to(torch.bfloat16).cuda()
+        out = torch.empty_like(q)
+        sel_c = torch.full((n, n_kv, channels), -7, dtype=torch.int32, device="cuda")
+        sel_p = torch.full((n, n_kv, S), -7, dtype=torch.int32, device="cuda")
+        approx = torch.zeros(n, n_kv, page_cap, dtype=torch.float32, device="cuda")
+        ws = rkv.rkv_hybrid_decode(q, k, v, lens_t, kmin, kmax, budget, page, channels, scale,
+                                   out, sel_channels=sel_c, sel_pages=sel_p,
+                                   approx_scores=approx)
+        rkv.rkv_check_status(ws)
+        qq = _f64(q)
+        for u, L in enumerate(lens):
+            for g in range(n_kv):
+                qh = qq[u, g * gqa:(g + 1) * gqa]
+                rmin, rmax = O.page_summaries(kk[u, g], L, page)
+                ref = O.hybrid_decode(qh, kk[u, g], vv[u, g], L, rmin, rmax, budget, page,
+                                      channels, scale)
+                tag = f"step {step} unit {u} kv {g} len {L}"
+                if ref["channels"] is None:
+                    assert (sel_c[u, g] == -1).all(), tag
+                    assert (sel_p[u, g] == -1).all(), tag
+                    parity.check_output(_f64(out[u, g * gqa:(g + 1) * gqa]), ref["out"], tag)
+                    continue
+                mag = np.abs(qh).sum(axis=0)
+                parity.check_selection(sel_c[u, g].cpu().numpy(), mag, channels,
+                                       f"{tag} channels")
+                gch = np.sort(sel_c[u, g].cpu().numpy())
+                q_g = qh.sum(axis=0)
+                # approximate scores: recompute on the GPU's channels (equal unless tie band)
+                ref_a = O.approx_scores(q_g, gch, rmin, rmax)
+                P = rmin.shape[1]
+                magn = sum(np.abs(q_g[i]) * np.maximum(np.abs(rmin[i]), np.abs(rmax[i]))
+                           for i in gch)
+                parity.check_approx(approx[u, g, :P].cpu().numpy(), ref_a, magn,
+                                    f"{tag} approx")
+                nsel = min(S, P)
+                gp = sel_p[u, g].cpu().numpy()
+                assert (gp[nsel:] == -1).all(), tag
+                parity.check_selection(gp[:nsel], ref_a, nsel, f"{tag} pages")
+                assert np.all(np.diff(gp[:nsel]) > 0), f"{tag} pages not ascending"
+                toks = np.concatenate([np.arange(pg * page, min(L, (pg + 1) * page))
+                                       for pg in gp[:nsel]])
+                ref_out = O.attention(qh, kk[u, g][toks], vv[u, g][toks], scale)
+                parity.check_output(_f64(out[u, g * gqa:(g + 1) * gqa]), ref_out, tag)
+
+
+def test_hybrid_config1_shape():
+    # 8 q / 2 kv heads, 4K cache, B 256, page 4, 32 channels (the tiny configuration's decode)
+    _hybrid_case(1, 2, 4, [4096], 4096, 256, 4, 32, seed=21, steps=4)
+
+
+def test_hybrid_ragged_and_dense_fallback():
+    # ragged lengths incl. a partial last page, P % 8 != 0, and len <= budget (dense path)
+    _hybrid_case(4, 2, 4, [4093, 200, 1030, 256], 4096, 256, 4, 32, seed=22)
+
+
+@pytest.mark.parametrize("gqa", [1, 2, 8])
+def test_hybrid_gqa_variants(gqa):
+    _hybrid_case(2, 2, gqa, [3001, 777], 3072, 256, 4, 32, seed=23 + gqa)
+
+
+@pytest.mark.parametrize("budget,page,channels", [(1024, 4, 32), (256, 16, 128), (128, 1, 16),
+                                                  (512, 8, 64)])
+def test_hybrid_budget_page_channel_variants(budget, page, channels):
+    _hybrid_case(2, 2, 4, [8191, 5000], 8192, budget, page, channels, seed=31 + page)
+
+
+def test_hybrid_page1_all_channels_is_exact_group_topk():
+    # the reduction the method's approximation collapses to (exact group top-k attention)
+    rkv = _lib()
+    n, n_kv, gqa, L, B = 1, 2, 4, 2000, 256
+    k, v = _make_cache(n, n_kv, 2048, [L], seed=41)
+    lens_t = torch.tensor([L], dtype=torch.int32, device="cuda")
+    page_cap = _page_cap(2048, 1)
+    kmin, kmax = _summaries(rkv, k, lens_t, 1, page_cap)
+    q = torch.randn(n, n_kv * gqa, D, generator=torch.Generator().manual_seed(42))
+    q = q.to(torch.bfloat16).cuda()
+    out = torch.empty_like(q)
+    sel_p = torch.empty(n, n_kv, B // 2, dtype=torch.int32, device="cuda")
+    ws = rkv.rkv_hybrid_decode(q, k, v, lens_t, kmin, kmax, B, 1, D, 0.1, out, sel_pages=sel_p)
+    rkv.rkv_check_status(ws)
+    for g in range(n_kv):
+        qh = _f64(q[0, g * gqa:(g + 1) * gqa])
+        ref_out, ref_tok = O.group_topk_attention(qh, _f64(k[0, g]), _f64(v[0, g]), L, B // 2,
+                                                  0.1)
+        true = _f64(k[0, g])[:L] @ qh.sum(axis=0)
+        parity.check_selection(sel_p[0, g].cpu().numpy(), true, B // 2, "exact top-k")
+        parity.check_output(_f64(out[0, g * gqa:(g + 1) * gqa]), ref_out, "exact top-k out")
+
+
+def test_hybrid_append_steps():
+    rkv = _lib()
+    n, n_kv, gqa, page, B, C = 3, 2, 4, 4, 256, 32
+    cap = 1100
+    lens = [1021, 400, 200]          # 200 crosses the budget while appending
+    k, v = _make_cache(n, n_kv, cap, lens, seed=51)
+    page_cap = _page_cap(cap, page)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    kmin, kmax = _summaries(rkv, k, lens_t, page, page_cap)
+    kk, vv = _f64(k), _f64(v)
+    cur = list(lens)
+    rmins, rmaxs = {}, {}
+    for u in range(n):
+        for g in range(n_kv):
+            a, b = O.page_summaries(kk[u, g], cur[u], page)
+            rmins[u, g] = np.zeros((D, page_cap))
+            rmaxs[u, g] = np.zeros((D, page_cap))
+            rmins[u, g][:, :a.shape[1]] = a
+            rmaxs[u, g][:, :a.shape[1]] = b
+    gen = torch.Generator().manual_seed(52)
+    scale = 1.0 / math.sqrt(D)
+    for step in range(70):
+        q = torch.randn(n, n_kv * gqa, D, generator=gen).to(torch.bfloat16).cuda()
+        nk = torch.randn(n, n_kv, D, generator=gen).to(torch.bfloat16).cuda()
+        nv = torch.randn(n, n_kv, D, generator=gen).to(torch.bfloat16).cuda()
+        out = torch.empty_like(q)
+        sel_p = torch.empty(n, n_kv, B // 2 // page, dtype=torch.int32, device="cuda")
+        ws = rkv.rkv_hybrid_decode(q, k, v, lens_t, kmin, kmax, B, page, C, scale, out,
+                                   new_k=nk, new_v=nv, sel_pages=sel_p)
+        rkv.rkv_check_status(ws)
+        qq, nkk, nvv = _f64(q), _f64(nk), _f64(nv)
+        for u in range(n):
+            newlen = None
+            for g in range(n_kv):
+                newlen = O.append_token(kk[u, g], vv[u, g], cur[u], rmins[u, g], rmaxs[u, g],
+                                        nkk[u, g], nvv[u, g], page)
+            cur[u] = newlen
+            for g in range(n_kv):
+                qh = qq[u, g * gqa:(g + 1) * gqa]
+                L = cur[u]
+                ref = O.hybrid_decode(qh, kk[u, g], vv[u, g], L, rmins[u, g], rmaxs[u, g], B,
+                                      page, C, scale)
+                tag = f"append step {step} unit {u} kv {g} len {L}"
+                if ref["pages"] is None:
+                    parity.check_output(_f64(out[u, g * gqa:(g + 1) * gqa]), ref["out"], tag)
+                    continue
+                gp = sel_p[u, g].cpu().numpy()
+                parity.check_selection(gp, ref["scores"], len(ref["pages"]), tag)
+                toks = np.concatenate([np.arange(pg * page, min(L, (pg + 1) * page))
+                                       for pg in gp])
+                ref_out = O.attention(qh, kk[u, g][toks], vv[u, g][toks], scale)
+                parity.check_output(_f64(out[u, g * gqa:(g + 1) * gqa]), ref_out, tag)
+    assert lens_t.cpu().tolist() == cur
+    for u in range(n):
+        for g in range(n_kv):
+            P = (cur[u] + page - 1) // page
+            assert np.array_equal(_f64(kmin[u, g, :, :P]), rmins[u, g][:, :P])
+            assert np.array_equal(_f64(kmax[u, g, :, :P]), rmaxs[u, g][:, :P])
+            assert np.array_equal(_f64(k[u, g, :cur[u]]), kk[u, g, :cur[u]])
+
+
+@pytest.mark.parametrize("gqa", [1, 4, 8])
+def test_dense_decode_ragged(gqa):
+    rkv = _lib()
+    n, n_kv, max_len = 3, 2, 5000
+    lens = [5000, 1, 2049]
+    k, v = _make_cache(n, n_kv, max_len, lens, seed=61)
+    q = torch.randn(n, n_kv * gqa, D, generator=torch.Generator().manual_seed(62))
+    q = q.to(torch.bfloat16).cuda()
+    out = torch.empty_like(q)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    ws = rkv.rkv_dense_decode(q, k, v, lens_t, 0.0884, out)
+    rkv.rkv_check_status(ws)
+    kk, vv, qq = _f64(k), _f64(v), _f64(q)
+    for u, L in enumerate(lens):
+        for g in range(n_kv):
+            qh = qq[u, g * gqa:(g + 1) * gqa]
+            ref = O.dense_decode(qh, kk[u, g], vv[u, g], L, 0.0884)
+            parity.check_output(_f64(out[u, g * gqa:(g + 1) * gqa]), ref, f"dense {u} {g}")
+
+
+def test_device_status_len_over_cap():
+    rkv = _lib()
+    k, v = _make_cache(1, 1, 64, [64], seed=71)
+    lens_t = torch.tensor([65], dtype=torch.int32, device="cuda")   # beyond cap
+    kmin = torch.zeros(1, 1, D, 16, dtype=torch.bfloat16, device="cuda")
+    kmax = torch.zeros_like(kmin)
+    ws = rkv.rkv_build_page_summaries(k, lens_t, 4, kmin, kmax)
+    with pytest.raises(rkv.RkvError) as ei:
+        rkv.rkv_check_status(ws)
+    assert ei.value.bits & 1
+    # the word is cleared by the check
+    assert rkv.rkv_check_status(ws) == 0
