@@ -168,7 +168,7 @@ struct SelectScratch {
 // Choose the k largest of keys[0..n) (ties -> lower index) and write their indices, ascending,
 // to out[0..k). keys may live in shared or global memory. 1 <= k <= n. Every thread of the
 // block must call it. Returns the number written (== k unless something is badly wrong).
-__device__ int block_topk_ascending(const float* keys, int n, int k, int* out,
+__device__ __noinline__ static int block_topk_ascending(const float* keys, int n, int k, int* out,
                                     SelectScratch& sc) {
   const int tid = threadIdx.x, nt = blockDim.x;
   uint32_t prefix = 0, mask = 0;

@@ -364,11 +364,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
 
   // q pre-scaled into registers
   __syncthreads();
-  if (tid < G * kHeadDim / 2) {
-    // scale in place (each thread two values)
-    qs[2 * tid] *= a.scale_log2;
-    qs[2 * tid + 1] *= a.scale_log2;
-  }
+  for (int i = tid; i < G * kHeadDim; i += kDecodeThreads) qs[i] *= a.scale_log2;
   __syncthreads();
   WarpAttn<G> wa;
   wa.init(qs);

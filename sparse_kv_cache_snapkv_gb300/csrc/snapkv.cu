@@ -1,24 +1,607 @@
-// Stage-1 kernels (SnapKV++): placeholder until the tensor-core score kernels land.
+// Stage-1 kernels of RocketKV (SnapKV++ prefill eviction) on sm_103a.
+//
+// Method: "RocketKV: Accelerating Long-Context LLM Inference via Two-Stage KV Cache
+// Compression" -- summarizepaper.com "Key points" (SnapKV with the grouped-query enhancement),
+// OpenReview author responses on paperhub.cn: "Novelty of SnapKV++" (scores summed over the
+// query heads of a KV group, so each KV head selects once), "Potential Sensitivity to Kernel
+// Size in SnapKV++" (1-D pooling whose size grows with the prompt length), "Is Needle Among
+// Evicted Tokens" (eviction independent per head and per layer).
+//
+// Score computation, per (unit, KV head) with R = gqa * window window rows (padded to RP = 128
+// or 256) and the prompt's K:
+//   pass 1  D1 = Qwin . K^T on tcgen05 (M = 128 query rows per block, N = 128 tokens), TMEM
+//           accumulators read back per row: online max / sum of 2^(scale*log2e*s) over the keys
+//           each window row may see (prefix + causal window) -> per-split partial (m, l).
+//   pass 2  D2 = K . Qwin^T (M = 128 tokens, N = RP rows): each TMEM lane is one token, so the
+//           column sum over window rows and group heads, sum_r 2^(s*c - lse_r), is a per-thread
+//           reduction. The partial (m, l) of all splits are merged into lse_r first.
+// Both passes stream 128-token K tiles by TMA (SWIZZLE_128B, 2 x 64-column boxes) through a
+// 4-stage mbarrier ring; one thread issues MMAs, eight warps run the epilogue; TMEM holds two
+// accumulator buffers so the epilogue of tile i overlaps the MMA of tile i+1. Units are
+// processed in waves small enough that pass 2 re-reads K from L2.
+//   select  max-pool (odd kernel, clipped ends) + block radix top-k, ascending kept positions
+//   gather  kept K / V rows -> compact cache (16-byte vector copies)
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "common.cuh"
 #include "rkv_internal.h"
 
 namespace rkv {
 
+constexpr int kTileTok = 128;
+constexpr int kKStages = 4;
+constexpr int kScoreThreads = 320;  // warp 0: TMA, warp 1: MMA, warps 2..9: epilogue
+constexpr int kEpiThreads = 256;
+constexpr int kTileBytes = kTileTok * kHeadDim * 2;  // 32 KB per K tile
+constexpr size_t kWaveBytes = 64ull << 20;           // K bytes per wave (L2-resident for pass 2)
+constexpr int kSMs = 152;
+
+// ------------------------------------------------------------------------------------------
+// tcgen05 / TMA wrappers
+// ------------------------------------------------------------------------------------------
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row core groups 1024 B
+// apart (SBO), descriptor version 1.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 accumulate, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(tmem_d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+      ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_addr(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__host__ __device__ inline int adaptive_kernel(int L) {
+  return L <= 8192 ? 7 : (L <= 32768 ? 15 : 31);
+}
+
+// ------------------------------------------------------------------------------------------
+// score kernel (both passes)
+// ------------------------------------------------------------------------------------------
+struct ScoreParams {
+  int n_kv, gqa, window, max_len, hq;
+  int unit0;
+  int nsplit, tiles_per_split;
+  float scale_log2;
+  const int32_t* seq_lens;
+  float* part_ml;  // [units][nsplit][RP][2]
+  float* scores;   // [units][max_len - window]
+  uint32_t* status;
+};
+
+template <int RB>
+struct ScoreSmem {
+  static constexpr int RP = RB * 128;
+  static constexpr size_t q_bytes = (size_t)RP * kHeadDim * 2;
+  static constexpr size_t k_off = q_bytes;
+  static constexpr size_t bar_off = k_off + (size_t)kKStages * kTileBytes;
+  static constexpr size_t misc_off = bar_off + 256;
+  static constexpr size_t total = misc_off + RP * 4 + 2 * 128 * 4 + 2 * 128 * 4 + 64 + 1024;
+};
+
+template <int PASS, int RB>
+__global__ void __launch_bounds__(kScoreThreads, 1)
+    score_kernel(const __grid_constant__ CUtensorMap kmap,
+                 const __grid_constant__ CUtensorMap qmap, ScoreParams p) {
+  constexpr int RP = RB * 128;
+  constexpr uint32_t kCols = (PASS == 1) ? (RB == 1 ? 256u : 512u) : (RP == 128 ? 256u : 512u);
+  using SM = ScoreSmem<RB>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* qs = smem;
+  uint8_t* ks = smem + SM::k_off;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::bar_off);
+  uint64_t* empty = full + kKStages;
+  uint64_t* tfull = empty + kKStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* qfull = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qfull + 1);
+  float* lse2 = reinterpret_cast<float*>(smem + SM::misc_off);   // [RP] (pass 2)
+  float* xch_m = lse2 + RP;                                      // [128] (pass 1 merge)
+  float* xch_l = xch_m + 128;                                    // [128]
+  float* spart = xch_l + 128;                                    // [2][128] (pass 2 merge)
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ukv = p.unit0 + blockIdx.x / p.nsplit;
+  const int split = blockIdx.x % p.nsplit;
+  const int u = ukv / p.n_kv, g = ukv - u * p.n_kv;
+  const int W = p.window;
+  const int R = p.gqa * W;
+  int L = p.seq_lens[u];
+  const bool bad = L <= W || L > p.max_len;
+  if (bad) {
+    if (tid == 0 && split == 0 && PASS == 1) set_status(p.status, RKV_DEV_BAD_WINDOW);
+    L = 0;
+  }
+  const int span = (PASS == 1) ? L : (L > W ? L - W : 0);  // tokens this pass covers
+  const int tiles_all = (span + kTileTok - 1) / kTileTok;
+  const int tile0 = split * p.tiles_per_split;
+  const int ntiles = max(0, min(p.tiles_per_split, tiles_all - tile0));
+
+  if (tid == 0) {
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], kEpiThreads / 32);
+    }
+    mbar_init(qfull, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_addr(tmem_slot)), "r"(kCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // pass 2: merge the per-split partials into lse2[r] (log2 domain); padded rows -> +big
+  if (PASS == 2 && tid < RP) {
+    float m = -1e30f, l = 0.f;
+    if (!bad && tid < R) {
+      const float* pm = p.part_ml + ((size_t)ukv * p.nsplit * RP + tid) * 2;
+      for (int s = 0; s < p.nsplit; ++s) {
+        const float ms = pm[(size_t)s * RP * 2], ls = pm[(size_t)s * RP * 2 + 1];
+        const float mn = fmaxf(m, ms);
+        l = l * exp2f(m - mn) + ls * exp2f(ms - mn);
+        m = mn;
+      }
+    }
+    lse2[tid] = (l > 0.f) ? m + log2f(l) : 1e30f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool aborted = false;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0 && ntiles > 0) {
+      const int qrow0 = (u * p.hq + g * p.gqa) * W;
+      mbar_arrive_expect_tx(qfull, (uint32_t)(RP * kHeadDim * 2));
+      for (int h = 0; h < 2; ++h)
+        for (int rb = 0; rb < RB; ++rb)
+          tma_load_2d(qs + (size_t)h * RP * 128 + (size_t)rb * 128 * 128, &qmap, 64 * h,
+                      qrow0 + rb * 128, qfull);
+      const int krow0 = ukv * p.max_len;
+      int it = 0;
+      for (; it < ntiles; ++it) {
+        const int s = it % kKStages;
+        if (it >= kKStages && !mbar_wait(&empty[s], (uint32_t)(((it / kKStages) - 1) & 1))) {
+          aborted = true;
+          break;
+        }
+        uint8_t* dst = ks + (size_t)s * kTileBytes;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)kTileBytes);
+        const int y = krow0 + (tile0 + it) * kTileTok;
+        tma_load_2d(dst, &kmap, 0, y, &full[s]);
+        tma_load_2d(dst + kTileBytes / 2, &kmap, 64, y, &full[s]);
+      }
+      // loads still in flight must land before the CTA may retire
+      for (int j = max(0, it - kKStages); j < it; ++j)
+        mbar_wait(&full[j % kKStages], (uint32_t)((j / kKStages) & 1));
+      if (aborted) set_status(p.status, RKV_DEV_WAIT_TIMEOUT);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      if (!mbar_wait(qfull, 0)) {
+        aborted = true;
+      }
+      for (int it = 0; it < ntiles && !aborted; ++it) {
+        const int s = it % kKStages, b = it & 1;
+        if (!mbar_wait(&full[s], (uint32_t)((it / kKStages) & 1))) {
+          aborted = true;
+          break;
+        }
+        if (it >= 2 && !mbar_wait(&tempty[b], (uint32_t)(((it >> 1) - 1) & 1))) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t kbase = smem_addr(ks + (size_t)s * kTileBytes);
+        const uint32_t qbase = smem_addr(qs);
+        if (PASS == 1) {
+          constexpr uint32_t id = idesc_bf16(128, kTileTok);
+#pragma unroll
+          for (int rb = 0; rb < RB; ++rb) {
+            const uint32_t d = tmem + (uint32_t)((b * RB + rb) * kTileTok);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (uint32_t)((kk >> 2) * RP * 128 + rb * 128 * 128 + (kk & 3) * 32);
+              const uint32_t koff = (uint32_t)((kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32);
+              umma_bf16(d, desc_sw128(qbase + off), desc_sw128(kbase + koff), id, kk > 0);
+            }
+          }
+        } else {
+          constexpr uint32_t id = idesc_bf16(kTileTok, RP);
+          const uint32_t d = tmem + (uint32_t)(b * RP);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t koff = (uint32_t)((kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32);
+            const uint32_t qoff = (uint32_t)((kk >> 2) * RP * 128 + (kk & 3) * 32);
+            umma_bf16(d, desc_sw128(kbase + koff), desc_sw128(qbase + qoff), id, kk > 0);
+          }
+        }
+        umma_commit(&empty[s]);
+        umma_commit(&tfull[b]);
+      }
+      if (aborted) set_status(p.status, RKV_DEV_WAIT_TIMEOUT);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int e = warp - 2;        // 0..7
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int hf = e >> 2;         // 0 / 1
+    const int lrow = quarter * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    if (PASS == 1) {
+      // row this thread owns and its visibility limit
+      const int rb = (RB == 2) ? hf : 0;
+      const int rg = rb * 128 + lrow;
+      const bool row_ok = rg < R;
+      const int lim = L - W + (row_ok ? rg % W : 0);  // last visible key position
+      const int c0 = (RB == 2) ? 0 : hf * 64;
+      const int ncol = (RB == 2) ? 128 : 64;
+      float m = -1e30f, l = 0.f;
+      for (int it = 0; it < ntiles && !aborted; ++it) {
+        const int b = it & 1;
+        if (!mbar_wait(&tfull[b], (uint32_t)((it >> 1) & 1))) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        const int t0 = (tile0 + it) * kTileTok;
+        for (int cc = 0; cc < ncol; cc += 32) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_addr + (uint32_t)((b * RB + rb) * kTileTok + c0 + cc), r);
+          const int tb = t0 + c0 + cc;
+          float s[32];
+          float mt = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float x = __uint_as_float(r[i]) * p.scale_log2;
+            s[i] = (tb + i <= lim) ? x : -INFINITY;
+            mt = fmaxf(mt, s[i]);
+          }
+          const float mn = fmaxf(m, mt);
+          float acc = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc += exp2f(s[i] - mn);
+          l = l * exp2f(m - mn) + acc;
+          m = mn;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[b]);
+      }
+      if (RB == 1) {
+        if (hf == 1) {
+          xch_m[lrow] = m;
+          xch_l[lrow] = l;
+        }
+        named_bar_sync(1, kEpiThreads);
+        if (hf == 0) {
+          const float m2 = xch_m[lrow], l2 = xch_l[lrow];
+          const float mn = fmaxf(m, m2);
+          l = l * exp2f(m - mn) + l2 * exp2f(m2 - mn);
+          m = mn;
+        }
+      }
+      if (RB == 2 || hf == 0) {
+        float* dst = p.part_ml + (((size_t)ukv * p.nsplit + split) * RP + rb * 128 + lrow) * 2;
+        dst[0] = m;
+        dst[1] = l;
+      }
+    } else {
+      // column sums: thread = token lrow of the tile, columns [c0, c0 + ncol) = window rows
+      const int ncol = RP / 2;
+      const int c0 = hf * ncol;
+      const int prefix = L - W;
+      float* out = p.scores + (size_t)ukv * (p.max_len - W);
+      // Every epilogue warp passes the named barrier once per tile, also after a failed wait,
+      // so that a timeout in one warp can never leave the others waiting at the barrier.
+      for (int it = 0; it < ntiles; ++it) {
+        const int b = it & 1;
+        if (!aborted && !mbar_wait(&tfull[b], (uint32_t)((it >> 1) & 1))) aborted = true;
+        float acc = 0.f;
+        if (!aborted) {
+          tc_fence_after();
+          for (int cc = 0; cc < ncol; cc += 32) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_addr + (uint32_t)(b * RP + c0 + cc), r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              acc += exp2f(fmaf(__uint_as_float(r[i]), p.scale_log2, -lse2[c0 + cc + i]));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[b]);
+        }
+        if (hf == 1) spart[b * 128 + lrow] = acc;
+        named_bar_sync(1, kEpiThreads);
+        if (hf == 0 && !aborted) {
+          const int t = (tile0 + it) * kTileTok + lrow;
+          if (t < prefix) out[t] = acc + spart[b * 128 + lrow];
+        }
+      }
+    }
+    if (aborted) set_status(p.status, RKV_DEV_WAIT_TIMEOUT);
+  }
+  if (PASS == 1 && ntiles == 0 && warp >= 2) {
+    // an empty split still publishes a neutral partial
+    const int e = warp - 2, hf = e >> 2, lrow = (warp & 3) * 32 + lane;
+    if (RB == 2 || hf == 0) {
+      const int rb = (RB == 2) ? hf : 0;
+      float* dst = p.part_ml + (((size_t)ukv * p.nsplit + split) * RP + rb * 128 + lrow) * 2;
+      dst[0] = -1e30f;
+      dst[1] = 0.f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// pooling + top-k selection: one CTA of 1024 threads per (unit, KV head)
+// ------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) select_kernel(SnapArgs a) {
+  __shared__ SelectScratch sc;
+  const int ukv = blockIdx.x;
+  const int u = ukv / a.n_kv, g = ukv - u * a.n_kv;
+  const int W = a.window;
+  const int L = a.seq_lens[u];
+  int32_t* kept = a.kept_idx + (size_t)ukv * a.keep;
+  if (L <= W || L > a.max_len) {
+    for (int i = threadIdx.x; i < a.keep; i += blockDim.x) kept[i] = -1;
+    if (g == 0 && threadIdx.x == 0) a.out_len[u] = 0;
+    return;
+  }
+  if (L <= a.keep) {
+    for (int i = threadIdx.x; i < a.keep; i += blockDim.x) kept[i] = i < L ? i : -1;
+    if (g == 0 && threadIdx.x == 0) a.out_len[u] = L;
+    return;
+  }
+  const int n = L - W;
+  const int ks = a.kernel_size > 0 ? a.kernel_size : adaptive_kernel(L);
+  const int r = ks / 2;
+  const float* in = a.scores + (size_t)ukv * (a.max_len - W);
+  float* pooled = a.pooled + (size_t)ukv * (a.max_len - W);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    float m = in[i];
+    const int lo = max(0, i - r), hi = min(n - 1, i + r);
+    for (int j = lo; j <= hi; ++j) m = fmaxf(m, in[j]);
+    pooled[i] = m;
+  }
+  __syncthreads();
+  const int want = a.keep - W;
+  const int got = block_topk_ascending(pooled, n, want, kept, sc);
+  if (got != want && threadIdx.x == 0) set_status(a.status, RKV_DEV_SELECT_FAILED);
+  for (int j = threadIdx.x; j < W; j += blockDim.x) kept[want + j] = L - W + j;
+  if (g == 0 && threadIdx.x == 0) a.out_len[u] = a.keep;
+}
+
+// ------------------------------------------------------------------------------------------
+// compaction gather: CTA = 64 kept rows of one (unit, KV head); each thread copies 16-byte
+// chunks of K and V rows
+// ------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) gather_kernel(SnapArgs a) {
+  const int ukv = blockIdx.y;
+  const int u = ukv / a.n_kv;
+  const int L = a.seq_lens[u];
+  if (L <= a.window || L > a.max_len) return;
+  const int cnt = min(L, a.keep);
+  const int row0 = blockIdx.x * 64;
+  if (row0 >= cnt) return;
+  const int32_t* kept = a.kept_idx + (size_t)ukv * a.keep;
+  const uint4* ksrc = reinterpret_cast<const uint4*>(a.k + (size_t)ukv * a.max_len * kHeadDim);
+  const uint4* vsrc = reinterpret_cast<const uint4*>(a.v + (size_t)ukv * a.max_len * kHeadDim);
+  uint4* kdst = reinterpret_cast<uint4*>(a.k_out + (size_t)ukv * a.cap * kHeadDim);
+  uint4* vdst = reinterpret_cast<uint4*>(a.v_out + (size_t)ukv * a.cap * kHeadDim);
+  uint4 kv[4], vv[4];
+  int dst[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = threadIdx.x + 256 * i;  // 64 rows x 16 chunks
+    const int row = row0 + (idx >> 4), ch = idx & 15;
+    dst[i] = -1;
+    if (row < cnt) {
+      const int src = kept[row];
+      if (src >= 0 && src < L) {
+        kv[i] = ksrc[(size_t)src * 16 + ch];
+        vv[i] = vsrc[(size_t)src * 16 + ch];
+        dst[i] = row * 16 + ch;
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (dst[i] >= 0) {
+      kdst[dst[i]] = kv[i];
+      vdst[dst[i]] = vv[i];
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------------------------
 void snapkv_plan(int n, int n_kv, int gqa, int max_len, int window, int* nsplit,
                  int* tokens_per_split, int* rows_pad) {
-  (void)n; (void)n_kv; (void)gqa; (void)window;
-  *nsplit = 1;
-  *tokens_per_split = max_len;
-  *rows_pad = 128;
+  const int units = n * n_kv;
+  const int tiles = (max_len + kTileTok - 1) / kTileTok;
+  const size_t unit_bytes = (size_t)max_len * kHeadDim * 2;
+  int wave = (int)(kWaveBytes / unit_bytes);
+  wave = wave < 1 ? 1 : (wave > units ? units : wave);
+  int ns = kSMs / wave;
+  ns = ns < 1 ? 1 : (ns > tiles ? tiles : ns);
+  const int tps = (tiles + ns - 1) / ns;
+  ns = (tiles + tps - 1) / tps;
+  *nsplit = ns;
+  *tokens_per_split = tps;  // in tiles
+  *rows_pad = gqa * window <= 128 ? 128 : 256;
+}
+
+static int wave_units(int units, int max_len) {
+  const size_t unit_bytes = (size_t)max_len * kHeadDim * 2;
+  int wave = (int)(kWaveBytes / unit_bytes);
+  return wave < 1 ? 1 : (wave > units ? units : wave);
 }
 
 size_t snapkv_scratch_bytes(int n, int n_kv, int gqa, int max_len, int window) {
-  (void)gqa;
-  return 2 * align_up((size_t)n * n_kv * (max_len - window) * 4, 256);
+  int ns, tps, rp;
+  snapkv_plan(n, n_kv, gqa, max_len, window, &ns, &tps, &rp);
+  const size_t plen = align_up((size_t)n * n_kv * (max_len - window) * 4, 256);
+  return 2 * plen + align_up((size_t)n * n_kv * ns * rp * 2 * 4, 256);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// rows x 128 bf16, row-major, boxes of 128 rows x 64 columns, 128-byte swizzle
+static bool make_rows_map(CUtensorMap* map, const void* base, uint64_t rows) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+template <int PASS, int RB>
+static cudaError_t launch_pass(const CUtensorMap& km, const CUtensorMap& qm,
+                               const ScoreParams& sp, int nunits, cudaStream_t s) {
+  const size_t smem = ScoreSmem<RB>::total;
+  cudaError_t e = cudaFuncSetAttribute(score_kernel<PASS, RB>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  score_kernel<PASS, RB><<<nunits * sp.nsplit, kScoreThreads, smem, s>>>(km, qm, sp);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_snapkv(const SnapArgs& a, cudaStream_t s) {
-  (void)a; (void)s;
-  return cudaErrorNotSupported;
+  CUtensorMap km, qm;
+  const uint64_t krows = (uint64_t)a.n * a.n_kv * a.max_len;
+  const uint64_t qrows = (uint64_t)a.n * a.n_kv * a.gqa * a.window;
+  if (!make_rows_map(&km, a.k, krows) || !make_rows_map(&qm, a.q_win, qrows))
+    return cudaErrorInvalidValue;
+  const int units = a.n * a.n_kv;
+  const int wave = wave_units(units, a.max_len);
+  ScoreParams sp{};
+  sp.n_kv = a.n_kv;
+  sp.gqa = a.gqa;
+  sp.window = a.window;
+  sp.max_len = a.max_len;
+  sp.hq = a.n_kv * a.gqa;
+  sp.nsplit = a.nsplit;
+  sp.tiles_per_split = a.tokens_per_split;
+  sp.scale_log2 = a.scale_log2;
+  sp.seq_lens = a.seq_lens;
+  sp.part_ml = a.part_ml;
+  sp.scores = a.scores;
+  sp.status = a.status;
+  cudaError_t e = cudaSuccess;
+  for (int u0 = 0; u0 < units; u0 += wave) {
+    const int nu = units - u0 < wave ? units - u0 : wave;
+    sp.unit0 = u0;
+    if (a.rows_pad == 128) {
+      e = launch_pass<1, 1>(km, qm, sp, nu, s);
+      if (e == cudaSuccess) e = launch_pass<2, 1>(km, qm, sp, nu, s);
+    } else {
+      e = launch_pass<1, 2>(km, qm, sp, nu, s);
+      if (e == cudaSuccess) e = launch_pass<2, 2>(km, qm, sp, nu, s);
+    }
+    if (e != cudaSuccess) return e;
+  }
+  select_kernel<<<units, 1024, 0, s>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  gather_kernel<<<dim3((a.keep + 63) / 64, units), 256, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace rkv

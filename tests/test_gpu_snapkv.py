@@ -1,0 +1,141 @@
+"""Parity of SnapKV++ compression (tensor-core window scores, pooling + top-k, gather) against the
+CPU oracle, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import rocketkv as O
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+SCORE_REL = 1e-4
+
+
+def _lib():
+    from sparse_kv_cache_snapkv_gb300 import rkv
+    rkv.load()
+    return rkv
+
+
+def _f64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def _inputs(n_seq, n_kv, gqa, lens, window, seed, needles=0, outliers=0, layers=1):
+    from sparse_kv_cache_snapkv_gb300 import synthetic as S
+    wl = S.Workload("t", n_seq, layers, n_kv, gqa, D, tuple(lens), window, 256,
+                    needles=needles, outliers=outliers)
+    x = S.prefill_inputs(wl, seed=seed, device="cuda")
+    return wl, x
+
+
+def _run(rkv, x, window, kernel, keep, cap=None):
+    k, v, q, lens = x["k"], x["v"], x["q_win"], x["seq_lens"]
+    n, n_kv, max_len, _ = k.shape
+    cap = cap or keep
+    k_out = torch.zeros(n, n_kv, cap, D, dtype=torch.bfloat16, device="cuda")
+    v_out = torch.zeros_like(k_out)
+    kept = torch.full((n, n_kv, keep), -9, dtype=torch.int32, device="cuda")
+    out_len = torch.full((n,), -9, dtype=torch.int32, device="cuda")
+    scores = torch.full((n, n_kv, max_len - window), -1.0, dtype=torch.float32, device="cuda")
+    ws = rkv.rkv_snapkv_compress(k, v, lens, q, kernel, keep, 1.0 / math.sqrt(D), k_out, v_out,
+                                 kept, out_len, scores_out=scores)
+    rkv.rkv_check_status(ws)
+    return k_out, v_out, kept, out_len, scores
+
+
+def _check_unit(x, u, g, gqa, window, kernel, keep, k_out, v_out, kept, out_len, scores,
+                tag=""):
+    L = int(x["seq_lens"][u])
+    W = window
+    k = _f64(x["k"][u, g, :L])
+    v = _f64(x["v"][u, g, :L])
+    q = _f64(x["q_win"][u, g * gqa:(g + 1) * gqa])
+    ref_scores = O.window_scores(k, q, 1.0 / math.sqrt(D))
+    gs = scores[u, g, :L - W].cpu().numpy().astype(np.float64)
+    err = np.abs(gs - ref_scores)
+    tol = SCORE_REL * np.abs(ref_scores) + 1e-30
+    assert (err <= tol).all(), (f"{tag} scores: {(err > tol).sum()} bad, worst rel "
+                                f"{(err / np.maximum(ref_scores, 1e-30)).max():.2e}")
+    kk = kernel if kernel > 0 else O.adaptive_kernel_size(L)
+    pooled = O.pool_max(ref_scores, kk)
+    got = kept[u, g].cpu().numpy()
+    cnt = min(L, keep)
+    assert int(out_len[u]) == cnt, tag
+    assert (got[cnt:] == -1).all(), tag
+    if L <= keep:
+        assert np.array_equal(got[:L], np.arange(L)), tag
+    else:
+        assert np.array_equal(got[keep - W:keep], np.arange(L - W, L)), f"{tag} window"
+        pre = got[:keep - W]
+        assert np.all(np.diff(pre) > 0), f"{tag} not ascending"
+        parity.check_selection(pre, pooled, keep - W, f"{tag} kept")
+    idx = got[:cnt]
+    assert np.array_equal(_f64(k_out[u, g, :cnt]), k[idx]), f"{tag} gathered K"
+    assert np.array_equal(_f64(v_out[u, g, :cnt]), v[idx]), f"{tag} gathered V"
+
+
+@pytest.mark.parametrize("keep", [256, 1024, 4096])
+def test_snapkv_tiny_config(keep):
+    # batch 1, 8 q / 2 kv heads, 4K prompt, W 32, pooling 7, 8 planted needles
+    rkv = _lib()
+    wl, x = _inputs(1, 2, 4, [4096], 32, seed=101, needles=8)
+    res = _run(rkv, x, 32, 7, keep)
+    for g in range(2):
+        _check_unit(x, 0, g, 4, 32, 7, keep, *res, tag=f"keep {keep} kv {g}")
+    if keep == 256:
+        kept = res[2].cpu().numpy()
+        for g in range(2):
+            assert set(x["needles"][0, g].tolist()) <= set(kept[0, g].tolist())
+
+
+def test_snapkv_window64_rows256_ragged():
+    # G * W = 256 (two 128-row blocks), ragged lengths incl. one <= keep and one not tile-aligned
+    rkv = _lib()
+    wl, x = _inputs(3, 2, 4, [5000, 700, 3333], 64, seed=102, needles=4)
+    res = _run(rkv, x, 64, 15, 1024)
+    for u in range(3):
+        for g in range(2):
+            _check_unit(x, u, g, 4, 64, 15, 1024, *res, tag=f"u{u} g{g}")
+
+
+@pytest.mark.parametrize("gqa,window", [(1, 32), (2, 48), (8, 16), (4, 5)])
+def test_snapkv_row_padding(gqa, window):
+    # G * W below 128 / between 128 and 256: padded query rows must not leak into the scores
+    rkv = _lib()
+    wl, x = _inputs(2, 2, gqa, [2047, 1500], window, seed=103 + gqa)
+    res = _run(rkv, x, window, 3, 512)
+    for u in range(2):
+        for g in range(2):
+            _check_unit(x, u, g, gqa, window, 3, 512, *res, tag=f"gqa{gqa} u{u} g{g}")
+
+
+def test_snapkv_adaptive_kernel_and_long_prompt():
+    # one 40K prompt (kernel 31 by the length rule) and one 9K prompt (kernel 15), many splits
+    rkv = _lib()
+    wl, x = _inputs(2, 1, 4, [40000, 9000], 32, seed=104, needles=16)
+    res = _run(rkv, x, 32, 0, 2048)
+    for u in range(2):
+        _check_unit(x, u, 0, 4, 32, 0, 2048, *res, tag=f"u{u}")
+
+
+def test_snapkv_multiple_waves():
+    # 6 units of 64K tokens: K of all units exceeds one L2-sized wave, so several waves run
+    rkv = _lib()
+    wl, x = _inputs(6, 1, 4, [65536, 65536, 60001, 65536, 1000, 65536], 32, seed=105)
+    res = _run(rkv, x, 32, 31, 4096)
+    for u in (0, 2, 4, 5):
+        _check_unit(x, u, 0, 4, 32, 31, 4096, *res, tag=f"u{u}")
+
+
+def test_snapkv_outlier_channels_128k_sample():
+    # 128K prompt with 4 outlier channels at 10x (large logits), budget 1024 -> keep 16384
+    rkv = _lib()
+    wl, x = _inputs(1, 2, 4, [131072], 32, seed=106, needles=64, outliers=4)
+    res = _run(rkv, x, 32, 31, 16384)
+    for g in range(2):
+        _check_unit(x, 0, g, 4, 32, 31, 16384, *res, tag=f"g{g}")
