@@ -1,0 +1,496 @@
+#!/usr/bin/env python
+"""Benchmark of the RocketKV hot path on GB300: decode steps/s of one full pass per step.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  SnapKV++ compression of every (layer, KV head) of the prompt  (score passes, select, gather)
+  + page summaries of the compact cache
+  + `decode_steps` hybrid sparse decode steps (each one launch over all layers and KV heads).
+Default workload: Llama-3.1-8B attention shapes (32 layers, 32 query / 8 KV heads, d 128, bf16),
+batch 1, 32K prompt, window 32, pooling 15, budget 256 (page 4, 32 of 128 channels, keep 4096),
+128 decode steps. value = decode steps per second over the whole pass (prompt compression
+included); the per-phase breakdown and the decode-only rate are reported beside it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the path has no
+exchange step); rank 0 prints the JSON line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode attention steps/s and HBM GB/s (% of peak) at 32K–128K ctx, budget 256"
+UNIT = "decode steps/s"
+FALLBACK_HBM = 6800.0
+FALLBACK_BF16 = 1900.0
+L2_BYTES = 129 * 1000 * 1000
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama8b_32k")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline leg")
+    ap.add_argument("--no-dense", action="store_true", help="skip the dense-decode comparison")
+    ap.add_argument("--seed", type=int, default=2000)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(
+            p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM, FALLBACK_BF16, 1700.0, "fallback"
+
+
+# --------------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------------- oracle CPU
+def _oracle_worker_init():
+    os.environ["OMP_NUM_THREADS"] = "1"
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+
+
+_UNIT_CACHE = {}
+
+
+def _unit_data(wl_name, unit, seed):
+    """One (layer, KV head) unit of the workload, drawn on the CPU in the worker (float64)."""
+    key = (wl_name, unit, seed)
+    if key not in _UNIT_CACHE:
+        from dataclasses import replace
+        from sparse_kv_cache_snapkv_gb300 import synthetic as S
+        wl = replace(S.WORKLOADS[wl_name], n_seq=1, n_layers=1, n_kv=1,
+                     lens=(S.WORKLOADS[wl_name].lens[0],))
+        x = S.prefill_inputs(wl, seed=seed + 7919 * unit, device="cpu")
+        if len(_UNIT_CACHE) >= 2:
+            _UNIT_CACHE.clear()
+        _UNIT_CACHE[key] = (x["k"][0, 0].double().numpy(), x["v"][0, 0].double().numpy(),
+                            x["q_win"][0].double().numpy(), int(x["seq_lens"][0]))
+    return _UNIT_CACHE[key]
+
+
+def _oracle_unit(args):
+    """Oracle work for one (layer, KV head) unit: compress + summaries + `steps` decode steps.
+    Returns (compress seconds, seconds per decode step); input drawing is not timed."""
+    import numpy as np
+    from oracle import rocketkv as O
+    wl_name, unit, seed, keep, kernel, budget, page, channels, steps = args
+    k, v, q_win, L = _unit_data(wl_name, unit, seed)
+    scale = 1.0 / math.sqrt(128)
+    t0 = time.perf_counter()
+    kept, kc, vc, _, _ = O.snapkv_compress(k[:L], v[:L], q_win, keep, kernel, scale)
+    n1 = kc.shape[0]
+    kmin, kmax = O.page_summaries(kc, n1, page)
+    t1 = time.perf_counter()
+    rng = np.random.default_rng(seed + unit)
+    for _ in range(steps):
+        q = rng.standard_normal((q_win.shape[0], 128))
+        O.hybrid_decode(q, kc, vc, n1, kmin, kmax, budget, page, channels, scale)
+    t2 = time.perf_counter()
+    return t1 - t0, (t2 - t1) / max(1, steps)
+
+
+def oracle_sample(wl, keep, kernel, units, cores, decode_sample, seed, pool):
+    """Time the oracle on `cores` units in parallel (one per core) and extrapolate a full step:
+    T = ceil(units / cores) * (t_compress + decode_steps * t_decode)."""
+    kernel = kernel or (7 if wl.max_len <= 8192 else 15 if wl.max_len <= 32768 else 31)
+    args = [(wl.name, i, seed, keep, kernel, wl.budget, wl.page, wl.channels, decode_sample)
+            for i in range(cores)]
+    t0 = time.perf_counter()
+    res = pool.map(_oracle_unit, args, chunksize=1)
+    wall = time.perf_counter() - t0
+    tc = statistics.mean(r[0] for r in res)
+    td = statistics.mean(r[1] for r in res)
+    full = math.ceil(units / cores) * (tc + wl.decode_steps * td)
+    return full, wall, tc, td
+
+
+# --------------------------------------------------------------------------------- helpers
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_config(wl, hp=None):
+    keep = hp.keep if hp else None
+    kernel = wl.kernel or (7 if wl.max_len <= 8192 else 15 if wl.max_len <= 32768 else 31)
+    return {"workload": wl.name, "layers": wl.n_layers, "batch": wl.n_seq, "q_heads": wl.n_q,
+            "kv_heads": wl.n_kv, "head_dim": 128, "ctx": wl.max_len, "window": wl.window,
+            "pool_kernel": kernel, "budget": wl.budget, "page": wl.page,
+            "channels": wl.channels, "keep": keep, "decode_steps_per_step": wl.decode_steps,
+            "append": wl.append, "needles": wl.needles,
+            "l2": "inputs larger than L2: prompt K/V %.2f GB per step, compact cache + summaries "
+                  "%.2f GB" % (2 * wl.n * wl.n_kv * wl.max_len * 256 / 1e9,
+                               (wl.n * wl.n_kv * (keep or 0) * 512 * 1.25) / 1e9),
+            "parallelism": "replicas"}
+
+
+# --------------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    from sparse_kv_cache_snapkv_gb300 import rkv, synthetic as S
+    from sparse_kv_cache_snapkv_gb300.pipeline import HotPath
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    rkv.load()
+    dev = torch.device("cuda", local)
+    wl = S.WORKLOADS[args.workload]
+    hbm_peak, bf16_peak, bf16_sus, peak_src = peaks()
+
+    # cpu-baseline pool first (spawn, before heavy GPU work)
+    pool = None
+    cores = min(16, len(os.sched_getaffinity(0)))
+    if rank == 0 and not args.no_cpu:
+        _oracle_worker_init_env()
+        pool = mp.get_context("spawn").Pool(cores, initializer=_oracle_worker_init)
+
+    x = S.prefill_inputs(wl, seed=args.seed + rank, device=dev)
+    dq = S.decode_queries(wl, wl.decode_steps, seed=args.seed + 500 + rank, device=dev)
+    nk = nv = None
+    if wl.append:
+        nk, nv = S.append_tokens(wl, wl.decode_steps, x["sigma"], seed=args.seed + 900, device=dev)
+    hp = HotPath(wl, x["k"], x["v"], x["q_win"], x["seq_lens"], dq, nk, nv)
+
+    # eager pass: sets kernel attributes, checks device status
+    hp.step()
+    torch.cuda.synchronize()
+    hp.check_status()
+
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    graphs = []
+    with torch.cuda.stream(stream):
+        for fn in (hp.compress, hp.summaries,
+                   lambda: [hp.decode(t) for t in range(wl.decode_steps)]):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            graphs.append(g)
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for g in graphs:
+                g.replay()
+        torch.cuda.synchronize()
+        hp.check_status()
+        barrier(world)
+        sampler = ClockSampler(local)
+        sampler.start()
+        time.sleep(0.3)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        barrier(world)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            graphs[0].replay()
+            ev[i][1].record(stream)
+            graphs[1].replay()
+            ev[i][2].record(stream)
+            graphs[2].replay()
+            ev[i][3].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        clocks = sampler.stop()
+    total_ms = ev[0][0].elapsed_time(ev[-1][3])
+    total_ms = max_over_ranks(total_ms, world)
+    comp_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    sum_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    dec_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    hp.check_status()
+
+    steps_total = args.steps * wl.decode_steps * world
+    value = steps_total / (total_ms / 1e3)
+    ms_per_step = total_ms / args.steps
+    dec_launch_us = dec_ms * 1e3 / wl.decode_steps
+    dec_bytes = hp.decode_bytes_per_launch()
+    dec_gbs = dec_bytes / (dec_launch_us * 1e-6) / 1e9
+    comp_bytes = hp.compress_bytes()
+    comp_gbs = comp_bytes / (comp_ms * 1e-3) / 1e9
+    comp_tflops = hp.compress_flops() / (comp_ms * 1e-3) / 1e12
+
+    # dominant phase -> roofline object
+    if dec_ms >= comp_ms:
+        roof = {"kernel": "hybrid_decode_kernel", "bound": "hbm", "achieved": round(dec_gbs, 1),
+                "peak": hbm_peak, "unit": "GB/s", "frac": round(dec_gbs / hbm_peak, 4),
+                "traffic": None, "peak_source": peak_src,
+                "bytes_per_launch": dec_bytes, "launch_us": round(dec_launch_us, 3)}
+    else:
+        roof = {"kernel": "snapkv compression (score passes + select + gather)", "bound": "hbm",
+                "achieved": round(comp_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(comp_gbs / hbm_peak, 4), "traffic": None,
+                "peak_source": peak_src, "bytes_per_launch": comp_bytes,
+                "launch_us": round(comp_ms * 1e3, 1)}
+    traffic = _profiled_traffic(roof["kernel"])
+    if traffic is not None:
+        roof["traffic"] = traffic
+
+    breakdown = {
+        "compress_ms": round(comp_ms, 4), "summaries_ms": round(sum_ms, 4),
+        "decode_ms": round(dec_ms, 4),
+        "decode_only_steps_per_s": round(wl.decode_steps / (dec_ms / 1e3) * world, 1),
+        "decode_launch_us": round(dec_launch_us, 3),
+        "decode_hbm_gbs": round(dec_gbs, 1), "decode_frac_of_peak": round(dec_gbs / hbm_peak, 4),
+        "compress_gbs": round(comp_gbs, 1), "compress_tflops": round(comp_tflops, 2),
+        "compress_frac_of_peak_hbm": round(comp_gbs / hbm_peak, 4),
+    }
+
+    # dense decode over the full prompt (the full-KV baseline), one launch over all units
+    if not args.no_dense:
+        breakdown["dense_decode"] = _dense_compare(hp, x, dq, wl, hbm_peak, stream, world)
+
+    # end-to-end: host buffers -> device -> the API calls -> result back to the host
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e(hp, x, dq, nk, nv, wl, stream, world, min(args.steps, 10))
+
+    # oracle on the host cores (rank 0 only)
+    cpu = None
+    if pool is not None:
+        oracle_sample(wl, hp.keep, wl.kernel, wl.n * wl.n_kv, cores, 1, args.seed, pool)
+        full_s, wall, tc, td = oracle_sample(wl, hp.keep, wl.kernel, wl.n * wl.n_kv, cores, 16,
+                                             args.seed, pool)
+        pool.close()
+        cpu = {"value": round(wl.decode_steps / full_s, 4), "unit": UNIT, "cores": cores,
+               "kind": "oracle",
+               "sample": (f"{cores} (layer, KV head) units of the same workload, one per core, "
+                          f"each: compression + summaries + 16 decode steps; per-unit mean "
+                          f"{tc:.3f} s compress, {td * 1e3:.2f} ms per decode step; "
+                          f"extrapolated to {wl.n * wl.n_kv} units x {wl.decode_steps} steps"),
+               "sample_wall_s": round(wall, 2)}
+
+    launches = hp.launches_per_step() * args.steps
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic (seeded; Llama-3.1-8B attention shapes, "
+                "random K/V with lognormal channel scales and planted needles)",
+                "config": workload_config(wl, hp), "roofline": roof, "cpu_baseline": cpu,
+                "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+                "breakdown": breakdown, "impl": "ours"}
+        print(json.dumps(line), flush=True)
+
+
+def _oracle_worker_init_env():
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+
+
+def _profiled_traffic(kernel_name):
+    """DRAM bytes per launch from the committed ncu summary of this kernel, when present."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        return t.get(kernel_name)
+    except Exception:
+        return None
+
+
+def _dense_compare(hp, x, dq, wl, hbm_peak, stream, world):
+    import torch
+    from sparse_kv_cache_snapkv_gb300 import rkv
+    n, n_kv = wl.n, wl.n_kv
+    out = torch.empty(n, wl.n_q, 128, dtype=torch.bfloat16, device=x["k"].device)
+    ws = rkv.workspace(rkv.rkv_dense_decode_workspace_bytes(n, n_kv, wl.gqa, wl.max_len),
+                       x["k"].device)
+    reps = 10
+    with torch.cuda.stream(stream):
+        for t in range(3):
+            rkv.rkv_dense_decode(dq[t], x["k"], x["v"], x["seq_lens"], hp.scale, out, ws=ws)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for t in range(reps):
+            rkv.rkv_dense_decode(dq[t % dq.shape[0]], x["k"], x["v"], x["seq_lens"], hp.scale,
+                                 out, ws=ws)
+        b.record(stream)
+        torch.cuda.synchronize()
+    rkv.rkv_check_status(ws)
+    ms = a.elapsed_time(b) / reps
+    byts = int(x["seq_lens"].sum().item()) * n_kv * 128 * 2 * 2 + n * wl.n_q * 128 * 4
+    gbs = byts / (ms * 1e-3) / 1e9
+    return {"steps_per_s": round(1e3 / ms * world, 2), "ms": round(ms, 4),
+            "hbm_gbs": round(gbs, 1), "frac_of_peak": round(gbs / hbm_peak, 4),
+            "bytes_per_launch": byts}
+
+
+def _e2e(hp, x, dq, nk, nv, wl, stream, world, steps):
+    import torch
+    dev_in = [x["k"], x["v"], x["q_win"], x["seq_lens"], dq]
+    if nk is not None:
+        dev_in += [nk, nv]
+    host_in = [t.cpu().pin_memory() for t in dev_in]
+    host_out = torch.empty(hp.out.shape, dtype=hp.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    with torch.cuda.stream(stream):
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            for d, h in zip(dev_in, host_in):
+                d.copy_(h, non_blocking=True)
+            hp.step()
+            host_out.copy_(hp.out, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+    hp.check_status()
+    ms = a.elapsed_time(b)
+    ms = max_over_ranks(ms, world)
+    return {"value": round(steps * wl.decode_steps * world / (ms / 1e3), 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms / steps, 3)}
+
+
+# --------------------------------------------------------------------------------- reference
+def run_reference(args):
+    """The oracle (plain fp64 CPU implementation) timed on the host cores, same metric/config."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from sparse_kv_cache_snapkv_gb300 import synthetic as S
+    wl = S.WORKLOADS[args.workload]
+    keep = wl.keep or min(wl.max_len, wl.budget * wl.page * 128 // wl.channels)
+    cores = min(16, len(os.sched_getaffinity(0)))
+    _oracle_worker_init_env()
+    pool = mp.get_context("spawn").Pool(cores, initializer=_oracle_worker_init)
+    dec_sample = 2
+    fulls = []
+    for i in range(args.warmup + args.steps):
+        full, wall, tc, td = oracle_sample(wl, keep, wl.kernel, wl.n * wl.n_kv, cores,
+                                           dec_sample, args.seed, pool)
+        if i >= args.warmup:
+            fulls.append(full)
+    pool.close()
+    step_s = statistics.mean(fulls)
+    value = wl.decode_steps / step_s
+    sample = (f"per step: {cores} (layer, KV head) units, one per core, each compression + "
+              f"summaries + {dec_sample} decode steps; extrapolated to {wl.n * wl.n_kv} units x "
+              f"{wl.decode_steps} decode steps")
+    line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "config": dict(workload_config(wl), keep=keep),
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -3,11 +3,42 @@
 #include <cuda_runtime.h>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
+#include <vector>
 
 #include "../../include/rkv.h"
 #include "rkv_internal.h"
 
 using namespace rkv;
+
+namespace rkv {
+
+cudaError_t ensure_dyn_smem(const void* func, size_t bytes) {
+  struct Entry {
+    const void* func;
+    int dev;
+    size_t bytes;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& x : done)
+    if (x.func == func && x.dev == dev && x.bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  for (Entry& x : done)
+    if (x.func == func && x.dev == dev) {
+      x.bytes = bytes;
+      return cudaSuccess;
+    }
+  done.push_back({func, dev, bytes});
+  return cudaSuccess;
+}
+
+}  // namespace rkv
 
 namespace {
 

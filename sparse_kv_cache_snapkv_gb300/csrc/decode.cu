@@ -411,8 +411,7 @@ cudaError_t launch_hybrid(const HybridArgs& a, cudaStream_t s) {
   switch (a.gqa) {
 #define RKV_CASE(GG)                                                                         \
   case GG:                                                                                   \
-    e = cudaFuncSetAttribute(hybrid_decode_kernel<GG>,                                       \
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);         \
+    e = ensure_dyn_smem((const void*)hybrid_decode_kernel<GG>, smem);                        \
     if (e != cudaSuccess) return e;                                                          \
     hybrid_decode_kernel<GG><<<grid, block, smem, s>>>(a);                                   \
     break;
@@ -690,8 +689,7 @@ cudaError_t launch_dense(const DenseArgs& a, cudaStream_t s) {
   switch (a.gqa) {
 #define RKV_CASE(GG)                                                                         \
   case GG:                                                                                   \
-    e = cudaFuncSetAttribute(dense_split_kernel<GG>,                                         \
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);         \
+    e = ensure_dyn_smem((const void*)dense_split_kernel<GG>, smem);                          \
     if (e != cudaSuccess) return e;                                                          \
     dense_split_kernel<GG><<<grid, block, smem, s>>>(a);                                     \
     break;

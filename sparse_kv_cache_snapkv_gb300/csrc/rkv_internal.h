@@ -70,6 +70,10 @@ struct DenseArgs {
   uint32_t* status;
 };
 
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device); later calls are
+// no-ops, so launches stay legal inside stream capture.
+cudaError_t ensure_dyn_smem(const void* func, size_t bytes);
+
 // split plan for dense decode, shared by the workspace query and the launch
 void dense_plan(int n, int n_kv, int max_len, int* nsplit, int* tokens_per_split);
 size_t dense_partials_bytes(int n, int n_kv, int gqa, int max_len);

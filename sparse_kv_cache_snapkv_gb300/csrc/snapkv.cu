@@ -556,8 +556,7 @@ template <int PASS, int RB>
 static cudaError_t launch_pass(const CUtensorMap& km, const CUtensorMap& qm,
                                const ScoreParams& sp, int nunits, cudaStream_t s) {
   const size_t smem = ScoreSmem<RB>::total;
-  cudaError_t e = cudaFuncSetAttribute(score_kernel<PASS, RB>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dyn_smem((const void*)score_kernel<PASS, RB>, smem);
   if (e != cudaSuccess) return e;
   score_kernel<PASS, RB><<<nunits * sp.nsplit, kScoreThreads, smem, s>>>(km, qm, sp);
   return cudaGetLastError();

@@ -1,0 +1,113 @@
+"""One pass of the RocketKV hot path over a batch: SnapKV++ compression of every (unit, KV head),
+page summaries of the compact cache, then `decode_steps` hybrid sparse decode steps (with a
+decode-token append before each step when the workload appends).
+
+Buffers are device tensors allocated here through torch (plumbing only); every step runs in
+librkv's kernels through the C ABI.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import rkv
+from .synthetic import Workload
+
+D = 128
+
+
+class HotPath:
+    def __init__(self, wl: Workload, k, v, q_win, seq_lens, dec_q, new_k=None, new_v=None,
+                 scale: float = 1.0 / math.sqrt(D)):
+        rkv.load()
+        self.wl = wl
+        self.k, self.v, self.q_win, self.seq_lens = k, v, q_win, seq_lens
+        self.dec_q = dec_q            # [steps, n, Hq, d]
+        self.new_k, self.new_v = new_k, new_v
+        self.scale = scale
+        dev = k.device
+        n, n_kv = wl.n, wl.n_kv
+        keep, page, channels, _ = rkv.rkv_plan(wl.max_len, wl.budget, D, wl.page, wl.channels)
+        self.keep = wl.keep or keep
+        self.page, self.channels = page, channels
+        steps = dec_q.shape[0]
+        self.cap = self.keep + (steps if wl.append else 0)
+        self.page_cap = ((self.cap + page - 1) // page + 7) // 8 * 8
+        self.k_out = torch.zeros(n, n_kv, self.cap, D, dtype=torch.bfloat16, device=dev)
+        self.v_out = torch.zeros_like(self.k_out)
+        self.kept = torch.empty(n, n_kv, self.keep, dtype=torch.int32, device=dev)
+        self.out_len = torch.zeros(n, dtype=torch.int32, device=dev)
+        self.length = torch.zeros(n, dtype=torch.int32, device=dev)   # decode-time length
+        self.kmin = torch.zeros(n, n_kv, D, self.page_cap, dtype=torch.bfloat16, device=dev)
+        self.kmax = torch.zeros_like(self.kmin)
+        self.out = torch.empty(steps, n, wl.n_q, D, dtype=torch.bfloat16, device=dev)
+        self.ws_snap = rkv.workspace(
+            rkv.rkv_snapkv_workspace_bytes(n, n_kv, wl.gqa, wl.max_len, wl.window), dev)
+        self.ws_sum = rkv.workspace(rkv.STATUS_BYTES, dev)
+        self.ws_dec = rkv.workspace(rkv.rkv_hybrid_decode_workspace_bytes(
+            n, n_kv, wl.gqa, self.page_cap, wl.budget, page), dev)
+
+    # individual phases ------------------------------------------------------------------
+    def compress(self):
+        rkv.rkv_snapkv_compress(self.k, self.v, self.seq_lens, self.q_win, self.wl.kernel,
+                                self.keep, self.scale, self.k_out, self.v_out, self.kept,
+                                self.out_len, ws=self.ws_snap)
+
+    def summaries(self):
+        # The decode-time length starts at the stage-1 length. With appends it grows, so it
+        # lives in its own array (a device-to-device copy); otherwise out_len is used as is.
+        if self.wl.append:
+            self.length.copy_(self.out_len)
+        else:
+            self.length = self.out_len
+        rkv.rkv_build_page_summaries(self.k_out, self.length, self.page, self.kmin, self.kmax,
+                                     ws=self.ws_sum)
+
+    def decode(self, t: int):
+        nk = self.new_k[t] if self.new_k is not None else None
+        nv = self.new_v[t] if self.new_v is not None else None
+        rkv.rkv_hybrid_decode(self.dec_q[t], self.k_out, self.v_out, self.length, self.kmin,
+                              self.kmax, self.wl.budget, self.page, self.channels, self.scale,
+                              self.out[t], new_k=nk, new_v=nv, ws=self.ws_dec)
+
+    def step(self):
+        self.compress()
+        self.summaries()
+        for t in range(self.dec_q.shape[0]):
+            self.decode(t)
+
+    def check_status(self):
+        for ws in (self.ws_snap, self.ws_sum, self.ws_dec):
+            rkv.rkv_check_status(ws)
+
+    # accounting ---------------------------------------------------------------------------
+    def launches_per_step(self) -> int:
+        """Kernel launches of one step (compress: 2 score passes per wave + select + gather)."""
+        unit_bytes = self.wl.max_len * D * 2
+        units = self.wl.n * self.wl.n_kv
+        wave = max(1, min(units, (64 << 20) // unit_bytes))
+        waves = (units + wave - 1) // wave
+        per_decode = 2 if self.wl.append else 1
+        return 2 * waves + 2 + 1 + per_decode * self.dec_q.shape[0]
+
+    def decode_bytes_per_launch(self) -> int:
+        """Algorithmic HBM bytes of one hybrid decode launch (all units), budget-implied:
+        per (unit, KV head): c rows of ceil(N1/p) bf16 summary values (one of Kmin / Kmax per
+        kept channel), (B/2) tokens of K and V rows, G query rows in and G output rows out."""
+        wl = self.wl
+        pages = (self.keep + self.page - 1) // self.page
+        per = (self.channels * pages * 2 + (wl.budget // 2) * D * 2 * 2 + 2 * wl.gqa * D * 2)
+        return wl.n * wl.n_kv * per
+
+    def compress_bytes(self) -> int:
+        """Algorithmic bytes of one compression: K read once, V rows of kept tokens read, kept
+        K / V rows written, window queries read."""
+        wl = self.wl
+        units = wl.n * wl.n_kv
+        return units * (wl.max_len * D * 2 + 3 * self.keep * D * 2) + wl.n * wl.n_q * wl.window * D * 2
+
+    def compress_flops(self) -> int:
+        """Tensor-core flops of the two score passes (2 GEMMs of (G*W) x L x d per unit)."""
+        wl = self.wl
+        return 2 * 2 * wl.n * wl.n_kv * wl.gqa * wl.window * wl.max_len * D
