@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
   int nsel;
   if (!dense) {
     // ---- channel pick: rank every channel (ties -> lower channel) ----------------------
+    bool pick = false;
     if (tid < kHeadDim) {
       const float mine = mag[tid];
       int rank = 0;
@@ -248,15 +249,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
         const float o = mag[j];
         rank += (o > mine) || (o == mine && j < tid);
       }
-      const bool pick = rank < a.channels;
-      const uint32_t b = __ballot_sync(0xffffffffu, pick);
-      if (lane == 0) ballots[warp] = b;
-      __syncwarp();
-      if (pick) {
-        int pos = __popc(b & ((1u << lane) - 1u));
-        for (int w = 0; w < warp; ++w) pos += __popc(ballots[w]);
-        chosen[pos] = tid;
-      }
+      pick = rank < a.channels;
+    }
+    const uint32_t picked = __ballot_sync(0xffffffffu, pick);
+    if (lane == 0 && warp < 4) ballots[warp] = picked;
+    __syncthreads();  // every warp's ballot is visible before any position is computed
+    if (pick) {
+      int pos = __popc(picked & ((1u << lane) - 1u));
+      for (int w = 0; w < warp; ++w) pos += __popc(ballots[w]);
+      chosen[pos] = tid;
+    }
+    if (tid == 0) {
+      const int total = __popc(ballots[0]) + __popc(ballots[1]) + __popc(ballots[2]) +
+                        __popc(ballots[3]);
+      if (total != a.channels) set_status(a.status, RKV_DEV_SELECT_FAILED);
     }
     __syncthreads();
     if (a.sel_channels && tid < a.channels)
@@ -275,7 +281,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
         float w[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          const int c = chosen[i + r];
+          const int c = chosen[i + r] & (kHeadDim - 1);
           w[r] = qg[c];
           const bf16* base = (w[r] >= 0.f) ? a.kmax : a.kmin;
           raw[r] = __ldg(reinterpret_cast<const uint4*>(
@@ -290,7 +296,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
         }
       }
       for (; i < a.channels; ++i) {
-        const int c = chosen[i];
+        const int c = chosen[i] & (kHeadDim - 1);
         const float w = qg[c];
         const bf16* base = (w >= 0.f) ? a.kmax : a.kmin;
         const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
