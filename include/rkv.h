@@ -50,7 +50,8 @@ typedef enum {
   RKV_ERR_UNSUPPORTED = 2,
   RKV_ERR_WORKSPACE = 3,
   RKV_ERR_CUDA = 4,
-  RKV_ERR_DEVICE_STATUS = 5
+  RKV_ERR_DEVICE_STATUS = 5,
+  RKV_ERR_TOO_LARGE = 6
 } rkv_status;
 
 /* Device status bits (reported by rkv_check_status through *bits). */
@@ -174,6 +175,31 @@ size_t rkv_dense_decode_workspace_bytes(int n, int n_kv, int gqa, int max_len);
 rkv_status rkv_dense_decode(const void* q, const void* k, const void* v, const int32_t* len,
                             int n, int n_kv, int gqa, int head_dim, int max_len, float scale,
                             void* out, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------------ */
+/* Allocation-free dense decode (a library convenience; the paper has no counterpart)          */
+/* ------------------------------------------------------------------------------------------ */
+/* Same computation, arguments and layouts as rkv_dense_decode, but without ws / ws_bytes: the
+ * split-K partials go to an 8 MiB array of device memory that the library reserves statically
+ * (every GPU that loads the library holds it until the process exits).
+ *
+ * It exists for callers that cannot call cudaMalloc to build a workspace: code that is only
+ * handed its input and output tensors (a plugin boundary, say), a host whose device memory
+ * belongs entirely to its own pool, or a region being recorded into a CUDA graph. The caller
+ * still passes inputs and outputs; nothing is allocated or freed by this call.
+ *
+ *  - Limit: 256 B + the partials of rkv_dense_decode_workspace_bytes(n, n_kv, gqa, max_len) must
+ *    fit in 8 MiB; otherwise RKV_ERR_TOO_LARGE is returned and nothing is launched.
+ *  - Set-up: the first call on each device looks up the device address of the array (with that
+ *    device current). Make that first call before any stream capture.
+ *  - All calls share the one array, which keeps the last call's contents. Each call clears the
+ *    status word at its start; calls that overlap on the GPU (different streams, or different
+ *    host threads) race on the array and must be serialised by the caller.
+ *  - Device-detected inconsistencies (len > max_len is clamped) are not reported by this entry
+ *    point. */
+rkv_status rkv_dense_decode_noalloc(const void* q, const void* k, const void* v,
+                                    const int32_t* len, int n, int n_kv, int gqa, int head_dim,
+                                    int max_len, float scale, void* out, void* stream);
 
 #ifdef __cplusplus
 }

@@ -62,6 +62,7 @@ const char* rkv_status_string(rkv_status s) {
     case RKV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case RKV_ERR_CUDA: return "CUDA launch or runtime error";
     case RKV_ERR_DEVICE_STATUS: return "kernel reported inconsistent device data";
+    case RKV_ERR_TOO_LARGE: return "problem too large for the fixed scratch of the allocation-free call";
   }
   return "unknown status";
 }

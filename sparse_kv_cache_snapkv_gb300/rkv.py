@@ -19,7 +19,8 @@ _lib = None
 
 RKV_OK = 0
 _STATUS = {0: "RKV_OK", 1: "RKV_ERR_INVALID_ARG", 2: "RKV_ERR_UNSUPPORTED",
-           3: "RKV_ERR_WORKSPACE", 4: "RKV_ERR_CUDA", 5: "RKV_ERR_DEVICE_STATUS"}
+           3: "RKV_ERR_WORKSPACE", 4: "RKV_ERR_CUDA", 5: "RKV_ERR_DEVICE_STATUS",
+           6: "RKV_ERR_TOO_LARGE"}
 STATUS_BYTES = 256
 HEAD_DIM = 128
 
@@ -27,7 +28,7 @@ SYMBOLS = [
     "rkv_status_string", "rkv_check_status", "rkv_plan", "rkv_snapkv_workspace_bytes",
     "rkv_snapkv_compress", "rkv_summaries_workspace_bytes", "rkv_build_page_summaries",
     "rkv_hybrid_decode_workspace_bytes", "rkv_hybrid_decode",
-    "rkv_dense_decode_workspace_bytes", "rkv_dense_decode",
+    "rkv_dense_decode_workspace_bytes", "rkv_dense_decode", "rkv_dense_decode_noalloc",
 ]
 
 
@@ -74,6 +75,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         "rkv_dense_decode_workspace_bytes": ([i32, i32, i32, i32], sz),
         "rkv_dense_decode": ([vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, sz, vp],
                              i32),
+        "rkv_dense_decode_noalloc": ([vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp],
+                                     i32),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -221,3 +224,14 @@ def rkv_dense_decode(q, k, v, length, scale: float, out, ws=None, stream=None):
                                    _stream(stream))
     _check("rkv_dense_decode", code)
     return ws
+
+
+def rkv_dense_decode_noalloc(q, k, v, length, scale: float, out, stream=None):
+    """Dense decode without a workspace: the library's fixed device scratch holds the partials.
+    For callers that cannot allocate; calls sharing the scratch must not overlap on the GPU."""
+    _bf16(q, "q"), _bf16(k, "k"), _i32(length, "len")
+    n, n_kv, max_len, d = k.shape
+    gqa = q.shape[1] // n_kv
+    code = load().rkv_dense_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(length), n, n_kv, gqa,
+                                           d, max_len, float(scale), _ptr(out), _stream(stream))
+    _check("rkv_dense_decode_noalloc", code)
