@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline leg")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense-decode comparison")
     ap.add_argument("--seed", type=int, default=2000)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run the workload with this many layers (smaller profiling cases)")
     return ap.parse_args()
 
 
@@ -236,6 +238,8 @@ def run_ours(args):
     rkv.load()
     dev = torch.device("cuda", local)
     wl = S.WORKLOADS[args.workload]
+    if args.layers:
+        wl = wl.with_layers(args.layers)
     hbm_peak, bf16_peak, bf16_sus, peak_src = peaks()
 
     # cpu-baseline pool first (spawn, before heavy GPU work)
