@@ -9,9 +9,15 @@
 // Direct Latency Comparison" (half of the budget to the approximation, half to exact sparse
 // attention), "Are Different KV Tokens Retrieved at Each Decoding Step?" (selection per step).
 //
-// Memory movement: K/V rows of the selected pages are staged in shared memory by
-// cp.async.bulk (one copy per page and tensor, completion on an mbarrier, kStages stages in
-// flight); summary rows are read with 16-byte vector loads, 8 pages per load.
+// Memory movement: the kept channels' summary rows and the K/V rows of the selected pages are
+// staged in shared memory by cp.async.bulk (one copy per row, all of a stage in flight at once,
+// completion on an mbarrier). K/V rows are stored 272 bytes apart so that ldmatrix reads them
+// without bank conflicts.
+//
+// Attention arithmetic: warp-level mma.sync m16n8k16 (bf16 in, fp32 accumulate). The G query
+// heads of a KV group are the rows of the A operand (padded to 16 with zeros); each warp takes 16
+// tokens at a time: S = Q K^T (16 MMAs), an online softmax on the accumulator fragments, and
+// O += P V (16 MMAs) with P re-packed from the accumulators as the next A operand.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -21,105 +27,135 @@
 
 namespace rkv {
 
-// ==========================================================================================
-// Warp-level online-softmax attention over rows staged in shared memory.
-//
-// Lane layout for q.k: lane = 8 * ts + e; ts (0..3) picks one of 4 tokens, e (0..7) owns 16
-// channels [16e, 16e + 16) as two 16-byte chunks. Lanes e >= 4 read their two chunks in swapped
-// order so that every quarter-warp touches 8 distinct 16-byte bank groups (conflict-free).
-// Lane layout for p.v: lane owns output channels [4 * lane, 4 * lane + 4).
-// Scores live in the log2 domain (q is pre-scaled by scale * log2(e)).
-// ==========================================================================================
+constexpr int kRowPad = 136;                                    // staged row stride (bf16)
+constexpr int kStageElems = 2 * kChunkTokens * kRowPad;         // K rows then V rows
+constexpr int kStageBytes = kStageElems * 2;                    // 34,816 B
+constexpr int kDecStages = 2;                                   // one per warp group
+
+// ------------------------------------------------------------------------------------------
+// warp-level MMA helpers
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                          uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D = A B + C for one m16n8k16 tile; only A rows 0..7 are ever non-zero here, so a1 = a3 = 0
+// and the outputs of rows 8..15 are dropped.
+__device__ __forceinline__ void mma_rows8(float& d0, float& d1, uint32_t a0, uint32_t a2,
+                                          uint32_t b0, uint32_t b1) {
+  float x2 = 0.f, x3 = 0.f;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d0), "+f"(d1), "+f"(x2), "+f"(x3)
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------------------------------------------
+// Warp attention state over 16-token groups of a stage.
+// Lane roles (m16n8k16 fragments): r0 = lane / 4 is the query-head row (rows >= G are zero
+// padding), t = lane % 4 picks the column pair 2t, 2t+1 of every 8-wide tile.
+// ------------------------------------------------------------------------------------------
 template <int G>
-struct WarpAttn {
-  float m[G];
-  float l[G];
-  float acc[G][4];
-  float qr[G][16];
-  int lane, ts, e, sw;
+struct MmaAttn {
+  const uint2* qf;  // Q A-fragments in shared memory: qf[ks * 32 + lane] = {a0, a2}
+  float m, l;       // running max (log2 domain) and sum for row r0 (partial per lane)
+  float o[16][2];   // row r0, channels 8nt + 2t, 8nt + 2t + 1
+  int lane, r0, t;
 
-  __device__ __forceinline__ void init(const float* qs /* [G][128], scaled */) {
+  // Q fragments are shared by every warp of the CTA: built once in shared memory by one warp
+  // (row r0 = lane / 4 < G holds query head r0; rows >= G are zero).
+  static __device__ __forceinline__ void build_fragments(const bf16* q_group, uint2* frag) {
+    const int ln = threadIdx.x & 31, rr = ln >> 2, tt = ln & 3;
+    const uint32_t* qw = reinterpret_cast<const uint32_t*>(q_group + rr * kHeadDim);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+      frag[ks * 32 + ln] = (rr < G) ? make_uint2(qw[ks * 8 + tt], qw[ks * 8 + 4 + tt])
+                                    : make_uint2(0u, 0u);
+  }
+
+  __device__ __forceinline__ void init(const uint2* frag) {
     lane = threadIdx.x & 31;
-    ts = lane >> 3;
-    e = lane & 7;
-    sw = (e >> 2) & 1;
+    r0 = lane >> 2;
+    t = lane & 3;
+    qf = frag;
+    m = -1e30f;
+    l = 0.f;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      m[h] = -1e30f;
-      l[h] = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[h][j] = 0.f;
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) qr[h][jj * 8 + i] = qs[h * 128 + 16 * e + 8 * (jj ^ sw) + i];
-    }
+    for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = 0.f;
   }
 
-  // Tokens t0 .. t0+3 of a stage holding `ntok` valid rows.
-  __device__ __forceinline__ void step4(const bf16* Ks, const bf16* Vs, int t0, int ntok) {
-    const int tk = t0 + ts;
-    const bool valid = tk < ntok;
-    float dot[G];
+  // tokens tok0 .. tok0 + 15 of a stage with `ntok` valid rows (rows >= ntok of V are zero)
+  __device__ __forceinline__ void step16(const bf16* Ks, const bf16* Vs, int tok0, int ntok,
+                                         float scale_log2) {
+    float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
+    {
+      const int n = (lane & 7) + ((lane >> 4) << 3), kh = (lane >> 3) & 1;
+      const uint32_t base = smem_addr(Ks + (tok0 + n) * kRowPad + kh * 8);
 #pragma unroll
-    for (int h = 0; h < G; ++h) dot[h] = 0.f;
-    if (valid) {
-      const uint4* row = reinterpret_cast<const uint4*>(Ks + tk * kHeadDim);
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const uint4 c = row[2 * e + (jj ^ sw)];
-        float f[8];
-        unpack8(c, f);
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) dot[h] = fmaf(qr[h][jj * 8 + i], f[i], dot[h]);
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(base + ks * 32, b0, b1, b2, b3);
+        const uint2 qa = qf[ks * 32 + lane];
+        mma_rows8(s00, s01, qa.x, qa.y, b0, b1);
+        mma_rows8(s10, s11, qa.x, qa.y, b2, b3);
       }
     }
-    float p[G], alpha[G];
+    const int j = tok0 + 2 * t;
+    float s[4] = {s00 * scale_log2, s01 * scale_log2, s10 * scale_log2, s11 * scale_log2};
+    s[0] = (j < ntok) ? s[0] : -INFINITY;
+    s[1] = (j + 1 < ntok) ? s[1] : -INFINITY;
+    s[2] = (j + 8 < ntok) ? s[2] : -INFINITY;
+    s[3] = (j + 9 < ntok) ? s[3] : -INFINITY;
+    float mt = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+    const float mn = fmaxf(m, mt);
+    const float alpha = exp2f(m - mn);
+    m = mn;
+    // P in bf16 (the A operand of P V); l sums the same rounded values
+    const __nv_bfloat162 p01 = __floats2bfloat162_rn(exp2f(s[0] - mn), exp2f(s[1] - mn));
+    const __nv_bfloat162 p23 = __floats2bfloat162_rn(exp2f(s[2] - mn), exp2f(s[3] - mn));
+    const float2 f01 = __bfloat1622float2(p01), f23 = __bfloat1622float2(p23);
+    l = l * alpha + ((f01.x + f01.y) + (f23.x + f23.y));
+    const uint32_t pa0 = *reinterpret_cast<const uint32_t*>(&p01);
+    const uint32_t pa2 = *reinterpret_cast<const uint32_t*>(&p23);
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float d = dot[h];
-      d += __shfl_xor_sync(0xffffffffu, d, 1);
-      d += __shfl_xor_sync(0xffffffffu, d, 2);
-      d += __shfl_xor_sync(0xffffffffu, d, 4);
-      const float s = valid ? d : -INFINITY;
-      float mt = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 8));
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-      const float mn = fmaxf(m[h], mt);
-      alpha[h] = exp2f(m[h] - mn);
-      p[h] = exp2f(s - mn);
-      m[h] = mn;
-      l[h] = l[h] * alpha[h] + p[h];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[h][j] *= alpha[h];
+    for (int nt = 0; nt < 16; ++nt) {
+      o[nt][0] *= alpha;
+      o[nt][1] *= alpha;
     }
+    {
+      const int tr = (lane & 7) + (((lane >> 3) & 1) << 3), cb = (lane >> 4) << 3;
+      const uint32_t base = smem_addr(Vs + (tok0 + tr) * kRowPad + cb);
 #pragma unroll
-    for (int uu = 0; uu < 4; ++uu) {
-      if (t0 + uu < ntok) {
-        const uint2 vv =
-            *reinterpret_cast<const uint2*>(Vs + (t0 + uu) * kHeadDim + 4 * lane);
-        const float vf[4] = {bf16_lo(vv.x), bf16_hi(vv.x), bf16_lo(vv.y), bf16_hi(vv.y)};
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float pu = __shfl_sync(0xffffffffu, p[h], uu * 8);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[h][j] = fmaf(pu, vf[j], acc[h][j]);
-        }
+      for (int np = 0; np < 8; ++np) {
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_t(base + np * 32, v0, v1, v2, v3);
+        mma_rows8(o[2 * np][0], o[2 * np][1], pa0, pa2, v0, v1);
+        mma_rows8(o[2 * np + 1][0], o[2 * np + 1][1], pa0, pa2, v2, v3);
       }
     }
   }
 
-  // Sum of l over the 4 token slots (every e-class ends up with the full sum).
-  __device__ __forceinline__ float total_l(int h) const {
-    float t = l[h];
-    t += __shfl_xor_sync(0xffffffffu, t, 8);
-    t += __shfl_xor_sync(0xffffffffu, t, 16);
-    return t;
+  __device__ __forceinline__ float row_l() const {
+    float x = l;
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    return x;
   }
 };
 
-// Shared-memory layout of the warp-combine step (re-uses the stage buffers).
 template <int G>
 struct CombineSmem {
   float m[8][G];
@@ -127,23 +163,24 @@ struct CombineSmem {
   float o[8][G][kHeadDim];
 };
 
-// Each warp deposits its state; afterwards thread i < G*128 owns (h, c) = (i / 128, i % 128).
 template <int G>
-__device__ __forceinline__ void warp_deposit(const WarpAttn<G>& wa, CombineSmem<G>* cs) {
+__device__ __forceinline__ void warp_deposit(const MmaAttn<G>& at, CombineSmem<G>* cs) {
   const int w = threadIdx.x >> 5;
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const float lt = wa.total_l(h);
-    if (wa.lane == 0) {
-      cs->m[w][h] = wa.m[h];
-      cs->l[w][h] = lt;
+  const float lt = at.row_l();
+  if (at.r0 < G) {
+    if (at.t == 0) {
+      cs->m[w][at.r0] = at.m;
+      cs->l[w][at.r0] = lt;
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) cs->o[w][h][4 * wa.lane + j] = wa.acc[h][j];
+    for (int nt = 0; nt < 16; ++nt) {
+      cs->o[w][at.r0][nt * 8 + 2 * at.t] = at.o[nt][0];
+      cs->o[w][at.r0][nt * 8 + 2 * at.t + 1] = at.o[nt][1];
+    }
   }
 }
 
-// Merge the 8 warps for (h, c): returns unnormalised output relative to max M, with L.
+// Merge the 8 warps for (h, c): unnormalised output relative to max M, with its sum L.
 template <int G>
 __device__ __forceinline__ void warp_merge(const CombineSmem<G>* cs, int h, int c, float* M,
                                            float* L, float* O) {
@@ -162,19 +199,32 @@ __device__ __forceinline__ void warp_merge(const CombineSmem<G>* cs, int h, int 
   *O = oo;
 }
 
-// ==========================================================================================
-// Hybrid sparse decode: one CTA per (unit, KV head).
-// ==========================================================================================
-constexpr int kStageBytes = 2 * kChunkTokens * kHeadDim * 2;  // K + V rows of one stage
+// Zero V rows [ntok, round_up(ntok, 16)) of a partially filled stage so that P = 0 never meets
+// stale bits there (0 * NaN would poison the accumulators). Called by the 128 threads of a group.
+__device__ __forceinline__ void zero_tail_rows(bf16* Vs, int ntok, int gtid) {
+  const int r1 = min(kChunkTokens, (ntok + 15) & ~15);
+  const int n16 = (r1 - ntok) * 16;  // 16-byte words
+  for (int i = gtid; i < n16; i += 128) {
+    const int r = ntok + (i >> 4), c = i & 15;
+    *reinterpret_cast<uint4*>(Vs + r * kRowPad + c * 8) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  fence_proxy_async();
+}
 
+__device__ __forceinline__ void group_sync(int group) {
+  asm volatile("bar.sync %0, 128;" ::"r"(1 + group) : "memory");
+}
+
+// ==========================================================================================
+// Hybrid sparse decode: one CTA of 8 warps per (unit, KV head).
+// ==========================================================================================
 size_t hybrid_smem_bytes(int gqa, int page_cap, int budget, int page) {
-  const int nsel_max = page_cap;  // selected-page list (dense path may select every page)
-  size_t b = (size_t)kStages * kStageBytes;   // stages (re-used by the warp combine)
-  b += align_up((size_t)page_cap * 4, 16);    // approximate scores
-  b += align_up((size_t)nsel_max * 4, 16);    // selected pages
   (void)gqa;
   (void)budget;
   (void)page;
+  size_t b = (size_t)kDecStages * kStageBytes;  // stages (also summary rows, warp combine)
+  b += align_up((size_t)page_cap * 4, 16);       // approximate scores
+  b += align_up((size_t)page_cap * 4, 16);       // selected pages
   return b;
 }
 
@@ -185,13 +235,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
   __shared__ float mag[kHeadDim];
   __shared__ float qg[kHeadDim];
   __shared__ int chosen[kHeadDim];
-  __shared__ uint32_t ballots[4];
-  __shared__ __align__(8) uint64_t bars[kStages];
-  __shared__ SelectScratch sc;
+  __shared__ float wsel[kHeadDim];
+  __shared__ __align__(8) uint64_t sbar;
+  __shared__ union {
+    SelectScratch generic;
+    FastSelectSmem fast;
+  } sel_smem;
+  __shared__ uint2 qfrag[8 * 32];
+  __shared__ uint2 wfrag[8 * 32];
 
   bf16* stages = reinterpret_cast<bf16*>(smem);
-  float* scores = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);
-  int* sel = reinterpret_cast<int*>(smem + (size_t)kStages * kStageBytes +
+  float* scores = reinterpret_cast<float*>(smem + (size_t)kDecStages * kStageBytes);
+  int* sel = reinterpret_cast<int*>(smem + (size_t)kDecStages * kStageBytes +
                                     align_up((size_t)a.page_cap * 4, 16));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -199,6 +254,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
   const int u = ukv / a.n_kv;
   const int g = ukv - u * a.n_kv;
   const int hq = a.n_kv * G;
+  pdl_wait();     // inputs may come from the kernel before this one in the stream
+  pdl_trigger();  // the next decode step may be scheduled while this one runs
   const int len = a.len[u];
   const int p = a.page;
   const int P = (len + p - 1) / p;
@@ -209,18 +266,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
     if (tid == 0 && len != 0) set_status(a.status, RKV_DEV_LEN_OVER_CAP);
     return;
   }
+  const bf16* qgroup = a.q + ((size_t)u * hq + g * G) * kHeadDim;
 
   // ---- q: raw values to shared memory -------------------------------------------------
   if (tid < G * 16) {
     const int h = tid >> 4, c8 = (tid & 15) * 8;
-    const uint4 c = *reinterpret_cast<const uint4*>(
-        a.q + ((size_t)u * hq + g * G + h) * kHeadDim + c8);
+    const uint4 c = *reinterpret_cast<const uint4*>(qgroup + h * kHeadDim + c8);
     float f[8];
     unpack8(c, f);
 #pragma unroll
     for (int i = 0; i < 8; ++i) qs[h * kHeadDim + c8 + i] = f[i];
   }
-  if (tid < kStages) mbar_init(&bars[tid], 1);
+  if (warp == 7) MmaAttn<G>::build_fragments(qgroup, qfrag);
+  if (tid == 0) mbar_init(&sbar, 1);
   fence_barrier_init();
   __syncthreads();
 
@@ -240,89 +298,122 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
 
   int nsel;
   if (!dense) {
-    // ---- channel pick: rank every channel (ties -> lower channel) ----------------------
-    bool pick = false;
-    if (tid < kHeadDim) {
-      const float mine = mag[tid];
-      int rank = 0;
-      for (int j = 0; j < kHeadDim; ++j) {
-        const float o = mag[j];
-        rank += (o > mine) || (o == mine && j < tid);
-      }
-      pick = rank < a.channels;
+    // ---- channel pick: top-c of sum_h |q_h| (ties -> lower channel), ascending -----------
+    {
+      const int got = block_topk_fast<1>(mag, kHeadDim, a.channels, chosen, sel_smem.fast);
+      if (got != a.channels && tid == 0) set_status(a.status, RKV_DEV_SELECT_FAILED);
     }
-    const uint32_t picked = __ballot_sync(0xffffffffu, pick);
-    if (lane == 0 && warp < 4) ballots[warp] = picked;
-    __syncthreads();  // every warp's ballot is visible before any position is computed
-    if (pick) {
-      int pos = __popc(picked & ((1u << lane) - 1u));
-      for (int w = 0; w < warp; ++w) pos += __popc(ballots[w]);
-      chosen[pos] = tid;
-    }
-    if (tid == 0) {
-      const int total = __popc(ballots[0]) + __popc(ballots[1]) + __popc(ballots[2]) +
-                        __popc(ballots[3]);
-      if (total != a.channels) set_status(a.status, RKV_DEV_SELECT_FAILED);
+    if (tid < a.channels) {
+      wsel[tid] = qg[chosen[tid] & (kHeadDim - 1)];
+      if (a.sel_channels) a.sel_channels[(size_t)ukv * a.channels + tid] = chosen[tid];
     }
     __syncthreads();
-    if (a.sel_channels && tid < a.channels)
-      a.sel_channels[(size_t)ukv * a.channels + tid] = chosen[tid];
 
-    // ---- approximate page scores: 8 pages per 16-byte load, one load per kept channel ----
-    const int nchunk = (P + 7) >> 3;
-    const size_t rowbase = (size_t)ukv * kHeadDim;
-    for (int ch = tid; ch < nchunk; ch += kDecodeThreads) {
-      float s8[8];
+    // ---- approximate page scores on the tensor cores ------------------------------------
+    // score[pg] = sum_i w_i R_i[pg] for the kept channels' summary rows R_i (Kmax where
+    // q_g >= 0, else Kmin), staged in shared memory by one bulk copy per row (one memory round
+    // trip), rows np16 + 8 elements apart so that ldmatrix.trans reads them conflict-free. Each
+    // m16n8k16 MMA takes 16 channels x 8 pages: A row 0 holds bf16(w) and row 1 the bf16 remainder
+    // w - bf16(w) (together ~16 bits of w), so score = D[0] + D[1], accumulated in fp32.
+    const int cn = a.channels;
+    const int nks = (cn + 15) >> 4;  // 16-channel steps
+    if (warp == 0) {
+      for (int ks = 0; ks < nks; ++ks) {
+        const int r0 = lane >> 2, t = lane & 3;
+        uint32_t v0 = 0u, v2 = 0u;
+        if (r0 < 2) {
+          float w4[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) s8[j] = 0.f;
-      int i = 0;
-      for (; i + 4 <= a.channels; i += 4) {
-        uint4 raw[4];
-        float w[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int c = chosen[i + r] & (kHeadDim - 1);
-          w[r] = qg[c];
-          const bf16* base = (w[r] >= 0.f) ? a.kmax : a.kmin;
-          raw[r] = __ldg(reinterpret_cast<const uint4*>(
-              base + (rowbase + c) * a.page_cap + (size_t)ch * 8));
+          for (int e = 0; e < 4; ++e) {
+            const int i = ks * 16 + 2 * t + (e & 1) + (e >> 1) * 8;
+            const float w = i < cn ? wsel[i] : 0.f;
+            const float whi = __bfloat162float(__float2bfloat16_rn(w));
+            w4[e] = r0 == 0 ? whi : (w - whi);
+          }
+          v0 = pack_bf16x2(w4[0], w4[1]);
+          v2 = pack_bf16x2(w4[2], w4[3]);
         }
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          float f[8];
-          unpack8(raw[r], f);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) s8[j] = fmaf(w[r], f[j], s8[j]);
-        }
-      }
-      for (; i < a.channels; ++i) {
-        const int c = chosen[i] & (kHeadDim - 1);
-        const float w = qg[c];
-        const bf16* base = (w >= 0.f) ? a.kmax : a.kmin;
-        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
-            base + (rowbase + c) * a.page_cap + (size_t)ch * 8));
-        float f[8];
-        unpack8(raw, f);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) s8[j] = fmaf(w, f[j], s8[j]);
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int pg = ch * 8 + j;
-        if (pg < P) {
-          scores[pg] = s8[j];
-          if (a.approx) a.approx[(size_t)ukv * a.page_cap + pg] = s8[j];
-        }
+        wfrag[ks * 32 + lane] = make_uint2(v0, v2);
       }
     }
-    __syncthreads();
+    const int Ppad = (P + 7) & ~7;
+    int pblk = ((int)(((size_t)kDecStages * kStageBytes) / ((size_t)nks * 32)) - 8) & ~15;
+    if (pblk > Ppad) pblk = (Ppad + 15) & ~15;
+    const size_t rowbase = (size_t)ukv * kHeadDim;
+    uint32_t sphase = 0;
+    for (int pb = 0; pb < Ppad; pb += pblk) {
+      const int np = min(pblk, Ppad - pb);  // pages copied (a multiple of 8)
+      const int np16 = (np + 15) & ~15;      // pages multiplied (a multiple of 16)
+      const int rs = np16 + 8;               // staged row stride (elements)
+      if (warp == 0) {
+        if (lane == 0) mbar_arrive_expect_tx(&sbar, (uint32_t)(cn * np * 2));
+        __syncwarp();
+        for (int i = lane; i < cn; i += 32) {
+          const int c = chosen[i] & (kHeadDim - 1);
+          const bf16* base = (qg[c] >= 0.f) ? a.kmax : a.kmin;
+          bulk_g2s(stages + (size_t)i * rs, base + (rowbase + c) * a.page_cap + pb,
+                   (uint32_t)(np * 2), &sbar);
+        }
+      }
+      // channel rows past cn (up to the 16-step) are multiplied by zero weights: make them zero
+      for (int i = tid; i < (nks * 16 - cn) * (rs / 8); i += kDecodeThreads) {
+        const int r = cn + i / (rs / 8), c8 = i % (rs / 8);
+        *reinterpret_cast<uint4*>(stages + (size_t)r * rs + c8 * 8) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      const bool ok = mbar_wait(&sbar, sphase);
+      sphase ^= 1u;
+      if (__syncthreads_or(!ok)) {
+        if (tid == 0) set_status(a.status, RKV_DEV_WAIT_TIMEOUT);
+        mbar_wait(&sbar, sphase ^ 1u);  // let the copies land before the CTA retires
+        return;
+      }
+      const int t = lane & 3;
+      const int krow = (lane & 7) + (((lane >> 3) & 1) << 3), pcol = (lane >> 4) << 3;
+      for (int pair = warp; pair < (np16 >> 4); pair += kDecodeThreads / 32) {
+        const int p0 = pair * 16;
+        float d0 = 0.f, d1 = 0.f, e0 = 0.f, e1 = 0.f;
+        const uint32_t base = smem_addr(stages + (size_t)krow * rs + p0 + pcol);
+        for (int ks = 0; ks < nks; ++ks) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(base + (uint32_t)(ks * 16 * rs * 2), b0, b1, b2, b3);
+          const uint2 wa = wfrag[ks * 32 + lane];
+          mma_rows8(d0, d1, wa.x, wa.y, b0, b1);
+          mma_rows8(e0, e1, wa.x, wa.y, b2, b3);
+        }
+        // row 0 (lanes 0..3) + row 1 (lanes 4..7)
+        d0 += __shfl_down_sync(0xffffffffu, d0, 4);
+        d1 += __shfl_down_sync(0xffffffffu, d1, 4);
+        e0 += __shfl_down_sync(0xffffffffu, e0, 4);
+        e1 += __shfl_down_sync(0xffffffffu, e1, 4);
+        if (lane < 4) {
+          const float v4[4] = {d0, d1, e0, e1};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int pg = pb + p0 + 2 * t + (e & 1) + (e >> 1) * 8;
+            if (pg < P && pg < pb + np) {
+              scores[pg] = v4[e];
+              if (a.approx) a.approx[(size_t)ukv * a.page_cap + pg] = v4[e];
+            }
+          }
+        }
+      }
+      __syncthreads();  // the staging area is refilled by the next block / the K/V stages
+    }
 
     // ---- page top-k ----------------------------------------------------------------------
     if (S >= P) {
       for (int i = tid; i < P; i += kDecodeThreads) sel[i] = i;
       nsel = P;
     } else {
-      const int got = block_topk_ascending(scores, P, S, sel, sc);
+      int got;
+      if (P <= 1024)
+        got = block_topk_fast<4>(scores, P, S, sel, sel_smem.fast);
+      else if (P <= 2048)
+        got = block_topk_fast<8>(scores, P, S, sel, sel_smem.fast);
+      else if (P <= 4096)
+        got = block_topk_fast<16>(scores, P, S, sel, sel_smem.fast);
+      else
+        got = block_topk_ascending(scores, P, S, sel, sel_smem.generic);
       if (got != S && tid == 0) set_status(a.status, RKV_DEV_SELECT_FAILED);
       nsel = S;
     }
@@ -338,69 +429,54 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
   }
 
   // ---- exact attention over the selected pages -------------------------------------------
-  const int ppc = kChunkTokens / p;  // pages per stage
+  // Chunks of 64 tokens alternate between two stages; warp group wg (warps 4wg .. 4wg+3)
+  // processes chunks wg, wg + 2, ... from stage wg, 16 tokens per warp.
+  const int ppc = kChunkTokens / p;
   const int nchunks = (nsel + ppc - 1) / ppc;
   const size_t cache_base = (size_t)ukv * a.cap;
+  const int wg = warp >> 2, wig = warp & 3, gtid = tid & 127;
 
-  auto issue = [&](int c) {  // warp 0 only
-    const int s = c % kStages;
-    bf16* Ks = stages + (size_t)s * (2 * kChunkTokens * kHeadDim);
-    bf16* Vs = Ks + kChunkTokens * kHeadDim;
+  auto chunk_tokens = [&](int c) {
     const int j0 = c * ppc, j1 = min(nsel, j0 + ppc);
-    if (lane == 0) {
-      uint32_t bytes = 0;
-      for (int j = j0; j < j1; ++j) {
-        const int t0 = sel[j] * p;
-        bytes += 2u * (uint32_t)min(p, len - t0) * (kHeadDim * 2);
-      }
-      mbar_arrive_expect_tx(&bars[s], bytes);
-    }
-    __syncwarp();
-    for (int j = j0 + lane; j < j1; j += 32) {
-      const int t0 = sel[j] * p;
-      const uint32_t nb = (uint32_t)min(p, len - t0) * (kHeadDim * 2);
-      const int r = (j - j0) * p;
-      bulk_g2s(Ks + r * kHeadDim, a.k_cache + (cache_base + t0) * kHeadDim, nb, &bars[s]);
-      bulk_g2s(Vs + r * kHeadDim, a.v_cache + (cache_base + t0) * kHeadDim, nb, &bars[s]);
-    }
+    return (j1 - j0 - 1) * p + min(p, len - sel[j1 - 1] * p);
   };
-
-  if (warp == 0)
-    for (int c = 0; c < min(nchunks, kStages); ++c) issue(c);
-
-  // q pre-scaled into registers
-  __syncthreads();
-  for (int i = tid; i < G * kHeadDim; i += kDecodeThreads) qs[i] *= a.scale_log2;
-  __syncthreads();
-  WarpAttn<G> wa;
-  wa.init(qs);
-
-  bool failed = false;
-  for (int c = 0; c < nchunks; ++c) {
-    const int s = c % kStages;
-    const bool ok = mbar_wait(&bars[s], (uint32_t)((c / kStages) & 1));
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      if (tid == 0) set_status(a.status, RKV_DEV_WAIT_TIMEOUT);
-      // drain the copies still in flight (bounded) before leaving
-      for (int c2 = c + 1; c2 < min(nchunks, c + kStages); ++c2)
-        mbar_wait(&bars[c2 % kStages], (uint32_t)((c2 / kStages) & 1));
-      break;
+  // The 128 threads of a group stage one chunk: 16-byte cp.async copies of K and V rows into
+  // rows kRowPad apart.
+  const int lp = __ffs(p) - 1;  // log2(page)
+  auto load = [&](int c) {
+    bf16* Ks = stages + (size_t)wg * kStageElems;
+    const int j0 = c * ppc;
+    const int nt = chunk_tokens(c);
+    for (int idx = gtid; idx < nt * 32; idx += 128) {
+      const int r = idx >> 5, tv = (idx >> 4) & 1, c16 = idx & 15;
+      const size_t tok = ((size_t)sel[j0 + (r >> lp)] << lp) + (r & (p - 1));
+      const bf16* src = (tv ? a.v_cache : a.k_cache) + (cache_base + tok) * kHeadDim + c16 * 8;
+      cp_async16(Ks + tv * (kChunkTokens * kRowPad) + r * kRowPad + c16 * 8, src);
     }
-    const bf16* Ks = stages + (size_t)s * (2 * kChunkTokens * kHeadDim);
-    const bf16* Vs = Ks + kChunkTokens * kHeadDim;
-    const int j0 = c * ppc, j1 = min(nsel, j0 + ppc);
-    const int last_t0 = sel[j1 - 1] * p;
-    const int ntok = (j1 - j0 - 1) * p + min(p, len - last_t0);
-    wa.step4(Ks, Vs, warp * 8, ntok);
-    wa.step4(Ks, Vs, warp * 8 + 4, ntok);
-    __syncthreads();
-    if (warp == 0 && c + kStages < nchunks) issue(c + kStages);
+    cp_async_commit();
+  };
+  if (wg < nchunks) load(wg);
+
+  MmaAttn<G> at;
+  at.init(qfrag);
+  for (int c = wg; c < nchunks; c += 2) {
+    cp_async_wait_all();
+    group_sync(wg);
+    const bf16* Ks = stages + (size_t)wg * kStageElems;
+    bf16* Vs = stages + (size_t)wg * kStageElems + kChunkTokens * kRowPad;
+    const int nt = chunk_tokens(c);
+    if (nt < kChunkTokens) {
+      zero_tail_rows(Vs, nt, gtid);
+      group_sync(wg);
+    }
+    if (wig * 16 < nt) at.step16(Ks, Vs, wig * 16, nt, a.scale_log2);
+    group_sync(wg);
+    if (c + 2 < nchunks) load(c + 2);
   }
-  if (failed) return;
+  __syncthreads();
 
   CombineSmem<G>* cs = reinterpret_cast<CombineSmem<G>*>(smem);
-  warp_deposit<G>(wa, cs);
+  warp_deposit<G>(at, cs);
   __syncthreads();
   for (int i = tid; i < G * kHeadDim; i += kDecodeThreads) {
     const int h = i >> 7, c = i & 127;
@@ -408,6 +484,24 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
     warp_merge<G>(cs, h, c, &M, &L, &O);
     a.out[((size_t)u * hq + g * G + h) * kHeadDim + c] = __float2bfloat16_rn(O / L);
   }
+}
+
+// Launch with programmatic stream serialisation (the kernel calls pdl_wait() before its first
+// global read, so it is correct after any kind of predecessor).
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 cudaError_t launch_hybrid(const HybridArgs& a, cudaStream_t s) {
@@ -419,7 +513,8 @@ cudaError_t launch_hybrid(const HybridArgs& a, cudaStream_t s) {
   case GG:                                                                                   \
     e = ensure_dyn_smem((const void*)hybrid_decode_kernel<GG>, smem);                        \
     if (e != cudaSuccess) return e;                                                          \
-    hybrid_decode_kernel<GG><<<grid, block, smem, s>>>(a);                                   \
+    e = launch_pdl(hybrid_decode_kernel<GG>, grid, block, smem, s, a);                       \
+    if (e != cudaSuccess) return e;                                                          \
     break;
     RKV_CASE(1)
     RKV_CASE(2)
@@ -563,9 +658,9 @@ cudaError_t launch_summaries(const SummaryArgs& a, cudaStream_t s) {
 }
 
 // ==========================================================================================
-// Dense decode (flash-decoding split-K): CTA = (unit, KV head, split); contiguous token runs
-// staged by two bulk copies (K rows, V rows) per 64-token stage; partials merged by a second
-// kernel.
+// Dense decode (flash-decoding split-K): CTA = (unit, KV head, split). Each split's tokens are
+// staged 64 rows at a time (one bulk copy per row) and consumed by the same MMA warp code;
+// per-split partials are merged by a second kernel.
 // ==========================================================================================
 void dense_plan(int n, int n_kv, int max_len, int* nsplit, int* tokens_per_split) {
   const int units = n * n_kv;
@@ -590,8 +685,7 @@ size_t dense_partials_bytes(int n, int n_kv, int gqa, int max_len) {
 template <int G>
 __global__ void __launch_bounds__(kDecodeThreads, 2) dense_split_kernel(DenseArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  __shared__ float qs[G * kHeadDim];
-  __shared__ __align__(8) uint64_t bars[kStages];
+  __shared__ uint2 qfrag[8 * 32];
   bf16* stages = reinterpret_cast<bf16*>(smem);
 
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -608,55 +702,47 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) dense_split_kernel(DenseArg
   const int ntok_all = max(0, te - tb);
   const int nchunks = (ntok_all + kChunkTokens - 1) / kChunkTokens;
   const size_t base = ((size_t)ukv * a.max_len + tb) * kHeadDim;
+  const bf16* qgroup = a.q + ((size_t)u * hq + g * G) * kHeadDim;
+  const int wg = warp >> 2, wig = warp & 3, gtid = tid & 127;
 
-  if (tid < G * 16) {
-    const int h = tid >> 4, c8 = (tid & 15) * 8;
-    const uint4 c = *reinterpret_cast<const uint4*>(
-        a.q + ((size_t)u * hq + g * G + h) * kHeadDim + c8);
-    float f[8];
-    unpack8(c, f);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) qs[h * kHeadDim + c8 + i] = f[i] * a.scale_log2;
+  if (warp == 7) MmaAttn<G>::build_fragments(qgroup, qfrag);
+
+  auto chunk_tokens = [&](int c) { return min(kChunkTokens, ntok_all - c * kChunkTokens); };
+  // the 128 threads of a group stage one chunk of contiguous rows with 16-byte cp.async copies
+  auto load = [&](int c) {
+    bf16* Ks = stages + (size_t)wg * kStageElems;
+    const int nt = chunk_tokens(c);
+    const size_t row0 = base + (size_t)c * kChunkTokens * kHeadDim;
+    for (int idx = gtid; idx < nt * 32; idx += 128) {
+      const int r = idx >> 5, tv = (idx >> 4) & 1, c16 = idx & 15;
+      const bf16* src = (tv ? a.v : a.k) + row0 + (size_t)r * kHeadDim + c16 * 8;
+      cp_async16(Ks + tv * (kChunkTokens * kRowPad) + r * kRowPad + c16 * 8, src);
+    }
+    cp_async_commit();
+  };
+  if (wg < nchunks) load(wg);
+  __syncthreads();  // Q fragments ready
+
+  MmaAttn<G> at;
+  at.init(qfrag);
+  for (int c = wg; c < nchunks; c += 2) {
+    cp_async_wait_all();
+    group_sync(wg);
+    const bf16* Ks = stages + (size_t)wg * kStageElems;
+    bf16* Vs = stages + (size_t)wg * kStageElems + kChunkTokens * kRowPad;
+    const int nt = chunk_tokens(c);
+    if (nt < kChunkTokens) {
+      zero_tail_rows(Vs, nt, gtid);
+      group_sync(wg);
+    }
+    if (wig * 16 < nt) at.step16(Ks, Vs, wig * 16, nt, a.scale_log2);
+    group_sync(wg);
+    if (c + 2 < nchunks) load(c + 2);
   }
-  if (tid < kStages) mbar_init(&bars[tid], 1);
-  fence_barrier_init();
   __syncthreads();
 
-  auto issue = [&](int c) {  // one thread
-    const int s = c % kStages;
-    bf16* Ks = stages + (size_t)s * (2 * kChunkTokens * kHeadDim);
-    bf16* Vs = Ks + kChunkTokens * kHeadDim;
-    const int nt = min(kChunkTokens, ntok_all - c * kChunkTokens);
-    const uint32_t nb = (uint32_t)nt * (kHeadDim * 2);
-    mbar_arrive_expect_tx(&bars[s], 2 * nb);
-    bulk_g2s(Ks, a.k + base + (size_t)c * kChunkTokens * kHeadDim, nb, &bars[s]);
-    bulk_g2s(Vs, a.v + base + (size_t)c * kChunkTokens * kHeadDim, nb, &bars[s]);
-  };
-  if (tid == 0)
-    for (int c = 0; c < min(nchunks, kStages); ++c) issue(c);
-
-  WarpAttn<G> wa;
-  wa.init(qs);
-  for (int c = 0; c < nchunks; ++c) {
-    const int s = c % kStages;
-    const bool ok = mbar_wait(&bars[s], (uint32_t)((c / kStages) & 1));
-    if (__syncthreads_or(!ok)) {
-      if (tid == 0) set_status(a.status, RKV_DEV_WAIT_TIMEOUT);
-      for (int c2 = c + 1; c2 < min(nchunks, c + kStages); ++c2)
-        mbar_wait(&bars[c2 % kStages], (uint32_t)((c2 / kStages) & 1));
-      return;
-    }
-    const bf16* Ks = stages + (size_t)s * (2 * kChunkTokens * kHeadDim);
-    const bf16* Vs = Ks + kChunkTokens * kHeadDim;
-    const int ntok = min(kChunkTokens, ntok_all - c * kChunkTokens);
-    wa.step4(Ks, Vs, warp * 8, ntok);
-    wa.step4(Ks, Vs, warp * 8 + 4, ntok);
-    __syncthreads();
-    if (tid == 0 && c + kStages < nchunks) issue(c + kStages);
-  }
-
   CombineSmem<G>* cs = reinterpret_cast<CombineSmem<G>*>(smem);
-  warp_deposit<G>(wa, cs);
+  warp_deposit<G>(at, cs);
   __syncthreads();
   for (int i = tid; i < G * kHeadDim; i += kDecodeThreads) {
     const int h = i >> 7, c = i & 127;
@@ -689,7 +775,7 @@ __global__ void dense_combine_kernel(DenseArgs a) {
 }
 
 cudaError_t launch_dense(const DenseArgs& a, cudaStream_t s) {
-  const size_t smem = (size_t)kStages * kStageBytes;
+  const size_t smem = (size_t)kDecStages * kStageBytes;
   const dim3 grid(a.n * a.n_kv, a.nsplit), block(kDecodeThreads);
   cudaError_t e = cudaSuccess;
   switch (a.gqa) {

@@ -12,7 +12,7 @@ constexpr int kHeadDim = 128;
 constexpr size_t kStatusBytes = 256;     // device status word + padding at the start of ws
 constexpr int kDecodeThreads = 256;      // 8 warps per decode CTA
 constexpr int kChunkTokens = 64;         // tokens per shared-memory stage in decode attention
-constexpr int kStages = 3;               // stages in flight per decode CTA
+
 
 typedef __nv_bfloat16 bf16;
 

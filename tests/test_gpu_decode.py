@@ -276,3 +276,28 @@ def test_device_status_len_over_cap():
     assert ei.value.bits & 1
     # the word is cleared by the check
     assert rkv.rkv_check_status(ws) == 0
+
+
+def test_hybrid_exact_ties_take_lowest_pages_and_channels():
+    # identical keys -> every page scores the same; a query whose |q| is equal on every channel
+    # -> every channel ties. Both selections must then be the lowest indices.
+    rkv = _lib()
+    n, n_kv, gqa, L, B, page, C = 1, 1, 4, 1000, 256, 4, 32
+    row = torch.randn(D, generator=torch.Generator().manual_seed(91)).to(torch.bfloat16)
+    k = row.expand(n, n_kv, 1024, D).contiguous().cuda()
+    v = torch.randn(n, n_kv, 1024, D, generator=torch.Generator().manual_seed(92))
+    v = v.to(torch.bfloat16).cuda()
+    lens_t = torch.tensor([L], dtype=torch.int32, device="cuda")
+    kmin, kmax = _summaries(rkv, k, lens_t, page, 256)
+    q = torch.ones(n, n_kv * gqa, D, dtype=torch.bfloat16, device="cuda")
+    q[:, :, 1::2] = -1.0
+    out = torch.empty_like(q)
+    sel_c = torch.empty(n, n_kv, C, dtype=torch.int32, device="cuda")
+    sel_p = torch.empty(n, n_kv, B // 2 // page, dtype=torch.int32, device="cuda")
+    ws = rkv.rkv_hybrid_decode(q, k, v, lens_t, kmin, kmax, B, page, C, 0.1, out,
+                               sel_channels=sel_c, sel_pages=sel_p)
+    rkv.rkv_check_status(ws)
+    assert sel_c[0, 0].tolist() == list(range(C))
+    assert sel_p[0, 0].tolist() == list(range(B // 2 // page))
+    ref = O.attention(_f64(q[0]), _f64(k[0, 0, :128]), _f64(v[0, 0, :128]), 0.1)
+    parity.check_output(_f64(out[0]), ref, "all-ties output")
