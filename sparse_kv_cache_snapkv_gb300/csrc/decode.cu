@@ -160,8 +160,27 @@ template <int G>
 struct CombineSmem {
   float m[8][G];
   float l[8][G];
+  float f[8][G];     // merge factor 2^(m_w - M) / L of warp w for head h
   float o[8][G][kHeadDim];
 };
+
+// Per head: the max over warps, each warp's factor 2^(m_w - M) and the inverse of the merged sum
+// (threads tid < G, after the deposit and a barrier). Returns nothing; fills cs->f.
+template <int G>
+__device__ __forceinline__ void merge_factors(CombineSmem<G>* cs, int h) {
+  float mm = -1e30f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) mm = fmaxf(mm, cs->m[w][h]);
+  float f[8], ll = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    f[w] = exp2f(cs->m[w][h] - mm);
+    ll = fmaf(cs->l[w][h], f[w], ll);
+  }
+  const float inv = ll > 0.f ? 1.f / ll : 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) cs->f[w][h] = f[w] * inv;
+}
 
 template <int G>
 __device__ __forceinline__ void warp_deposit(const MmaAttn<G>& at, CombineSmem<G>* cs) {
@@ -369,30 +388,41 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
       }
       const int t = lane & 3;
       const int krow = (lane & 7) + (((lane >> 3) & 1) << 3), pcol = (lane >> 4) << 3;
-      for (int pair = warp; pair < (np16 >> 4); pair += kDecodeThreads / 32) {
-        const int p0 = pair * 16;
-        float d0 = 0.f, d1 = 0.f, e0 = 0.f, e1 = 0.f;
-        const uint32_t base = smem_addr(stages + (size_t)krow * rs + p0 + pcol);
-        for (int ks = 0; ks < nks; ++ks) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(base + (uint32_t)(ks * 16 * rs * 2), b0, b1, b2, b3);
-          const uint2 wa = wfrag[ks * 32 + lane];
-          mma_rows8(d0, d1, wa.x, wa.y, b0, b1);
-          mma_rows8(e0, e1, wa.x, wa.y, b2, b3);
-        }
-        // row 0 (lanes 0..3) + row 1 (lanes 4..7)
-        d0 += __shfl_down_sync(0xffffffffu, d0, 4);
-        d1 += __shfl_down_sync(0xffffffffu, d1, 4);
-        e0 += __shfl_down_sync(0xffffffffu, e0, 4);
-        e1 += __shfl_down_sync(0xffffffffu, e1, 4);
-        if (lane < 4) {
-          const float v4[4] = {d0, d1, e0, e1};
+      const int npairs = np16 >> 4;  // 16-page tiles
+      const uint32_t rows_base = smem_addr(stages + (size_t)krow * rs + pcol);
+      // four independent 16-page tiles per warp and iteration (tiles warp, +8, +16, +24)
+      for (int pq = warp; pq < npairs; pq += 32) {
+        float d[4][4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int pg = pb + p0 + 2 * t + (e & 1) + (e >> 1) * 8;
-            if (pg < P && pg < pb + np) {
-              scores[pg] = v4[e];
-              if (a.approx) a.approx[(size_t)ukv * a.page_cap + pg] = v4[e];
+        for (int x = 0; x < 4; ++x) d[x][0] = d[x][1] = d[x][2] = d[x][3] = 0.f;
+        for (int ks = 0; ks < nks; ++ks) {
+          const uint2 wa = wfrag[ks * 32 + lane];
+          const uint32_t kofs = (uint32_t)(ks * 16 * rs * 2);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const int pair = pq + 8 * x;
+            if (pair < npairs) {
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4_t(rows_base + kofs + (uint32_t)(pair * 32), b0, b1, b2, b3);
+              mma_rows8(d[x][0], d[x][1], wa.x, wa.y, b0, b1);
+              mma_rows8(d[x][2], d[x][3], wa.x, wa.y, b2, b3);
+            }
+          }
+        }
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const int pair = pq + 8 * x;
+          // row 0 (lanes 0..3) + row 1 (lanes 4..7)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) d[x][e] += __shfl_down_sync(0xffffffffu, d[x][e], 4);
+          if (lane < 4 && pair < npairs) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int pg = pb + pair * 16 + 2 * t + (e & 1) + (e >> 1) * 8;
+              if (pg < P && pg < pb + np) {
+                scores[pg] = d[x][e];
+                if (a.approx) a.approx[(size_t)ukv * a.page_cap + pg] = d[x][e];
+              }
             }
           }
         }
@@ -478,11 +508,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
   CombineSmem<G>* cs = reinterpret_cast<CombineSmem<G>*>(smem);
   warp_deposit<G>(at, cs);
   __syncthreads();
-  for (int i = tid; i < G * kHeadDim; i += kDecodeThreads) {
-    const int h = i >> 7, c = i & 127;
-    float M, L, O;
-    warp_merge<G>(cs, h, c, &M, &L, &O);
-    a.out[((size_t)u * hq + g * G + h) * kHeadDim + c] = __float2bfloat16_rn(O / L);
+  if (tid < G) merge_factors<G>(cs, tid);
+  __syncthreads();
+  for (int i = tid; i < G * kHeadDim / 2; i += kDecodeThreads) {
+    const int h = i >> 6, c = (i & 63) * 2;
+    float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const float f = cs->f[w][h];
+      const float2 x = *reinterpret_cast<const float2*>(&cs->o[w][h][c]);
+      o0 = fmaf(f, x.x, o0);
+      o1 = fmaf(f, x.y, o1);
+    }
+    *reinterpret_cast<uint32_t*>(a.out + ((size_t)u * hq + g * G + h) * kHeadDim + c) =
+        pack_bf16x2(o0, o1);
   }
 }
 
