@@ -382,14 +382,24 @@ def _oracle_worker_init_env():
 
 
 def _profiled_traffic(kernel_name):
-    """DRAM bytes per launch from the committed ncu summary of this kernel, when present."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.md), only while the
+    kernel's source file is unchanged since the capture (its hash matches); else None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.md")
     try:
-        with open(path) as f:
-            t = json.load(f)
-        return t.get(kernel_name)
-    except Exception:
+        lines = open(path).read().splitlines()
+    except OSError:
         return None
+    for line in lines:
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) == 5 and cells[0] == kernel_name:
+            src = os.path.join(ROOT, "sparse_kv_cache_snapkv_gb300", "csrc", cells[3])
+            try:
+                digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+            except OSError:
+                return None
+            return int(cells[1]) if digest == cells[4] else None
+    return None
 
 
 def _dense_compare(hp, x, dq, wl, hbm_peak, stream, world):
