@@ -234,6 +234,73 @@ __device__ __forceinline__ void group_sync(int group) {
   asm volatile("bar.sync %0, 128;" ::"r"(1 + group) : "memory");
 }
 
+// D (16 x 8) += A (16 x 16) B (16 x 8), all four accumulators of a lane kept.
+__device__ __forceinline__ void mma_full(float (&d)[4], const uint4& a, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+}
+
+// Approximate page scores of one staged block on the tensor cores. A row 0 holds bf16(w) and
+// row 8 the bf16 remainder w - bf16(w) for the kept channels (wfrag, one uint4 per lane and
+// 16-channel step), B = the staged summary rows (channels x pages) read by ldmatrix.trans, so
+// lanes 0..3 end up with both partial sums of their pages: score = D[row 0] + D[row 8]. Each
+// warp takes four 16-page tiles per iteration (tiles warp, +8, +16, +24).
+template <int NKS>
+__device__ __forceinline__ void score_block(const bf16* rows, int rs, int npairs,
+                                            const uint4* wfrag, float* scores, float* approx,
+                                            int pb, int limit) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, t = lane & 3;
+  const int krow = (lane & 7) + (((lane >> 3) & 1) << 3), pcol = (lane >> 4) << 3;
+  const uint32_t base = smem_addr(rows + (size_t)krow * rs + pcol);
+  uint4 wa[NKS];
+#pragma unroll
+  for (int ks = 0; ks < NKS; ++ks) wa[ks] = wfrag[ks * 32 + lane];
+  for (int pq = warp; pq < npairs; pq += 32) {
+    float d[4][2][4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) d[x][nt][0] = d[x][nt][1] = d[x][nt][2] = d[x][nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < NKS; ++ks) {
+      uint32_t b[4][4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int pair = min(pq + 8 * x, npairs - 1);
+        ldsm_x4_t(base + (uint32_t)(ks * 16 * rs * 2 + pair * 32), b[x][0], b[x][1], b[x][2],
+                  b[x][3]);
+      }
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        mma_full(d[x][0], wa[ks], b[x][0], b[x][1]);
+        mma_full(d[x][1], wa[ks], b[x][2], b[x][3]);
+      }
+    }
+    if (lane < 4) {
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int pair = pq + 8 * x;
+        if (pair < npairs) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int nt = e >> 1, c = e & 1;
+            const int pg = pb + pair * 16 + nt * 8 + 2 * t + c;
+            const float v = d[x][nt][c] + d[x][nt][c + 2];
+            if (pg < limit) {
+              scores[pg] = v;
+              if (approx) approx[pg] = v;
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
 // ==========================================================================================
 // Hybrid sparse decode: one CTA of 8 warps per (unit, KV head).
 // ==========================================================================================
@@ -261,7 +328,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
     FastSelectSmem fast;
   } sel_smem;
   __shared__ uint2 qfrag[8 * 32];
-  __shared__ uint2 wfrag[8 * 32];
+  __shared__ uint4 wfrag[8 * 32];
 
   bf16* stages = reinterpret_cast<bf16*>(smem);
   float* scores = reinterpret_cast<float*>(smem + (size_t)kDecStages * kStageBytes);
@@ -337,22 +404,25 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
     const int cn = a.channels;
     const int nks = (cn + 15) >> 4;  // 16-channel steps
     if (warp == 0) {
+      // lanes 0..3 (A rows 0 and 8): bf16(w) in row 0, the bf16 remainder in row 8
       for (int ks = 0; ks < nks; ++ks) {
-        const int r0 = lane >> 2, t = lane & 3;
-        uint32_t v0 = 0u, v2 = 0u;
-        if (r0 < 2) {
-          float w4[4];
+        const int t = lane & 3;
+        uint4 f = make_uint4(0u, 0u, 0u, 0u);
+        if (lane < 4) {
+          float hi4[4], lo4[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int i = ks * 16 + 2 * t + (e & 1) + (e >> 1) * 8;
             const float w = i < cn ? wsel[i] : 0.f;
-            const float whi = __bfloat162float(__float2bfloat16_rn(w));
-            w4[e] = r0 == 0 ? whi : (w - whi);
+            hi4[e] = __bfloat162float(__float2bfloat16_rn(w));
+            lo4[e] = w - hi4[e];
           }
-          v0 = pack_bf16x2(w4[0], w4[1]);
-          v2 = pack_bf16x2(w4[2], w4[3]);
+          f.x = pack_bf16x2(hi4[0], hi4[1]);  // row 0, k 2t..2t+1
+          f.y = pack_bf16x2(lo4[0], lo4[1]);  // row 8
+          f.z = pack_bf16x2(hi4[2], hi4[3]);  // row 0, k 2t+8..
+          f.w = pack_bf16x2(lo4[2], lo4[3]);  // row 8
         }
-        wfrag[ks * 32 + lane] = make_uint2(v0, v2);
+        wfrag[ks * 32 + lane] = f;
       }
     }
     const int Ppad = (P + 7) & ~7;
@@ -379,52 +449,33 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
         const int r = cn + i / (rs / 8), c8 = i % (rs / 8);
         *reinterpret_cast<uint4*>(stages + (size_t)r * rs + c8 * 8) = make_uint4(0u, 0u, 0u, 0u);
       }
-      const bool ok = mbar_wait(&sbar, sphase);
+      // one thread waits for the rows; the barrier then publishes them to the block
+      bool ok = true;
+      if (tid == 0) ok = mbar_wait(&sbar, sphase);
       sphase ^= 1u;
       if (__syncthreads_or(!ok)) {
         if (tid == 0) set_status(a.status, RKV_DEV_WAIT_TIMEOUT);
         mbar_wait(&sbar, sphase ^ 1u);  // let the copies land before the CTA retires
         return;
       }
-      const int t = lane & 3;
-      const int krow = (lane & 7) + (((lane >> 3) & 1) << 3), pcol = (lane >> 4) << 3;
-      const int npairs = np16 >> 4;  // 16-page tiles
-      const uint32_t rows_base = smem_addr(stages + (size_t)krow * rs + pcol);
-      // four independent 16-page tiles per warp and iteration (tiles warp, +8, +16, +24)
-      for (int pq = warp; pq < npairs; pq += 32) {
-        float d[4][4];
-#pragma unroll
-        for (int x = 0; x < 4; ++x) d[x][0] = d[x][1] = d[x][2] = d[x][3] = 0.f;
-        for (int ks = 0; ks < nks; ++ks) {
-          const uint2 wa = wfrag[ks * 32 + lane];
-          const uint32_t kofs = (uint32_t)(ks * 16 * rs * 2);
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const int pair = pq + 8 * x;
-            if (pair < npairs) {
-              uint32_t b0, b1, b2, b3;
-              ldsm_x4_t(rows_base + kofs + (uint32_t)(pair * 32), b0, b1, b2, b3);
-              mma_rows8(d[x][0], d[x][1], wa.x, wa.y, b0, b1);
-              mma_rows8(d[x][2], d[x][3], wa.x, wa.y, b2, b3);
-            }
-          }
-        }
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const int pair = pq + 8 * x;
-          // row 0 (lanes 0..3) + row 1 (lanes 4..7)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) d[x][e] += __shfl_down_sync(0xffffffffu, d[x][e], 4);
-          if (lane < 4 && pair < npairs) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int pg = pb + pair * 16 + 2 * t + (e & 1) + (e >> 1) * 8;
-              if (pg < P && pg < pb + np) {
-                scores[pg] = d[x][e];
-                if (a.approx) a.approx[(size_t)ukv * a.page_cap + pg] = d[x][e];
-              }
-            }
-          }
+      {
+        const int npairs = np16 >> 4;  // 16-page tiles
+        float* approx_row = a.approx ? a.approx + (size_t)ukv * a.page_cap : nullptr;
+        const int limit = min(P, pb + np);
+        switch (nks) {
+#define RKV_SCORE(NK)                                                                        \
+  case NK:                                                                                   \
+    score_block<NK>(stages, rs, npairs, wfrag, scores, approx_row, pb, limit);               \
+    break;
+          RKV_SCORE(1)
+          RKV_SCORE(2)
+          RKV_SCORE(3)
+          RKV_SCORE(4)
+          RKV_SCORE(5)
+          RKV_SCORE(6)
+          RKV_SCORE(7)
+          RKV_SCORE(8)
+#undef RKV_SCORE
         }
       }
       __syncthreads();  // the staging area is refilled by the next block / the K/V stages

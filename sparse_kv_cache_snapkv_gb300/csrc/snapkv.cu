@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* qfull = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qfull + 1);
-  float* lse2 = reinterpret_cast<float*>(smem + SM::misc_off);   // [RP] (pass 2)
+  float* lse2 = reinterpret_cast<float*>(smem + SM::misc_off);   // [RP] negated (pass 2)
   float* xch_m = lse2 + RP;                                      // [128] (pass 1 merge)
   float* xch_l = xch_m + 128;                                    // [128]
   float* spart = xch_l + 128;                                    // [2][128] (pass 2 merge)
@@ -165,6 +165,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const int u = ukv / p.n_kv, g = ukv - u * p.n_kv;
   const int W = p.window;
   const int R = p.gqa * W;
+  pdl_wait();     // inputs (and pass-1 partials) come from earlier kernels in the stream
+  pdl_trigger();
   int L = p.seq_lens[u];
   const bool bad = L <= W || L > p.max_len;
   if (bad) {
@@ -193,19 +195,27 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                  ::"r"(smem_addr(tmem_slot)), "r"(kCols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // pass 2: merge the per-split partials into lse2[r] (log2 domain); padded rows -> +big
+  // pass 2: merge the per-split partials into lse2[r] (log2 domain); padded rows -> +big.
+  // The partials are fetched eight splits at a time so that their loads overlap.
   if (PASS == 2 && tid < RP) {
     float m = -1e30f, l = 0.f;
     if (!bad && tid < R) {
-      const float* pm = p.part_ml + ((size_t)ukv * p.nsplit * RP + tid) * 2;
-      for (int s = 0; s < p.nsplit; ++s) {
-        const float ms = pm[(size_t)s * RP * 2], ls = pm[(size_t)s * RP * 2 + 1];
-        const float mn = fmaxf(m, ms);
-        l = l * exp2f(m - mn) + ls * exp2f(ms - mn);
-        m = mn;
+      const float2* pm = reinterpret_cast<const float2*>(p.part_ml) +
+                         (size_t)ukv * p.nsplit * RP + tid;
+      for (int s0 = 0; s0 < p.nsplit; s0 += 8) {
+        float2 x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          x[j] = (s0 + j < p.nsplit) ? pm[(size_t)(s0 + j) * RP] : make_float2(-1e30f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float mn = fmaxf(m, x[j].x);
+          l = l * exp2f(m - mn) + x[j].y * exp2f(x[j].x - mn);
+          m = mn;
+        }
       }
     }
-    lse2[tid] = (l > 0.f) ? m + log2f(l) : 1e30f;
+    lse2[tid] = (l > 0.f) ? -(m + log2f(l)) : -1e30f;  // negated: consumed as an FMA addend
   }
   tc_fence_before();
   __syncthreads();
@@ -315,19 +325,27 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           uint32_t r[32];
           tmem_ld32(tmem + lane_addr + (uint32_t)((b * RB + rb) * kTileTok + c0 + cc), r);
           const int tb = t0 + c0 + cc;
-          float s[32];
+          // max on the raw logits (the scale is positive); only chunks that reach the causal
+          // part of the window need the visibility mask
           float mt = -INFINITY;
+          if (tb + 31 <= lim) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float x = __uint_as_float(r[i]) * p.scale_log2;
-            s[i] = (tb + i <= lim) ? x : -INFINITY;
-            mt = fmaxf(mt, s[i]);
+            for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __uint_as_float(r[i]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float x = (tb + i <= lim) ? __uint_as_float(r[i]) : -INFINITY;
+              r[i] = __float_as_uint(x);
+              mt = fmaxf(mt, x);
+            }
           }
-          const float mn = fmaxf(m, mt);
-          float acc = 0.f;
+          const float mn = fmaxf(m, mt * p.scale_log2);
+          const float nmn = -mn;
+          float a4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc += exp2f(s[i] - mn);
-          l = l * exp2f(m - mn) + acc;
+          for (int i = 0; i < 32; ++i)
+            a4[i & 3] += exp2f(fmaf(__uint_as_float(r[i]), p.scale_log2, nmn));
+          l = l * exp2f(m - mn) + ((a4[0] + a4[1]) + (a4[2] + a4[3]));
           m = mn;
         }
         tc_fence_before();
@@ -366,13 +384,21 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         float acc = 0.f;
         if (!aborted) {
           tc_fence_after();
+          float a4[4] = {0.f, 0.f, 0.f, 0.f};
           for (int cc = 0; cc < ncol; cc += 32) {
             uint32_t r[32];
             tmem_ld32(tmem + lane_addr + (uint32_t)(b * RP + c0 + cc), r);
+            const float4* nl = reinterpret_cast<const float4*>(lse2 + c0 + cc);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              acc += exp2f(fmaf(__uint_as_float(r[i]), p.scale_log2, -lse2[c0 + cc + i]));
+            for (int i4 = 0; i4 < 8; ++i4) {
+              const float4 v = nl[i4];  // negated log-sum-exp of four window rows
+              a4[0] += exp2f(fmaf(__uint_as_float(r[4 * i4 + 0]), p.scale_log2, v.x));
+              a4[1] += exp2f(fmaf(__uint_as_float(r[4 * i4 + 1]), p.scale_log2, v.y));
+              a4[2] += exp2f(fmaf(__uint_as_float(r[4 * i4 + 2]), p.scale_log2, v.z));
+              a4[3] += exp2f(fmaf(__uint_as_float(r[4 * i4 + 3]), p.scale_log2, v.w));
+            }
           }
+          acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&tempty[b]);
@@ -558,7 +584,18 @@ static cudaError_t launch_pass(const CUtensorMap& km, const CUtensorMap& qm,
   const size_t smem = ScoreSmem<RB>::total;
   cudaError_t e = ensure_dyn_smem((const void*)score_kernel<PASS, RB>, smem);
   if (e != cudaSuccess) return e;
-  score_kernel<PASS, RB><<<nunits * sp.nsplit, kScoreThreads, smem, s>>>(km, qm, sp);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nunits * sp.nsplit);
+  cfg.blockDim = dim3(kScoreThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, score_kernel<PASS, RB>, km, qm, sp);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
