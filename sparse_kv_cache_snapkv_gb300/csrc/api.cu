@@ -154,6 +154,8 @@ rkv_status rkv_snapkv_compress(const void* k, const void* v, const int32_t* seq_
   }
   p += plen;
   a.part_ml = reinterpret_cast<float*>(p);
+  p += align_up((size_t)n * n_kv * a.nsplit * a.rows_pad * 2 * 4, 256);
+  a.nlse = reinterpret_cast<float*>(p);
   a.status = status_ptr(ws);
   return from_cuda(launch_snapkv(a, as_stream(stream)));
 }

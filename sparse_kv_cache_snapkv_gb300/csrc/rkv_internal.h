@@ -99,6 +99,7 @@ struct SnapArgs {
   float* scores;       // [n][n_kv][max_len - window] (caller's buffer or workspace)
   float* pooled;       // workspace, same shape
   float* part_ml;      // workspace: [n*n_kv][nsplit][rows_pad][2] (max, sum) per split
+  float* nlse;         // workspace: [n*n_kv][rows_pad] merged negated log2-sum-exp per row
   int nsplit, tokens_per_split, rows_pad;
   uint32_t* status;
 };

@@ -35,7 +35,6 @@ constexpr int kKStages = 4;
 constexpr int kScoreThreads = 320;  // warp 0: TMA, warp 1: MMA, warps 2..9: epilogue
 constexpr int kEpiThreads = 256;
 constexpr int kTileBytes = kTileTok * kHeadDim * 2;  // 32 KB per K tile
-constexpr size_t kWaveBytes = 64ull << 20;           // K bytes per wave (L2-resident for pass 2)
 constexpr int kSMs = 152;
 
 // ------------------------------------------------------------------------------------------
@@ -113,15 +112,21 @@ __host__ __device__ inline int adaptive_kernel(int L) {
 }
 
 // ------------------------------------------------------------------------------------------
-// score kernel (both passes)
+// score kernel (both passes), persistent over work items
 // ------------------------------------------------------------------------------------------
+// A work item is one split (a contiguous range of 128-token tiles) of one (unit, KV head); the
+// launch covers every item of every unit and each CTA streams its items (i = blockIdx.x,
+// + gridDim.x, ...) through one continuous TMA -> MMA -> epilogue pipeline, so the pipeline fills
+// once per launch. The Q tile of the next item is loaded into the other Q buffer while the
+// current item's MMAs run (one buffer when G * W > 128, whose Q tile is twice the size).
 struct ScoreParams {
   int n_kv, gqa, window, max_len, hq;
-  int unit0;
-  int nsplit, tiles_per_split;
+  int units, nsplit, tiles_per_split;
+  int reverse;     // walk the units last-to-first (pass 2 starts where pass 1 ended: L2-warm)
   float scale_log2;
   const int32_t* seq_lens;
-  float* part_ml;  // [units][nsplit][RP][2]
+  float* part_ml;  // [units][nsplit][RP][2]: per-split (max, sum) of every window row (pass 1)
+  const float* nlse;  // [units][RP]: merged, negated log2-sum-exp of every row (pass 2)
   float* scores;   // [units][max_len - window]
   uint32_t* status;
 };
@@ -129,12 +134,37 @@ struct ScoreParams {
 template <int RB>
 struct ScoreSmem {
   static constexpr int RP = RB * 128;
+  static constexpr int kQBufs = RB == 1 ? 2 : 1;
   static constexpr size_t q_bytes = (size_t)RP * kHeadDim * 2;
-  static constexpr size_t k_off = q_bytes;
+  static constexpr size_t k_off = kQBufs * q_bytes;
   static constexpr size_t bar_off = k_off + (size_t)kKStages * kTileBytes;
   static constexpr size_t misc_off = bar_off + 256;
   static constexpr size_t total = misc_off + RP * 4 + 2 * 128 * 4 + 2 * 128 * 4 + 64 + 1024;
 };
+
+struct ItemInfo {
+  int ukv, u, g, split, L, tile0, ntiles;
+  bool bad;
+};
+
+template <int PASS>
+__device__ __forceinline__ ItemInfo score_item(const ScoreParams& p, int i) {
+  ItemInfo it;
+  const int ui = i / p.nsplit;
+  it.split = i - ui * p.nsplit;
+  it.ukv = p.reverse ? (p.units - 1 - ui) : ui;
+  it.u = it.ukv / p.n_kv;
+  it.g = it.ukv - it.u * p.n_kv;
+  int L = p.seq_lens[it.u];
+  it.bad = L <= p.window || L > p.max_len;
+  if (it.bad) L = 0;
+  it.L = L;
+  const int span = (PASS == 1) ? L : (L > p.window ? L - p.window : 0);
+  const int tiles_all = (span + kTileTok - 1) / kTileTok;
+  it.tile0 = it.split * p.tiles_per_split;
+  it.ntiles = max(0, min(p.tiles_per_split, tiles_all - it.tile0));
+  return it;
+}
 
 template <int PASS, int RB>
 __global__ void __launch_bounds__(kScoreThreads, 1)
@@ -143,6 +173,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   constexpr int RP = RB * 128;
   constexpr uint32_t kCols = (PASS == 1) ? (RB == 1 ? 256u : 512u) : (RP == 128 ? 256u : 512u);
   using SM = ScoreSmem<RB>;
+  constexpr int QB = SM::kQBufs;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -153,30 +184,17 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   uint64_t* tfull = empty + kKStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* qfull = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qfull + 1);
-  float* lse2 = reinterpret_cast<float*>(smem + SM::misc_off);   // [RP] negated (pass 2)
-  float* xch_m = lse2 + RP;                                      // [128] (pass 1 merge)
-  float* xch_l = xch_m + 128;                                    // [128]
-  float* spart = xch_l + 128;                                    // [2][128] (pass 2 merge)
+  uint64_t* qempty = qfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qempty + 2);
+  float* nlse_s = reinterpret_cast<float*>(smem + SM::misc_off);  // [RP] negated LSE (pass 2)
+  float* xch_m = nlse_s + RP;                                      // [128] (pass 1 merge)
+  float* xch_l = xch_m + 128;                                      // [128]
+  float* spart = xch_l + 128;                                      // [2][128] (pass 2 merge)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ukv = p.unit0 + blockIdx.x / p.nsplit;
-  const int split = blockIdx.x % p.nsplit;
-  const int u = ukv / p.n_kv, g = ukv - u * p.n_kv;
   const int W = p.window;
   const int R = p.gqa * W;
-  pdl_wait();     // inputs (and pass-1 partials) come from earlier kernels in the stream
-  pdl_trigger();
-  int L = p.seq_lens[u];
-  const bool bad = L <= W || L > p.max_len;
-  if (bad) {
-    if (tid == 0 && split == 0 && PASS == 1) set_status(p.status, RKV_DEV_BAD_WINDOW);
-    L = 0;
-  }
-  const int span = (PASS == 1) ? L : (L > W ? L - W : 0);  // tokens this pass covers
-  const int tiles_all = (span + kTileTok - 1) / kTileTok;
-  const int tile0 = split * p.tiles_per_split;
-  const int ntiles = max(0, min(p.tiles_per_split, tiles_all - tile0));
+  const int items = p.units * p.nsplit;
 
   if (tid == 0) {
     for (int i = 0; i < kKStages; ++i) {
@@ -186,8 +204,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], kEpiThreads / 32);
+      mbar_init(&qfull[i], 1);
+      mbar_init(&qempty[i], 1);
     }
-    mbar_init(qfull, 1);
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -195,105 +214,108 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                  ::"r"(smem_addr(tmem_slot)), "r"(kCols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // pass 2: merge the per-split partials into lse2[r] (log2 domain); padded rows -> +big.
-  // The partials are fetched eight splits at a time so that their loads overlap.
-  if (PASS == 2 && tid < RP) {
-    float m = -1e30f, l = 0.f;
-    if (!bad && tid < R) {
-      const float2* pm = reinterpret_cast<const float2*>(p.part_ml) +
-                         (size_t)ukv * p.nsplit * RP + tid;
-      for (int s0 = 0; s0 < p.nsplit; s0 += 8) {
-        float2 x[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          x[j] = (s0 + j < p.nsplit) ? pm[(size_t)(s0 + j) * RP] : make_float2(-1e30f, 0.f);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float mn = fmaxf(m, x[j].x);
-          l = l * exp2f(m - mn) + x[j].y * exp2f(x[j].x - mn);
-          m = mn;
-        }
-      }
-    }
-    lse2[tid] = (l > 0.f) ? -(m + log2f(l)) : -1e30f;  // negated: consumed as an FMA addend
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();     // inputs (and the pass-1 results) come from earlier kernels in the stream
+  pdl_trigger();
   bool aborted = false;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0 && ntiles > 0) {
-      const int qrow0 = (u * p.hq + g * p.gqa) * W;
-      mbar_arrive_expect_tx(qfull, (uint32_t)(RP * kHeadDim * 2));
-      for (int h = 0; h < 2; ++h)
-        for (int rb = 0; rb < RB; ++rb)
-          tma_load_2d(qs + (size_t)h * RP * 128 + (size_t)rb * 128 * 128, &qmap, 64 * h,
-                      qrow0 + rb * 128, qfull);
-      const int krow0 = ukv * p.max_len;
-      int it = 0;
-      for (; it < ntiles; ++it) {
-        const int s = it % kKStages;
-        if (it >= kKStages && !mbar_wait(&empty[s], (uint32_t)(((it / kKStages) - 1) & 1))) {
+    if (lane == 0) {
+      int it = 0, ic = 0;
+      for (int i = blockIdx.x; i < items && !aborted; i += gridDim.x) {
+        const ItemInfo itm = score_item<PASS>(p, i);
+        if (itm.ntiles == 0) continue;
+        const int qb = QB == 2 ? (ic & 1) : 0;
+        if (ic >= QB && !mbar_wait(&qempty[qb], (uint32_t)(((ic / QB) - 1) & 1))) {
           aborted = true;
           break;
         }
-        uint8_t* dst = ks + (size_t)s * kTileBytes;
-        mbar_arrive_expect_tx(&full[s], (uint32_t)kTileBytes);
-        const int y = krow0 + (tile0 + it) * kTileTok;
-        tma_load_2d(dst, &kmap, 0, y, &full[s]);
-        tma_load_2d(dst + kTileBytes / 2, &kmap, 64, y, &full[s]);
+        uint8_t* qdst = qs + (size_t)qb * SM::q_bytes;
+        const int qrow0 = (itm.u * p.hq + itm.g * p.gqa) * W;
+        mbar_arrive_expect_tx(&qfull[qb], (uint32_t)(RP * kHeadDim * 2));
+        for (int h = 0; h < 2; ++h)
+          for (int rb = 0; rb < RB; ++rb)
+            tma_load_2d(qdst + (size_t)h * RP * 128 + (size_t)rb * 128 * 128, &qmap, 64 * h,
+                        qrow0 + rb * 128, &qfull[qb]);
+        const int krow0 = itm.ukv * p.max_len;
+        for (int t = 0; t < itm.ntiles; ++t, ++it) {
+          const int s = it % kKStages;
+          if (it >= kKStages && !mbar_wait(&empty[s], (uint32_t)(((it / kKStages) - 1) & 1))) {
+            aborted = true;
+            break;
+          }
+          uint8_t* dst = ks + (size_t)s * kTileBytes;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)kTileBytes);
+          const int y = krow0 + (itm.tile0 + t) * kTileTok;
+          tma_load_2d(dst, &kmap, 0, y, &full[s]);
+          tma_load_2d(dst + kTileBytes / 2, &kmap, 64, y, &full[s]);
+        }
+        ++ic;
       }
-      // loads still in flight must land before the CTA may retire
-      for (int j = max(0, it - kKStages); j < it; ++j)
-        mbar_wait(&full[j % kKStages], (uint32_t)((j / kKStages) & 1));
-      if (aborted) set_status(p.status, RKV_DEV_WAIT_TIMEOUT);
+      if (aborted) {
+        set_status(p.status, RKV_DEV_WAIT_TIMEOUT);
+        for (int j = max(0, it - kKStages); j < it; ++j)  // let issued loads land
+          mbar_wait(&full[j % kKStages], (uint32_t)((j / kKStages) & 1));
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0 && ntiles > 0) {
-      if (!mbar_wait(qfull, 0)) {
-        aborted = true;
-      }
-      for (int it = 0; it < ntiles && !aborted; ++it) {
-        const int s = it % kKStages, b = it & 1;
-        if (!mbar_wait(&full[s], (uint32_t)((it / kKStages) & 1))) {
+    if (lane == 0) {
+      int it = 0, ic = 0;
+      for (int i = blockIdx.x; i < items && !aborted; i += gridDim.x) {
+        const ItemInfo itm = score_item<PASS>(p, i);
+        if (itm.ntiles == 0) continue;
+        const int qb = QB == 2 ? (ic & 1) : 0;
+        if (!mbar_wait(&qfull[qb], (uint32_t)((ic / QB) & 1))) {
           aborted = true;
           break;
         }
-        if (it >= 2 && !mbar_wait(&tempty[b], (uint32_t)(((it >> 1) - 1) & 1))) {
-          aborted = true;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t kbase = smem_addr(ks + (size_t)s * kTileBytes);
-        const uint32_t qbase = smem_addr(qs);
-        if (PASS == 1) {
-          constexpr uint32_t id = idesc_bf16(128, kTileTok);
+        const uint32_t qbase = smem_addr(qs + (size_t)qb * SM::q_bytes);
+        for (int t = 0; t < itm.ntiles; ++t, ++it) {
+          const int s = it % kKStages, b = it & 1;
+          if (!mbar_wait(&full[s], (uint32_t)((it / kKStages) & 1))) {
+            aborted = true;
+            break;
+          }
+          if (it >= 2 && !mbar_wait(&tempty[b], (uint32_t)(((it >> 1) - 1) & 1))) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t kbase = smem_addr(ks + (size_t)s * kTileBytes);
+          if (PASS == 1) {
+            constexpr uint32_t id = idesc_bf16(128, kTileTok);
 #pragma unroll
-          for (int rb = 0; rb < RB; ++rb) {
-            const uint32_t d = tmem + (uint32_t)((b * RB + rb) * kTileTok);
+            for (int rb = 0; rb < RB; ++rb) {
+              const uint32_t d = tmem + (uint32_t)((b * RB + rb) * kTileTok);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t off =
+                    (uint32_t)((kk >> 2) * RP * 128 + rb * 128 * 128 + (kk & 3) * 32);
+                const uint32_t koff = (uint32_t)((kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32);
+                umma_bf16(d, desc_sw128(qbase + off), desc_sw128(kbase + koff), id, kk > 0);
+              }
+            }
+          } else {
+            constexpr uint32_t id = idesc_bf16(kTileTok, RP);
+            const uint32_t d = tmem + (uint32_t)(b * RP);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t off = (uint32_t)((kk >> 2) * RP * 128 + rb * 128 * 128 + (kk & 3) * 32);
               const uint32_t koff = (uint32_t)((kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32);
-              umma_bf16(d, desc_sw128(qbase + off), desc_sw128(kbase + koff), id, kk > 0);
+              const uint32_t qoff = (uint32_t)((kk >> 2) * RP * 128 + (kk & 3) * 32);
+              umma_bf16(d, desc_sw128(kbase + koff), desc_sw128(qbase + qoff), id, kk > 0);
             }
           }
-        } else {
-          constexpr uint32_t id = idesc_bf16(kTileTok, RP);
-          const uint32_t d = tmem + (uint32_t)(b * RP);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t koff = (uint32_t)((kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32);
-            const uint32_t qoff = (uint32_t)((kk >> 2) * RP * 128 + (kk & 3) * 32);
-            umma_bf16(d, desc_sw128(kbase + koff), desc_sw128(qbase + qoff), id, kk > 0);
-          }
+          umma_commit(&empty[s]);
+          umma_commit(&tfull[b]);
         }
-        umma_commit(&empty[s]);
-        umma_commit(&tfull[b]);
+        if (aborted) break;
+        umma_commit(&qempty[qb]);  // arrives once this item's MMAs are done with its Q tile
+        ++ic;
       }
       if (aborted) set_status(p.status, RKV_DEV_WAIT_TIMEOUT);
     }
@@ -303,125 +325,128 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int hf = e >> 2;         // 0 / 1
     const int lrow = quarter * 32 + lane;
+    const int etid = tid - 64;     // 0..255
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    if (PASS == 1) {
-      // row this thread owns and its visibility limit
-      const int rb = (RB == 2) ? hf : 0;
-      const int rg = rb * 128 + lrow;
-      const bool row_ok = rg < R;
-      const int lim = L - W + (row_ok ? rg % W : 0);  // last visible key position
-      const int c0 = (RB == 2) ? 0 : hf * 64;
-      const int ncol = (RB == 2) ? 128 : 64;
-      float m = -1e30f, l = 0.f;
-      for (int it = 0; it < ntiles && !aborted; ++it) {
-        const int b = it & 1;
-        if (!mbar_wait(&tfull[b], (uint32_t)((it >> 1) & 1))) {
-          aborted = true;
-          break;
-        }
-        tc_fence_after();
-        const int t0 = (tile0 + it) * kTileTok;
-        for (int cc = 0; cc < ncol; cc += 32) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_addr + (uint32_t)((b * RB + rb) * kTileTok + c0 + cc), r);
-          const int tb = t0 + c0 + cc;
-          // max on the raw logits (the scale is positive); only chunks that reach the causal
-          // part of the window need the visibility mask
-          float mt = -INFINITY;
-          if (tb + 31 <= lim) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __uint_as_float(r[i]));
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float x = (tb + i <= lim) ? __uint_as_float(r[i]) : -INFINITY;
-              r[i] = __float_as_uint(x);
-              mt = fmaxf(mt, x);
-            }
+    int it = 0;
+    for (int i = blockIdx.x; i < items; i += gridDim.x) {
+      const ItemInfo itm = score_item<PASS>(p, i);
+      if (PASS == 1 && itm.bad && itm.split == 0 && etid == 0)
+        set_status(p.status, RKV_DEV_BAD_WINDOW);
+      if (PASS == 1) {
+        // row this thread owns and its visibility limit
+        const int rb = (RB == 2) ? hf : 0;
+        const int rg = rb * 128 + lrow;
+        const bool row_ok = rg < R;
+        const int lim = itm.L - W + (row_ok ? rg % W : 0);  // last visible key position
+        const int c0 = (RB == 2) ? 0 : hf * 64;
+        const int ncol = (RB == 2) ? 128 : 64;
+        float m = -1e30f, l = 0.f;
+        for (int t = 0; t < itm.ntiles; ++t, ++it) {
+          const int b = it & 1;
+          if (aborted) continue;
+          if (!mbar_wait(&tfull[b], (uint32_t)((it >> 1) & 1))) {
+            aborted = true;
+            continue;
           }
-          const float mn = fmaxf(m, mt * p.scale_log2);
-          const float nmn = -mn;
-          float a4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            a4[i & 3] += exp2f(fmaf(__uint_as_float(r[i]), p.scale_log2, nmn));
-          l = l * exp2f(m - mn) + ((a4[0] + a4[1]) + (a4[2] + a4[3]));
-          m = mn;
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[b]);
-      }
-      if (RB == 1) {
-        if (hf == 1) {
-          xch_m[lrow] = m;
-          xch_l[lrow] = l;
-        }
-        named_bar_sync(1, kEpiThreads);
-        if (hf == 0) {
-          const float m2 = xch_m[lrow], l2 = xch_l[lrow];
-          const float mn = fmaxf(m, m2);
-          l = l * exp2f(m - mn) + l2 * exp2f(m2 - mn);
-          m = mn;
-        }
-      }
-      if (RB == 2 || hf == 0) {
-        float* dst = p.part_ml + (((size_t)ukv * p.nsplit + split) * RP + rb * 128 + lrow) * 2;
-        dst[0] = m;
-        dst[1] = l;
-      }
-    } else {
-      // column sums: thread = token lrow of the tile, columns [c0, c0 + ncol) = window rows
-      const int ncol = RP / 2;
-      const int c0 = hf * ncol;
-      const int prefix = L - W;
-      float* out = p.scores + (size_t)ukv * (p.max_len - W);
-      // Every epilogue warp passes the named barrier once per tile, also after a failed wait,
-      // so that a timeout in one warp can never leave the others waiting at the barrier.
-      for (int it = 0; it < ntiles; ++it) {
-        const int b = it & 1;
-        if (!aborted && !mbar_wait(&tfull[b], (uint32_t)((it >> 1) & 1))) aborted = true;
-        float acc = 0.f;
-        if (!aborted) {
           tc_fence_after();
-          float a4[4] = {0.f, 0.f, 0.f, 0.f};
+          const int t0 = (itm.tile0 + t) * kTileTok;
           for (int cc = 0; cc < ncol; cc += 32) {
             uint32_t r[32];
-            tmem_ld32(tmem + lane_addr + (uint32_t)(b * RP + c0 + cc), r);
-            const float4* nl = reinterpret_cast<const float4*>(lse2 + c0 + cc);
+            tmem_ld32(tmem + lane_addr + (uint32_t)((b * RB + rb) * kTileTok + c0 + cc), r);
+            const int tb = t0 + c0 + cc;
+            // max on the raw logits (the scale is positive); only chunks that reach the causal
+            // part of the window need the visibility mask
+            float mt = -INFINITY;
+            if (tb + 31 <= lim) {
 #pragma unroll
-            for (int i4 = 0; i4 < 8; ++i4) {
-              const float4 v = nl[i4];  // negated log-sum-exp of four window rows
-              a4[0] += exp2f(fmaf(__uint_as_float(r[4 * i4 + 0]), p.scale_log2, v.x));
-              a4[1] += exp2f(fmaf(__uint_as_float(r[4 * i4 + 1]), p.scale_log2, v.y));
-              a4[2] += exp2f(fmaf(__uint_as_float(r[4 * i4 + 2]), p.scale_log2, v.z));
-              a4[3] += exp2f(fmaf(__uint_as_float(r[4 * i4 + 3]), p.scale_log2, v.w));
+              for (int j = 0; j < 32; ++j) mt = fmaxf(mt, __uint_as_float(r[j]));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float x = (tb + j <= lim) ? __uint_as_float(r[j]) : -INFINITY;
+                r[j] = __float_as_uint(x);
+                mt = fmaxf(mt, x);
+              }
             }
+            const float mn = fmaxf(m, mt * p.scale_log2);
+            const float nmn = -mn;
+            float a4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              a4[j & 3] += exp2f(fmaf(__uint_as_float(r[j]), p.scale_log2, nmn));
+            l = l * exp2f(m - mn) + ((a4[0] + a4[1]) + (a4[2] + a4[3]));
+            m = mn;
           }
-          acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&tempty[b]);
         }
-        if (hf == 1) spart[b * 128 + lrow] = acc;
+        if (RB == 1) {
+          if (hf == 1) {
+            xch_m[lrow] = m;
+            xch_l[lrow] = l;
+          }
+          named_bar_sync(1, kEpiThreads);
+          if (hf == 0) {
+            const float m2 = xch_m[lrow], l2 = xch_l[lrow];
+            const float mn = fmaxf(m, m2);
+            l = l * exp2f(m - mn) + l2 * exp2f(m2 - mn);
+            m = mn;
+          }
+          named_bar_sync(1, kEpiThreads);  // xch is rewritten by the next item
+        }
+        if (RB == 2 || hf == 0) {
+          float* dst =
+              p.part_ml + (((size_t)itm.ukv * p.nsplit + itm.split) * RP + rb * 128 + lrow) * 2;
+          dst[0] = m;  // an empty split publishes the neutral (-1e30, 0)
+          dst[1] = l;
+        }
+      } else {
+        // column sums: thread = token lrow of the tile, columns [c0, c0 + ncol) = window rows
+        const int ncol = RP / 2;
+        const int c0 = hf * ncol;
+        const int prefix = itm.L - W;
+        float* out = p.scores + (size_t)itm.ukv * (p.max_len - W);
+        named_bar_sync(1, kEpiThreads);  // everyone is done with the previous item's rows
+        if (etid < RP) nlse_s[etid] = p.nlse[(size_t)itm.ukv * RP + etid];
         named_bar_sync(1, kEpiThreads);
-        if (hf == 0 && !aborted) {
-          const int t = (tile0 + it) * kTileTok + lrow;
-          if (t < prefix) out[t] = acc + spart[b * 128 + lrow];
+        // Every epilogue warp passes the named barrier once per tile, also after a failed wait,
+        // so that a timeout in one warp can never leave the others waiting at the barrier.
+        for (int t = 0; t < itm.ntiles; ++t, ++it) {
+          const int b = it & 1;
+          if (!aborted && !mbar_wait(&tfull[b], (uint32_t)((it >> 1) & 1))) aborted = true;
+          float acc = 0.f;
+          if (!aborted) {
+            tc_fence_after();
+            float a4[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int cc = 0; cc < ncol; cc += 32) {
+              uint32_t r[32];
+              tmem_ld32(tmem + lane_addr + (uint32_t)(b * RP + c0 + cc), r);
+              const float4* nl = reinterpret_cast<const float4*>(nlse_s + c0 + cc);
+#pragma unroll
+              for (int i4 = 0; i4 < 8; ++i4) {
+                const float4 v = nl[i4];  // negated log-sum-exp of four window rows
+                a4[0] += exp2f(fmaf(__uint_as_float(r[4 * i4 + 0]), p.scale_log2, v.x));
+                a4[1] += exp2f(fmaf(__uint_as_float(r[4 * i4 + 1]), p.scale_log2, v.y));
+                a4[2] += exp2f(fmaf(__uint_as_float(r[4 * i4 + 2]), p.scale_log2, v.z));
+                a4[3] += exp2f(fmaf(__uint_as_float(r[4 * i4 + 3]), p.scale_log2, v.w));
+              }
+            }
+            acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[b]);
+          }
+          if (hf == 1) spart[b * 128 + lrow] = acc;
+          named_bar_sync(1, kEpiThreads);
+          if (hf == 0 && !aborted) {
+            const int tt = (itm.tile0 + t) * kTileTok + lrow;
+            if (tt < prefix) out[tt] = acc + spart[b * 128 + lrow];
+          }
         }
       }
     }
     if (aborted) set_status(p.status, RKV_DEV_WAIT_TIMEOUT);
-  }
-  if (PASS == 1 && ntiles == 0 && warp >= 2) {
-    // an empty split still publishes a neutral partial
-    const int e = warp - 2, hf = e >> 2, lrow = (warp & 3) * 32 + lane;
-    if (RB == 2 || hf == 0) {
-      const int rb = (RB == 2) ? hf : 0;
-      float* dst = p.part_ml + (((size_t)ukv * p.nsplit + split) * RP + rb * 128 + lrow) * 2;
-      dst[0] = -1e30f;
-      dst[1] = 0.f;
-    }
   }
   tc_fence_before();
   __syncthreads();
@@ -430,6 +455,34 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols)
                  : "memory");
   }
+}
+
+// Merge the per-split (max, sum) of every window row into its negated log2-sum-exp (padded
+// rows -> -1e30, so that they contribute nothing). Grid: units; block: RP threads.
+__global__ void lse_merge_kernel(ScoreParams p, int rp) {
+  const int ukv = blockIdx.x, r = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  const int u = ukv / p.n_kv;
+  const int L = p.seq_lens[u];
+  const bool bad = L <= p.window || L > p.max_len;
+  float m = -1e30f, l = 0.f;
+  if (!bad && r < p.gqa * p.window) {
+    const float2* pm = reinterpret_cast<const float2*>(p.part_ml) + (size_t)ukv * p.nsplit * rp + r;
+    for (int s0 = 0; s0 < p.nsplit; s0 += 8) {
+      float2 x[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        x[j] = (s0 + j < p.nsplit) ? pm[(size_t)(s0 + j) * rp] : make_float2(-1e30f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float mn = fmaxf(m, x[j].x);
+        l = l * exp2f(m - mn) + x[j].y * exp2f(x[j].x - mn);
+        m = mn;
+      }
+    }
+  }
+  const_cast<float*>(p.nlse)[(size_t)ukv * rp + r] = (l > 0.f) ? -(m + log2f(l)) : -1e30f;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -516,15 +569,15 @@ __global__ void __launch_bounds__(256) gather_kernel(SnapArgs a) {
 // ------------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------------
+// Split plan: about 16 work items per SM for balance, at least 4 tiles per item.
 void snapkv_plan(int n, int n_kv, int gqa, int max_len, int window, int* nsplit,
                  int* tokens_per_split, int* rows_pad) {
+  (void)window;
   const int units = n * n_kv;
   const int tiles = (max_len + kTileTok - 1) / kTileTok;
-  const size_t unit_bytes = (size_t)max_len * kHeadDim * 2;
-  int wave = (int)(kWaveBytes / unit_bytes);
-  wave = wave < 1 ? 1 : (wave > units ? units : wave);
-  int ns = kSMs / wave;
-  ns = ns < 1 ? 1 : (ns > tiles ? tiles : ns);
+  int ns = (16 * kSMs + units - 1) / units;
+  const int max_ns = tiles / 4 > 1 ? tiles / 4 : 1;
+  ns = ns < 1 ? 1 : (ns > max_ns ? max_ns : ns);
   const int tps = (tiles + ns - 1) / ns;
   ns = (tiles + tps - 1) / tps;
   *nsplit = ns;
@@ -532,17 +585,12 @@ void snapkv_plan(int n, int n_kv, int gqa, int max_len, int window, int* nsplit,
   *rows_pad = gqa * window <= 128 ? 128 : 256;
 }
 
-static int wave_units(int units, int max_len) {
-  const size_t unit_bytes = (size_t)max_len * kHeadDim * 2;
-  int wave = (int)(kWaveBytes / unit_bytes);
-  return wave < 1 ? 1 : (wave > units ? units : wave);
-}
-
 size_t snapkv_scratch_bytes(int n, int n_kv, int gqa, int max_len, int window) {
   int ns, tps, rp;
   snapkv_plan(n, n_kv, gqa, max_len, window, &ns, &tps, &rp);
   const size_t plen = align_up((size_t)n * n_kv * (max_len - window) * 4, 256);
-  return 2 * plen + align_up((size_t)n * n_kv * ns * rp * 2 * 4, 256);
+  return 2 * plen + align_up((size_t)n * n_kv * ns * rp * 2 * 4, 256) +
+         align_up((size_t)n * n_kv * rp * 4, 256);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -578,15 +626,12 @@ static bool make_rows_map(CUtensorMap* map, const void* base, uint64_t rows) {
          CUDA_SUCCESS;
 }
 
-template <int PASS, int RB>
-static cudaError_t launch_pass(const CUtensorMap& km, const CUtensorMap& qm,
-                               const ScoreParams& sp, int nunits, cudaStream_t s) {
-  const size_t smem = ScoreSmem<RB>::total;
-  cudaError_t e = ensure_dyn_smem((const void*)score_kernel<PASS, RB>, smem);
-  if (e != cudaSuccess) return e;
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t s, Args... args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(nunits * sp.nsplit);
-  cfg.blockDim = dim3(kScoreThreads);
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -594,7 +639,19 @@ static cudaError_t launch_pass(const CUtensorMap& km, const CUtensorMap& qm,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, score_kernel<PASS, RB>, km, qm, sp);
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <int PASS, int RB>
+static cudaError_t launch_pass(const CUtensorMap& km, const CUtensorMap& qm,
+                               const ScoreParams& sp, cudaStream_t s) {
+  const size_t smem = ScoreSmem<RB>::total;
+  cudaError_t e = ensure_dyn_smem((const void*)score_kernel<PASS, RB>, smem);
+  if (e != cudaSuccess) return e;
+  const int items = sp.units * sp.nsplit;
+  const int grid = items < kSMs ? items : kSMs;
+  e = launch_pdl_kernel(score_kernel<PASS, RB>, dim3(grid), dim3(kScoreThreads), smem, s, km, qm,
+                        sp);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -606,33 +663,30 @@ cudaError_t launch_snapkv(const SnapArgs& a, cudaStream_t s) {
   if (!make_rows_map(&km, a.k, krows) || !make_rows_map(&qm, a.q_win, qrows))
     return cudaErrorInvalidValue;
   const int units = a.n * a.n_kv;
-  const int wave = wave_units(units, a.max_len);
   ScoreParams sp{};
   sp.n_kv = a.n_kv;
   sp.gqa = a.gqa;
   sp.window = a.window;
   sp.max_len = a.max_len;
   sp.hq = a.n_kv * a.gqa;
+  sp.units = units;
   sp.nsplit = a.nsplit;
   sp.tiles_per_split = a.tokens_per_split;
   sp.scale_log2 = a.scale_log2;
   sp.seq_lens = a.seq_lens;
   sp.part_ml = a.part_ml;
+  sp.nlse = a.nlse;
   sp.scores = a.scores;
   sp.status = a.status;
-  cudaError_t e = cudaSuccess;
-  for (int u0 = 0; u0 < units; u0 += wave) {
-    const int nu = units - u0 < wave ? units - u0 : wave;
-    sp.unit0 = u0;
-    if (a.rows_pad == 128) {
-      e = launch_pass<1, 1>(km, qm, sp, nu, s);
-      if (e == cudaSuccess) e = launch_pass<2, 1>(km, qm, sp, nu, s);
-    } else {
-      e = launch_pass<1, 2>(km, qm, sp, nu, s);
-      if (e == cudaSuccess) e = launch_pass<2, 2>(km, qm, sp, nu, s);
-    }
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t e;
+  sp.reverse = 0;
+  e = a.rows_pad == 128 ? launch_pass<1, 1>(km, qm, sp, s) : launch_pass<1, 2>(km, qm, sp, s);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl_kernel(lse_merge_kernel, dim3(units), dim3(a.rows_pad), 0, s, sp, a.rows_pad);
+  if (e != cudaSuccess) return e;
+  sp.reverse = 1;
+  e = a.rows_pad == 128 ? launch_pass<2, 1>(km, qm, sp, s) : launch_pass<2, 2>(km, qm, sp, s);
+  if (e != cudaSuccess) return e;
   select_kernel<<<units, 1024, 0, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
