@@ -83,13 +83,11 @@ class HotPath:
 
     # accounting ---------------------------------------------------------------------------
     def launches_per_step(self) -> int:
-        """Kernel launches of one step (compress: 2 score passes per wave + select + gather)."""
-        unit_bytes = self.wl.max_len * D * 2
-        units = self.wl.n * self.wl.n_kv
-        wave = max(1, min(units, (64 << 20) // unit_bytes))
-        waves = (units + wave - 1) // wave
+        """Kernel launches of one step: compression = score pass 1, LSE merge, score pass 2,
+        select, gather; then the summaries; then one decode launch per step (two with appends:
+        the append kernel and the decode)."""
         per_decode = 2 if self.wl.append else 1
-        return 2 * waves + 2 + 1 + per_decode * self.dec_q.shape[0]
+        return 5 + 1 + per_decode * self.dec_q.shape[0]
 
     def decode_bytes_per_launch(self) -> int:
         """Algorithmic HBM bytes of one hybrid decode launch (all units), budget-implied:
