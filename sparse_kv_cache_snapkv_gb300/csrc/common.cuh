@@ -338,119 +338,67 @@ __device__ __noinline__ static int block_topk_ascending(const float* keys, int n
   return total;
 }
 
-// One warp chooses the k largest of keys[0..n) (n <= 128, keys in shared memory; ties -> lower
-// index) and writes their indices ascending to out[0..k). Bit-plane radix select with ballots:
-// no block barrier, no atomics. Every lane of the warp must call it. Returns the count written.
-__device__ __forceinline__ int warp_topk_small(const float* keys, int n, int k, int* out) {
-  const int lane = threadIdx.x & 31;
-  uint32_t u[4];
-  bool valid[4];
-  uint32_t hi = 0u, lo = 0xffffffffu;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int idx = 4 * lane + j;
-    valid[j] = idx < n;
-    u[j] = valid[j] ? ordered_key(keys[idx]) : 0u;
-    if (valid[j]) {
-      hi = max(hi, u[j]);
-      lo = min(lo, u[j]);
-    }
-  }
-  hi = __reduce_max_sync(0xffffffffu, hi);
-  lo = __reduce_min_sync(0xffffffffu, lo);
-  const uint32_t diff = hi ^ lo;
-  const int top = diff ? 31 - __clz(diff) : -1;  // highest bit where keys differ
-  uint32_t prefix = top < 0 ? hi : (top >= 31 ? 0u : (hi & ~((2u << top) - 1u)));
-  int remaining = k;
-  for (int b = top; b >= 0; --b) {
-    const uint32_t cand = prefix | (1u << b);
-    int cnt = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      cnt += __popc(__ballot_sync(0xffffffffu, valid[j] && (u[j] >> b) == (cand >> b)));
-    if (cnt >= remaining)
-      prefix = cand;
-    else
-      remaining -= cnt;
-  }
-  // prefix is the k-th largest key; `remaining` keys equal to it are taken, lowest index first
-  const uint32_t lt = (1u << lane) - 1u;
-  uint32_t eqb[4], selb[4];
-  bool eq[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    eq[j] = valid[j] && u[j] == prefix;
-    eqb[j] = __ballot_sync(0xffffffffu, eq[j]);
-  }
-  int eq_before = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) eq_before += __popc(eqb[j] & lt);
-  bool take[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    take[j] = valid[j] && (u[j] > prefix || (eq[j] && eq_before < remaining));
-    eq_before += eq[j] ? 1 : 0;
-    selb[j] = __ballot_sync(0xffffffffu, take[j]);
-  }
-  int pos = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) pos += __popc(selb[j] & lt);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    if (take[j]) {
-      if (pos < k) out[pos] = 4 * lane + j;
-      ++pos;
-    }
-  }
-  int total = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) total += __popc(selb[j]);
-  return total;
-}
-
 // ------------------------------------------------------------------------------------------
 // Low-latency top-k for one 256-thread block with at most NK * 256 keys.
 // ------------------------------------------------------------------------------------------
 struct __align__(16) FastSelectSmem {
-  uint32_t hist[2][4][256];  // double-buffered; warps 2p (low 16 bits) and 2p+1 (high) share row p
+  uint32_t h11[2048];        // fine histogram of the first pass (up to 11 bits)
+  uint32_t coarse[64];       // the same counts summed over 32 fine bins
+  uint32_t hist[2][4][256];  // 8-bit fallback passes, double-buffered; warps 2p, 2p+1 share row p
   uint32_t wmax[8], wmin[8];
-  int wsum[8];               // per-warp sums of the descending bin scan
-  int found[4];              // digit, keys above, keys in the digit's bin
+  int wsum[8];               // per-warp sums of a fallback pass's descending bin scan
+  int found[4];              // fallback pass: digit, keys above, keys in the digit's bin
   uint32_t cnt[16][8];       // per key round and warp: (keys above << 16) | keys equal
+  uint32_t cand_u[32];       // keys of a small final bin and their indices
+  int cand_i[32];
+  int ncand;
 };
 
-// Same contract as block_topk_ascending (k largest, ties -> lower index, indices written
-// ascending; returns the count), for blockDim.x == 256 and n <= NK * 256. Keys stay in
-// registers (key i = 256 j + tid). MSB-first radix select with 8-bit digits after the bits all
-// keys share; per pass: counts into per-warp-pair rows (atomics contend only within a warp
-// pair), thread b totals bin 255 - b, warps scan 32 bins each, the thread whose bin holds the
-// k-th key publishes it (three barriers). The search stops as soon as a whole bin is taken.
-// The in-order compaction packs per-warp (above, equal) counts of every key round.
-template <int NK>
-__device__ __forceinline__ int block_topk_fast(const float* keys, int n, int k, int* out,
-                                               FastSelectSmem& sm) {
+// First phase of block_topk_fast, to be fused into whatever produces the keys: each thread
+// passes the max / min of the ordered keys (ordered_key) it produced (0 / ~0 if none); this
+// records the per-warp range and clears the histograms. A barrier must separate it from
+// block_topk_fast (the one that publishes the keys serves).
+__device__ __forceinline__ void fast_select_prepare(uint32_t hi, uint32_t lo, FastSelectSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t u[NK];
-  bool v[NK];
-  uint32_t hi = 0u, lo = 0xffffffffu;
-#pragma unroll
-  for (int j = 0; j < NK; ++j) {
-    const int idx = j * 256 + tid;
-    v[j] = idx < n;
-    u[j] = v[j] ? ordered_key(keys[idx]) : 0u;
-    if (v[j]) {
-      hi = max(hi, u[j]);
-      lo = min(lo, u[j]);
-    }
-  }
   hi = __reduce_max_sync(0xffffffffu, hi);
   lo = __reduce_min_sync(0xffffffffu, lo);
   if (lane == 0) {
     sm.wmax[warp] = hi;
     sm.wmin[warp] = lo;
   }
+  uint4* h = reinterpret_cast<uint4*>(sm.h11);
+  h[2 * tid] = make_uint4(0u, 0u, 0u, 0u);
+  h[2 * tid + 1] = make_uint4(0u, 0u, 0u, 0u);
+  if (tid < 16) reinterpret_cast<uint4*>(sm.coarse)[tid] = make_uint4(0u, 0u, 0u, 0u);
   reinterpret_cast<uint4*>(&sm.hist[0][0][0])[tid] = make_uint4(0u, 0u, 0u, 0u);
-  __syncthreads();
+  if (tid == 0) sm.ncand = 0;
+}
+
+// Same contract as block_topk_ascending (k largest, ties -> lower index, indices written
+// ascending; returns the count), for blockDim.x == 256, 1 <= k <= n <= NK * 256, after
+// fast_select_prepare over the same keys. Keys stay in registers (key i = 256 j + tid).
+// MSB-first radix select on the bits below those all keys share. First pass: up to 11 bits
+// counted at once into a fine and a coarse histogram; every warp then finds the bin of the k-th
+// key on its own (a scan of the 64 coarse bins, then of the 32 fine bins inside the chosen one),
+// so no barrier is spent on publishing it. If that bin is taken whole the threshold is known;
+// if it holds at most 32 keys they are gathered and every warp ranks them by (key desc, index
+// asc), which yields the exact k-th key; otherwise 8-bit passes continue (three barriers each,
+// warps scan 32 bins of per-warp-pair counts). The compaction packs per-warp (above, equal)
+// counts of every key round. Ends without a barrier: the caller synchronises before reading
+// out[] or reusing `sm`.
+template <int NK>
+__device__ __forceinline__ int block_topk_fast(const float* keys, int n, int k, int* out,
+                                               FastSelectSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t u[NK];
+  bool v[NK];
+#pragma unroll
+  for (int j = 0; j < NK; ++j) {
+    const int idx = j * 256 + tid;
+    v[j] = idx < n;
+    u[j] = v[j] ? ordered_key(keys[idx]) : 0u;
+  }
+  uint32_t hi, lo;
   {
     const uint4 a0 = reinterpret_cast<const uint4*>(sm.wmax)[0];
     const uint4 a1 = reinterpret_cast<const uint4*>(sm.wmax)[1];
@@ -465,8 +413,75 @@ __device__ __forceinline__ int block_topk_fast(const float* keys, int n, int k, 
   uint32_t prefix = hi & mask;
   int remaining = k;
   bool inclusive = false;
+  if (start > 0) {
+    const int nb = start < 11 ? start : 11;
+    const int shift = start - nb;
+    const uint32_t dmask = (1u << nb) - 1u;
+#pragma unroll
+    for (int j = 0; j < NK; ++j) {
+      if (v[j]) {
+        const uint32_t d = (u[j] >> shift) & dmask;
+        atomicAdd(&sm.h11[d], 1u);
+        atomicAdd(&sm.coarse[d >> 5], 1u);
+      }
+    }
+    __syncthreads();
+    // coarse bins in descending order: lane l holds bins 63 - 2l and 62 - 2l
+    const uint2 cc = *reinterpret_cast<const uint2*>(&sm.coarse[62 - 2 * lane]);
+    const int c_hi = (int)cc.y, c_lo = (int)cc.x;
+    int incl = warp_incl_scan(c_hi + c_lo);
+    int excl = incl - c_hi - c_lo;
+    uint32_t b = __ballot_sync(0xffffffffu, excl < remaining && incl >= remaining);
+    int src = __ffs(b) - 1;
+    const int cbin_l = (excl + c_hi >= remaining) ? 63 - 2 * lane : 62 - 2 * lane;
+    const int above_l = (excl + c_hi >= remaining) ? excl : excl + c_hi;
+    const int cbin = __shfl_sync(0xffffffffu, cbin_l, src);
+    const int above_c = __shfl_sync(0xffffffffu, above_l, src);
+    // fine bins of that coarse bin, descending: lane l holds bin 32 cbin + 31 - l
+    const int f = (int)sm.h11[cbin * 32 + 31 - lane];
+    incl = warp_incl_scan(f) + above_c;
+    excl = incl - f;
+    b = __ballot_sync(0xffffffffu, excl < remaining && incl >= remaining);
+    src = __ffs(b) - 1;
+    const int digit = cbin * 32 + 31 - src;
+    const int above = __shfl_sync(0xffffffffu, excl, src);
+    const int in_bin = __shfl_sync(0xffffffffu, f, src);
+    prefix |= (uint32_t)digit << shift;
+    mask |= dmask << shift;
+    remaining -= above;
+    start = shift;
+    if (in_bin == remaining) {
+      inclusive = true;
+      start = 0;
+    } else if (start > 0 && in_bin <= 32) {
+#pragma unroll
+      for (int j = 0; j < NK; ++j) {
+        if (v[j] && (u[j] & mask) == prefix) {
+          const int slot = atomicAdd(&sm.ncand, 1);
+          sm.cand_u[slot] = u[j];
+          sm.cand_i[slot] = j * 256 + tid;
+        }
+      }
+      __syncthreads();
+      const bool mine = lane < in_bin;
+      const uint32_t cu = mine ? sm.cand_u[lane] : 0u;
+      const int ci = mine ? sm.cand_i[lane] : 0x7fffffff;
+      int rank = 0, gt = 0;
+      for (int m = 0; m < in_bin; ++m) {
+        const uint32_t ou = __shfl_sync(0xffffffffu, cu, m);
+        const int oi = __shfl_sync(0xffffffffu, ci, m);
+        gt += ou > cu ? 1 : 0;
+        rank += (ou > cu || (ou == cu && oi < ci)) ? 1 : 0;
+      }
+      b = __ballot_sync(0xffffffffu, mine && rank == remaining - 1);
+      src = __ffs(b) - 1;
+      prefix = __shfl_sync(0xffffffffu, cu, src);
+      remaining -= __shfl_sync(0xffffffffu, gt, src);
+      start = 0;
+    }
+  }
   const uint32_t inc = (warp & 1) ? 0x10000u : 1u;
-  for (int pass = 0; start > 0; ++pass) {
+  for (int pass = 0; start > 0 && !inclusive; ++pass) {
     const int nb = start < 8 ? start : 8;
     const int shift = start - nb;
     const uint32_t dmask = (1u << nb) - 1u;
@@ -543,7 +558,122 @@ __device__ __forceinline__ int block_topk_fast(const float* keys, int n, int k, 
     gt_acc += (int)(all >> 16);
     eq_acc += (int)(all & 0xffffu);
   }
-  __syncthreads();
+  return gt_acc + min(eq_acc, need_eq);
+}
+
+// Top-k of 128 keys within one warp (no block barrier): keys already mapped by ordered_key
+// in shared memory (ukeys[0..127]); lane l holds keys l, l + 32, l + 64, l + 96. Same contract as
+// block_topk_fast (k largest, ties -> lower index, indices written ascending to out[0..k),
+// returns the count; 1 <= k <= 128). MSB-first radix select on the bits below those all keys
+// share, 8-bit digits counted in `hist` (256 words of warp-private scratch); once the k-th key's
+// bin holds at most 32 keys they are gathered in index order into `cand` (32 words of
+// warp-private scratch) and ranked directly by (key desc, index asc). Only the calling warp may
+// touch hist / cand meanwhile.
+__device__ __forceinline__ int warp_topk128(const uint32_t* ukeys, int k, int* out,
+                                            uint32_t* hist, uint32_t* cand) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t lt = (1u << lane) - 1u;
+  uint32_t u[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) u[j] = ukeys[32 * j + lane];
+  const uint32_t hi =
+      __reduce_max_sync(0xffffffffu, max(max(u[0], u[1]), max(u[2], u[3])));
+  const uint32_t lo =
+      __reduce_min_sync(0xffffffffu, min(min(u[0], u[1]), min(u[2], u[3])));
+  const uint32_t diff = hi ^ lo;
+  int start = diff ? 32 - __clz(diff) : 0;
+  uint32_t mask = start >= 32 ? 0u : ~((1u << start) - 1u);
+  uint32_t prefix = hi & mask;
+  int remaining = k;
+  bool inclusive = false;
+  while (start > 0 && !inclusive) {
+    const int nb = start < 8 ? start : 8;
+    const int shift = start - nb;
+    const uint32_t dmask = (1u << nb) - 1u;
+    uint4* h4 = reinterpret_cast<uint4*>(hist);
+    __syncwarp();  // the previous pass's reads of hist are done
+    h4[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
+    h4[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if ((u[j] & mask) == prefix) atomicAdd(&hist[(u[j] >> shift) & dmask], 1u);
+    __syncwarp();
+    // lane l holds bins 255 - 8l .. 248 - 8l (descending)
+    const uint4 g0 = h4[62 - 2 * lane], g1 = h4[63 - 2 * lane];
+    const int c8[8] = {(int)g1.w, (int)g1.z, (int)g1.y, (int)g1.x,
+                       (int)g0.w, (int)g0.z, (int)g0.y, (int)g0.x};
+    int own = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) own += c8[j];
+    const int incl = warp_incl_scan(own);
+    const int excl = incl - own;
+    int dl = 0, al = 0, nl = 0;
+    {
+      int acc = excl;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (acc < remaining && acc + c8[j] >= remaining) {
+          dl = 255 - 8 * lane - j;
+          al = acc;
+          nl = c8[j];
+        }
+        acc += c8[j];
+      }
+    }
+    const uint32_t b = __ballot_sync(0xffffffffu, excl < remaining && incl >= remaining);
+    const int src = __ffs(b) - 1;
+    const int digit = __shfl_sync(0xffffffffu, dl, src);
+    const int above = __shfl_sync(0xffffffffu, al, src);
+    const int in_bin = __shfl_sync(0xffffffffu, nl, src);
+    prefix |= (uint32_t)digit << shift;
+    mask |= dmask << shift;
+    remaining -= above;
+    start = shift;
+    if (in_bin == remaining) {
+      inclusive = true;
+    } else if (start > 0 && in_bin <= 32) {
+      // gather the bin's keys (index order) and rank them
+      int base = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool m = (u[j] & mask) == prefix;
+        const uint32_t bm = __ballot_sync(0xffffffffu, m);
+        if (m) cand[base + __popc(bm & lt)] = u[j];
+        base += __popc(bm);
+      }
+      __syncwarp();
+      const bool mine = lane < in_bin;
+      const uint32_t cu = mine ? cand[lane] : 0u;
+      int rank = 0, gt = 0;
+      for (int m = 0; m < in_bin; ++m) {
+        const uint32_t ou = cand[m];  // candidates are in index order: m < lane is lower
+        gt += ou > cu ? 1 : 0;
+        rank += (ou > cu || (ou == cu && m < lane)) ? 1 : 0;
+      }
+      const uint32_t bt = __ballot_sync(0xffffffffu, mine && rank == remaining - 1);
+      const int st = __ffs(bt) - 1;
+      prefix = __shfl_sync(0xffffffffu, cu, st);
+      remaining -= __shfl_sync(0xffffffffu, gt, st);
+      start = 0;
+      __syncwarp();
+    }
+  }
+  // compaction in index order (round j, then lane)
+  const int need_eq = inclusive ? 0 : remaining;
+  int gt_acc = 0, eq_acc = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const bool g = inclusive ? u[j] >= prefix : u[j] > prefix;
+    const bool e = !inclusive && u[j] == prefix;
+    const uint32_t bg = __ballot_sync(0xffffffffu, g);
+    const uint32_t be = __ballot_sync(0xffffffffu, e);
+    const int eq_before = eq_acc + __popc(be & lt);
+    const int pos = gt_acc + __popc(bg & lt) + min(eq_before, need_eq);
+    if ((g || (e && eq_before < need_eq)) && pos < k) out[pos] = 32 * j + lane;
+    gt_acc += __popc(bg);
+    eq_acc += __popc(be);
+  }
   return gt_acc + min(eq_acc, need_eq);
 }
 

@@ -9,9 +9,10 @@
 // Direct Latency Comparison" (half of the budget to the approximation, half to exact sparse
 // attention), "Are Different KV Tokens Retrieved at Each Decoding Step?" (selection per step).
 //
-// Memory movement: the kept channels' summary rows and the K/V rows of the selected pages are
-// staged in shared memory by cp.async.bulk (one copy per row, all of a stage in flight at once,
-// completion on an mbarrier). K/V rows are stored 272 bytes apart so that ldmatrix reads them
+// Memory movement: the approximate scores read the kept channels' summary rows straight from
+// global memory into registers (a vector-matrix product: fp32 FMAs, no staging); the K/V rows of
+// the selected pages are staged in shared memory by 16-byte cp.async copies, each warp group
+// the 64-token chunk it attends over, rows padded by 16 bytes so that ldmatrix reads them
 // without bank conflicts.
 //
 // Attention arithmetic: warp-level mma.sync m16n8k16 (bf16 in, fp32 accumulate). The G query
@@ -74,7 +75,24 @@ struct MmaAttn {
   int lane, r0, t;
 
   // Q fragments are shared by every warp of the CTA: built once in shared memory by one warp
-  // (row r0 = lane / 4 < G holds query head r0; rows >= G are zero).
+  // from the fp32 copy of q (exact: the values are bf16); row r0 = lane / 4 < G holds query head
+  // r0, rows >= G are zero.
+  static __device__ __forceinline__ void build_fragments(const float* q_group, uint2* frag) {
+    const int ln = threadIdx.x & 31, rr = ln >> 2, tt = ln & 3;
+    const float* qr = q_group + rr * kHeadDim;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      uint2 f = make_uint2(0u, 0u);
+      if (rr < G) {
+        const float2 x = *reinterpret_cast<const float2*>(qr + ks * 16 + 2 * tt);
+        const float2 y = *reinterpret_cast<const float2*>(qr + ks * 16 + 8 + 2 * tt);
+        f = make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(y.x, y.y));
+      }
+      frag[ks * 32 + ln] = f;
+    }
+  }
+
+  // The same fragments straight from the bf16 q rows in global memory.
   static __device__ __forceinline__ void build_fragments(const bf16* q_group, uint2* frag) {
     const int ln = threadIdx.x & 31, rr = ln >> 2, tt = ln & 3;
     const uint32_t* qw = reinterpret_cast<const uint32_t*>(q_group + rr * kHeadDim);
@@ -234,73 +252,6 @@ __device__ __forceinline__ void group_sync(int group) {
   asm volatile("bar.sync %0, 128;" ::"r"(1 + group) : "memory");
 }
 
-// D (16 x 8) += A (16 x 16) B (16 x 8), all four accumulators of a lane kept.
-__device__ __forceinline__ void mma_full(float (&d)[4], const uint4& a, uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
-}
-
-// Approximate page scores of one staged block on the tensor cores. A row 0 holds bf16(w) and
-// row 8 the bf16 remainder w - bf16(w) for the kept channels (wfrag, one uint4 per lane and
-// 16-channel step), B = the staged summary rows (channels x pages) read by ldmatrix.trans, so
-// lanes 0..3 end up with both partial sums of their pages: score = D[row 0] + D[row 8]. Each
-// warp takes four 16-page tiles per iteration (tiles warp, +8, +16, +24).
-template <int NKS>
-__device__ __forceinline__ void score_block(const bf16* rows, int rs, int npairs,
-                                            const uint4* wfrag, float* scores, float* approx,
-                                            int pb, int limit) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, t = lane & 3;
-  const int krow = (lane & 7) + (((lane >> 3) & 1) << 3), pcol = (lane >> 4) << 3;
-  const uint32_t base = smem_addr(rows + (size_t)krow * rs + pcol);
-  uint4 wa[NKS];
-#pragma unroll
-  for (int ks = 0; ks < NKS; ++ks) wa[ks] = wfrag[ks * 32 + lane];
-  for (int pq = warp; pq < npairs; pq += 32) {
-    float d[4][2][4];
-#pragma unroll
-    for (int x = 0; x < 4; ++x)
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) d[x][nt][0] = d[x][nt][1] = d[x][nt][2] = d[x][nt][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < NKS; ++ks) {
-      uint32_t b[4][4];
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int pair = min(pq + 8 * x, npairs - 1);
-        ldsm_x4_t(base + (uint32_t)(ks * 16 * rs * 2 + pair * 32), b[x][0], b[x][1], b[x][2],
-                  b[x][3]);
-      }
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        mma_full(d[x][0], wa[ks], b[x][0], b[x][1]);
-        mma_full(d[x][1], wa[ks], b[x][2], b[x][3]);
-      }
-    }
-    if (lane < 4) {
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int pair = pq + 8 * x;
-        if (pair < npairs) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int nt = e >> 1, c = e & 1;
-            const int pg = pb + pair * 16 + nt * 8 + 2 * t + c;
-            const float v = d[x][nt][c] + d[x][nt][c + 2];
-            if (pg < limit) {
-              scores[pg] = v;
-              if (approx) approx[pg] = v;
-            }
-          }
-        }
-      }
-    }
-  }
-}
-
 // ==========================================================================================
 // Hybrid sparse decode: one CTA of 8 warps per (unit, KV head).
 // ==========================================================================================
@@ -308,7 +259,7 @@ size_t hybrid_smem_bytes(int gqa, int page_cap, int budget, int page) {
   (void)gqa;
   (void)budget;
   (void)page;
-  size_t b = (size_t)kDecStages * kStageBytes;  // stages (also summary rows, warp combine)
+  size_t b = (size_t)kDecStages * kStageBytes;  // K/V stages (also the warp combine)
   b += align_up((size_t)page_cap * 4, 16);       // approximate scores
   b += align_up((size_t)page_cap * 4, 16);       // selected pages
   return b;
@@ -318,17 +269,14 @@ template <int G>
 __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(HybridArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
   __shared__ float qs[G * kHeadDim];
-  __shared__ float mag[kHeadDim];
+  __shared__ __align__(16) uint32_t umag[kHeadDim];
   __shared__ float qg[kHeadDim];
   __shared__ int chosen[kHeadDim];
-  __shared__ float wsel[kHeadDim];
-  __shared__ __align__(8) uint64_t sbar;
   __shared__ union {
     SelectScratch generic;
     FastSelectSmem fast;
   } sel_smem;
   __shared__ uint2 qfrag[8 * 32];
-  __shared__ uint4 wfrag[8 * 32];
 
   bf16* stages = reinterpret_cast<bf16*>(smem);
   float* scores = reinterpret_cast<float*>(smem + (size_t)kDecStages * kStageBytes);
@@ -342,6 +290,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
   const int hq = a.n_kv * G;
   pdl_wait();     // inputs may come from the kernel before this one in the stream
   pdl_trigger();  // the next decode step may be scheduled while this one runs
+  // q and len are loaded together (q's address does not depend on len)
+  const bf16* qgroup = a.q + ((size_t)u * hq + g * G) * kHeadDim;
+  uint4 qraw = make_uint4(0u, 0u, 0u, 0u);
+  if (tid < G * 16) qraw = *reinterpret_cast<const uint4*>(qgroup + tid * 8);
   const int len = a.len[u];
   const int p = a.page;
   const int P = (len + p - 1) / p;
@@ -352,20 +304,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
     if (tid == 0 && len != 0) set_status(a.status, RKV_DEV_LEN_OVER_CAP);
     return;
   }
-  const bf16* qgroup = a.q + ((size_t)u * hq + g * G) * kHeadDim;
 
   // ---- q: raw values to shared memory -------------------------------------------------
   if (tid < G * 16) {
-    const int h = tid >> 4, c8 = (tid & 15) * 8;
-    const uint4 c = *reinterpret_cast<const uint4*>(qgroup + h * kHeadDim + c8);
     float f[8];
-    unpack8(c, f);
+    unpack8(qraw, f);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) qs[h * kHeadDim + c8 + i] = f[i];
+    for (int i = 0; i < 8; ++i) qs[tid * 8 + i] = f[i];
   }
-  if (warp == 7) MmaAttn<G>::build_fragments(qgroup, qfrag);
-  if (tid == 0) mbar_init(&sbar, 1);
-  fence_barrier_init();
   __syncthreads();
 
   // ---- group sums: |q| for the channel pick, signed q for the score --------------------
@@ -377,108 +323,81 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
       s += fabsf(x);
       t += x;
     }
-    mag[tid] = s;
+    umag[tid] = ordered_key(s);
     qg[tid] = t;
   }
+  if (warp == 7) MmaAttn<G>::build_fragments(qs, qfrag);
   __syncthreads();
 
   int nsel;
   if (!dense) {
     // ---- channel pick: top-c of sum_h |q_h| (ties -> lower channel), ascending -----------
-    {
-      const int got = block_topk_fast<1>(mag, kHeadDim, a.channels, chosen, sel_smem.fast);
-      if (got != a.channels && tid == 0) set_status(a.status, RKV_DEV_SELECT_FAILED);
-    }
-    if (tid < a.channels) {
-      wsel[tid] = qg[chosen[tid] & (kHeadDim - 1)];
-      if (a.sel_channels) a.sel_channels[(size_t)ukv * a.channels + tid] = chosen[tid];
+    const int cn = a.channels;
+    if (warp == 0) {
+      // warp-private scratch: the first 256 words of the page select's fine histogram (cleared
+      // again before that select) and 32 words of its second fallback buffer
+      const int got = warp_topk128(umag, cn, chosen, sel_smem.fast.h11,
+                                   &sel_smem.fast.hist[1][0][0]);
+      if (got != cn && lane == 0) set_status(a.status, RKV_DEV_SELECT_FAILED);
     }
     __syncthreads();
+    if (a.sel_channels && tid < cn) a.sel_channels[(size_t)ukv * cn + tid] = chosen[tid];
 
-    // ---- approximate page scores on the tensor cores ------------------------------------
-    // score[pg] = sum_i w_i R_i[pg] for the kept channels' summary rows R_i (Kmax where
-    // q_g >= 0, else Kmin), staged in shared memory by one bulk copy per row (one memory round
-    // trip), rows np16 + 8 elements apart so that ldmatrix.trans reads them conflict-free. Each
-    // m16n8k16 MMA takes 16 channels x 8 pages: A row 0 holds bf16(w) and row 1 the bf16 remainder
-    // w - bf16(w) (together ~16 bits of w), so score = D[0] + D[1], accumulated in fp32.
-    const int cn = a.channels;
-    const int nks = (cn + 15) >> 4;  // 16-channel steps
-    if (warp == 0) {
-      // lanes 0..3 (A rows 0 and 8): bf16(w) in row 0, the bf16 remainder in row 8
-      for (int ks = 0; ks < nks; ++ks) {
-        const int t = lane & 3;
-        uint4 f = make_uint4(0u, 0u, 0u, 0u);
-        if (lane < 4) {
-          float hi4[4], lo4[4];
+    // ---- approximate page scores -------------------------------------------------------
+    // score[pg] = sum_i w_i R_i[pg] with w_i = q_g of kept channel i and R_i its summary row
+    // (Kmax where q_g >= 0, else Kmin): a vector-matrix product over the kept rows, bound by
+    // HBM, so plain fp32 FMAs on rows read straight from global memory (nothing staged).
+    // Thread pair (2p, 2p + 1) takes the 8-page groups p, p + 128, ... (16 bytes of a row) over
+    // the even / odd kept channels; one shuffle joins the pair's partial sums. The same pass
+    // records the range of the scores' ordered keys and clears the select's histograms.
+    {
+      const int h = tid & 1, pr = tid >> 1;
+      const int ngroups = (P + 7) >> 3;
+      const size_t rowbase = (size_t)ukv * kHeadDim;
+      float* approx_row = a.approx ? a.approx + (size_t)ukv * a.page_cap : nullptr;
+      uint32_t khi = 0u, klo = 0xffffffffu;
+      for (int gb = 0; gb < ngroups; gb += kDecodeThreads / 2) {
+        const int gi = gb + pr;
+        const bool valid = gi < ngroups;
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        if (valid) {
+          const size_t col = (size_t)gi * 8;
+#pragma unroll 8
+          for (int i = h; i < cn; i += 2) {
+            const int c = chosen[i] & (kHeadDim - 1);
+            const float w = qg[c];
+            const bf16* row = ((w >= 0.f) ? a.kmax : a.kmin) + (rowbase + c) * a.page_cap;
+            const uint4 x = __ldg(reinterpret_cast<const uint4*>(row + col));
+            float f[8];
+            unpack8(x, f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(w, f[e], acc[e]);
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 1);
+        if (valid) {
+          // both threads of the pair hold the 8 sums; thread h publishes pages 4h .. 4h + 3
+          const int p0 = gi * 8 + 4 * h;
+          const float4 o = h ? make_float4(acc[4], acc[5], acc[6], acc[7])
+                             : make_float4(acc[0], acc[1], acc[2], acc[3]);
+          *reinterpret_cast<float4*>(scores + p0) = o;
+          const float ov[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int i = ks * 16 + 2 * t + (e & 1) + (e >> 1) * 8;
-            const float w = i < cn ? wsel[i] : 0.f;
-            hi4[e] = __bfloat162float(__float2bfloat16_rn(w));
-            lo4[e] = w - hi4[e];
+            if (p0 + e < P) {
+              const uint32_t kk = ordered_key(ov[e]);
+              khi = max(khi, kk);
+              klo = min(klo, kk);
+              if (approx_row) approx_row[p0 + e] = ov[e];
+            }
           }
-          f.x = pack_bf16x2(hi4[0], hi4[1]);  // row 0, k 2t..2t+1
-          f.y = pack_bf16x2(lo4[0], lo4[1]);  // row 8
-          f.z = pack_bf16x2(hi4[2], hi4[3]);  // row 0, k 2t+8..
-          f.w = pack_bf16x2(lo4[2], lo4[3]);  // row 8
-        }
-        wfrag[ks * 32 + lane] = f;
-      }
-    }
-    const int Ppad = (P + 7) & ~7;
-    int pblk = ((int)(((size_t)kDecStages * kStageBytes) / ((size_t)nks * 32)) - 8) & ~15;
-    if (pblk > Ppad) pblk = (Ppad + 15) & ~15;
-    const size_t rowbase = (size_t)ukv * kHeadDim;
-    uint32_t sphase = 0;
-    for (int pb = 0; pb < Ppad; pb += pblk) {
-      const int np = min(pblk, Ppad - pb);  // pages copied (a multiple of 8)
-      const int np16 = (np + 15) & ~15;      // pages multiplied (a multiple of 16)
-      const int rs = np16 + 8;               // staged row stride (elements)
-      if (warp == 0) {
-        if (lane == 0) mbar_arrive_expect_tx(&sbar, (uint32_t)(cn * np * 2));
-        __syncwarp();
-        for (int i = lane; i < cn; i += 32) {
-          const int c = chosen[i] & (kHeadDim - 1);
-          const bf16* base = (qg[c] >= 0.f) ? a.kmax : a.kmin;
-          bulk_g2s(stages + (size_t)i * rs, base + (rowbase + c) * a.page_cap + pb,
-                   (uint32_t)(np * 2), &sbar);
         }
       }
-      // channel rows past cn (up to the 16-step) are multiplied by zero weights: make them zero
-      for (int i = tid; i < (nks * 16 - cn) * (rs / 8); i += kDecodeThreads) {
-        const int r = cn + i / (rs / 8), c8 = i % (rs / 8);
-        *reinterpret_cast<uint4*>(stages + (size_t)r * rs + c8 * 8) = make_uint4(0u, 0u, 0u, 0u);
-      }
-      // one thread waits for the rows; the barrier then publishes them to the block
-      bool ok = true;
-      if (tid == 0) ok = mbar_wait(&sbar, sphase);
-      sphase ^= 1u;
-      if (__syncthreads_or(!ok)) {
-        if (tid == 0) set_status(a.status, RKV_DEV_WAIT_TIMEOUT);
-        mbar_wait(&sbar, sphase ^ 1u);  // let the copies land before the CTA retires
-        return;
-      }
-      {
-        const int npairs = np16 >> 4;  // 16-page tiles
-        float* approx_row = a.approx ? a.approx + (size_t)ukv * a.page_cap : nullptr;
-        const int limit = min(P, pb + np);
-        switch (nks) {
-#define RKV_SCORE(NK)                                                                        \
-  case NK:                                                                                   \
-    score_block<NK>(stages, rs, npairs, wfrag, scores, approx_row, pb, limit);               \
-    break;
-          RKV_SCORE(1)
-          RKV_SCORE(2)
-          RKV_SCORE(3)
-          RKV_SCORE(4)
-          RKV_SCORE(5)
-          RKV_SCORE(6)
-          RKV_SCORE(7)
-          RKV_SCORE(8)
-#undef RKV_SCORE
-        }
-      }
-      __syncthreads();  // the staging area is refilled by the next block / the K/V stages
+      fast_select_prepare(khi, klo, sel_smem.fast);
+      __syncthreads();
     }
 
     // ---- page top-k ----------------------------------------------------------------------
