@@ -178,27 +178,8 @@ template <int G>
 struct CombineSmem {
   float m[8][G];
   float l[8][G];
-  float f[8][G];     // merge factor 2^(m_w - M) / L of warp w for head h
   float o[8][G][kHeadDim];
 };
-
-// Per head: the max over warps, each warp's factor 2^(m_w - M) and the inverse of the merged sum
-// (threads tid < G, after the deposit and a barrier). Returns nothing; fills cs->f.
-template <int G>
-__device__ __forceinline__ void merge_factors(CombineSmem<G>* cs, int h) {
-  float mm = -1e30f;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) mm = fmaxf(mm, cs->m[w][h]);
-  float f[8], ll = 0.f;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    f[w] = exp2f(cs->m[w][h] - mm);
-    ll = fmaf(cs->l[w][h], f[w], ll);
-  }
-  const float inv = ll > 0.f ? 1.f / ll : 0.f;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) cs->f[w][h] = f[w] * inv;
-}
 
 template <int G>
 __device__ __forceinline__ void warp_deposit(const MmaAttn<G>& at, CombineSmem<G>* cs) {
@@ -326,8 +307,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
     umag[tid] = ordered_key(s);
     qg[tid] = t;
   }
-  if (warp == 7) MmaAttn<G>::build_fragments(qs, qfrag);
   __syncthreads();
+  if (warp == 7) MmaAttn<G>::build_fragments(qs, qfrag);  // overlaps the channel pick
 
   int nsel;
   if (!dense) {
@@ -429,69 +410,62 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
   }
 
   // ---- exact attention over the selected pages -------------------------------------------
-  // Chunks of 64 tokens alternate between two stages; warp group wg (warps 4wg .. 4wg+3)
-  // processes chunks wg, wg + 2, ... from stage wg, 16 tokens per warp.
-  const int ppc = kChunkTokens / p;
-  const int nchunks = (nsel + ppc - 1) / ppc;
+  // The selected pages' tokens, in page order, are cut into 16-token units; warp w takes units
+  // w, w + 8, ...: it stages the unit's K and V rows with 16-byte cp.async into its own area
+  // (rows kRowPad apart), waits for its own copies only, and runs one MMA step over them.
   const size_t cache_base = (size_t)ukv * a.cap;
-  const int wg = warp >> 2, wig = warp & 3, gtid = tid & 127;
-
-  auto chunk_tokens = [&](int c) {
-    const int j0 = c * ppc, j1 = min(nsel, j0 + ppc);
-    return (j1 - j0 - 1) * p + min(p, len - sel[j1 - 1] * p);
-  };
-  // The 128 threads of a group stage one chunk: 16-byte cp.async copies of K and V rows into
-  // rows kRowPad apart.
   const int lp = __ffs(p) - 1;  // log2(page)
-  auto load = [&](int c) {
-    bf16* Ks = stages + (size_t)wg * kStageElems;
-    const int j0 = c * ppc;
-    const int nt = chunk_tokens(c);
-    for (int idx = gtid; idx < nt * 32; idx += 128) {
-      const int r = idx >> 5, tv = (idx >> 4) & 1, c16 = idx & 15;
-      const size_t tok = ((size_t)sel[j0 + (r >> lp)] << lp) + (r & (p - 1));
-      const bf16* src = (tv ? a.v_cache : a.k_cache) + (cache_base + tok) * kHeadDim + c16 * 8;
-      cp_async16(Ks + tv * (kChunkTokens * kRowPad) + r * kRowPad + c16 * 8, src);
-    }
-    cp_async_commit();
-  };
-  if (wg < nchunks) load(wg);
-
+  const int ntok_all = (nsel - 1) * p + min(p, len - sel[nsel - 1] * p);
+  const int nunits = (ntok_all + 15) >> 4;
+  bf16* Kw = stages + (size_t)warp * (2 * 16 * kRowPad);
+  bf16* Vw = Kw + 16 * kRowPad;
   MmaAttn<G> at;
   at.init(qfrag);
-  for (int c = wg; c < nchunks; c += 2) {
-    cp_async_wait_all();
-    group_sync(wg);
-    const bf16* Ks = stages + (size_t)wg * kStageElems;
-    bf16* Vs = stages + (size_t)wg * kStageElems + kChunkTokens * kRowPad;
-    const int nt = chunk_tokens(c);
-    if (nt < kChunkTokens) {
-      zero_tail_rows(Vs, nt, gtid);
-      group_sync(wg);
+  for (int t = warp; t < nunits; t += kDecodeThreads / 32) {
+    const int v0 = t * 16;
+    const int nt = min(16, ntok_all - v0);
+    // lanes 0..15 copy a K row, lanes 16..31 the V row of the same token, 16 bytes each
+    const int half = (lane >> 4) & 1, c16 = lane & 15;
+    const bf16* cache = half ? a.v_cache : a.k_cache;
+    bf16* dst = (half ? Vw : Kw) + c16 * 8;
+    for (int r = 0; r < nt; ++r) {
+      const int v = v0 + r;
+      const size_t tok = ((size_t)sel[v >> lp] << lp) + (v & (p - 1));
+      cp_async16(dst + r * kRowPad, cache + (cache_base + tok) * kHeadDim + c16 * 8);
     }
-    if (wig * 16 < nt) at.step16(Ks, Vs, wig * 16, nt, a.scale_log2);
-    group_sync(wg);
-    if (c + 2 < nchunks) load(c + 2);
+    cp_async_commit();
+    // V rows past the unit's tokens meet P = 0: make them zero, not stale bits (0 * NaN)
+    for (int i = lane; i < (16 - nt) * 16; i += 32)
+      *reinterpret_cast<uint4*>(Vw + (nt + (i >> 4)) * kRowPad + (i & 15) * 8) =
+          make_uint4(0u, 0u, 0u, 0u);
+    cp_async_wait_all();
+    __syncwarp();
+    at.step16(Kw, Vw, 0, nt, a.scale_log2);
+    __syncwarp();  // the next unit refills this warp's rows
   }
   __syncthreads();
 
   CombineSmem<G>* cs = reinterpret_cast<CombineSmem<G>*>(smem);
   warp_deposit<G>(at, cs);
   __syncthreads();
-  if (tid < G) merge_factors<G>(cs, tid);
-  __syncthreads();
+  // output pair (h, c): merge the 8 warps' partial states, each thread forming head h's factors
   for (int i = tid; i < G * kHeadDim / 2; i += kDecodeThreads) {
     const int h = i >> 6, c = (i & 63) * 2;
-    float o0 = 0.f, o1 = 0.f;
+    float mm = -1e30f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) mm = fmaxf(mm, cs->m[w][h]);
+    float ll = 0.f, o0 = 0.f, o1 = 0.f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-      const float f = cs->f[w][h];
+      const float f = exp2f(cs->m[w][h] - mm);
       const float2 x = *reinterpret_cast<const float2*>(&cs->o[w][h][c]);
+      ll = fmaf(cs->l[w][h], f, ll);
       o0 = fmaf(f, x.x, o0);
       o1 = fmaf(f, x.y, o1);
     }
+    const float inv = ll > 0.f ? 1.f / ll : 0.f;
     *reinterpret_cast<uint32_t*>(a.out + ((size_t)u * hq + g * G + h) * kHeadDim + c) =
-        pack_bf16x2(o0, o1);
+        pack_bf16x2(o0 * inv, o1 * inv);
   }
 }
 
