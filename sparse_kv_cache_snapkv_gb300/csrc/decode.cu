@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
         if (valid) {
           const size_t col = (size_t)gi * 8;
-#pragma unroll 8
+#pragma unroll 16
           for (int i = h; i < cn; i += 2) {
             const int c = chosen[i] & (kHeadDim - 1);
             const float w = qg[c];

@@ -525,6 +525,221 @@ __global__ void __launch_bounds__(1024) select_kernel(SnapArgs a) {
 }
 
 // ------------------------------------------------------------------------------------------
+// pooling + top-k selection with the whole unit in shared memory (n = L - W <= 32768 scores,
+// pooling kernel 2^k - 1): one CTA of 1024 threads per (unit, KV head); thread t owns the 32
+// consecutive positions [32t, 32t + 32).
+// ------------------------------------------------------------------------------------------
+constexpr int kSelThreads = 1024;
+constexpr int kSelPerThread = 32;
+constexpr int kSelMaxN = kSelThreads * kSelPerThread;  // 32768
+
+// shared-memory slot of position i: one pad word per 32 keeps a thread's run conflict-free
+__device__ __forceinline__ int sel_slot(int i) { return i + (i >> 5); }
+
+size_t select_fast_smem_bytes() { return (size_t)(kSelMaxN + kSelMaxN / 32) * 4; }
+
+// Max pooling over [max(0, i - r), min(n - 1, i + r)] for 2r + 1 = 2^k - 1 by doubling: with
+// m_w[i] = max over [i, min(i + w - 1, n - 1)], m_{2w}[i] = max(m_w[i], m_w[i + w]); once
+// w = r + 1, the pooled value is max(m_w[max(0, i - r)], m_w[i]) (the two runs meet or overlap
+// and end exactly at the window's clipped edges). Then a radix select over the ordered keys.
+__global__ void __launch_bounds__(kSelThreads, 1) select_fast_kernel(SnapArgs a) {
+  extern __shared__ __align__(16) float sh[];
+  __shared__ uint32_t hist[2048];
+  __shared__ int wsum[32], wsum2[32];
+  __shared__ uint32_t wmax[32], wmin[32];
+  __shared__ int found[4];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ukv = blockIdx.x;
+  const int u = ukv / a.n_kv, g = ukv - u * a.n_kv;
+  const int W = a.window;
+  const int L = a.seq_lens[u];
+  int32_t* kept = a.kept_idx + (size_t)ukv * a.keep;
+  if (L <= W || L > a.max_len) {
+    for (int i = tid; i < a.keep; i += kSelThreads) kept[i] = -1;
+    if (g == 0 && tid == 0) a.out_len[u] = 0;
+    return;
+  }
+  if (L <= a.keep) {
+    for (int i = tid; i < a.keep; i += kSelThreads) kept[i] = i < L ? i : -1;
+    if (g == 0 && tid == 0) a.out_len[u] = L;
+    return;
+  }
+  const int n = L - W;  // <= kSelMaxN (checked by the launcher)
+  const int ks = a.kernel_size > 0 ? a.kernel_size : adaptive_kernel(L);
+  const int r = ks / 2;
+  const float* in = a.scores + (size_t)ukv * (a.max_len - W);
+  for (int i = tid; i < n; i += kSelThreads) sh[sel_slot(i)] = in[i];
+  for (int i = tid; i < 2048; i += kSelThreads) hist[i] = 0u;
+  __syncthreads();
+
+  const int base = tid * kSelPerThread;
+  float x[kSelPerThread];
+  for (int w = 1; w <= r; w *= 2) {  // m_w -> m_2w until 2w = r + 1
+#pragma unroll
+    for (int q = 0; q < kSelPerThread; ++q) {
+      const int i = base + q;
+      float v = -INFINITY;
+      if (i < n) {
+        v = sh[sel_slot(i)];
+        if (i + w < n) v = fmaxf(v, sh[sel_slot(i + w)]);
+      }
+      x[q] = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < kSelPerThread; ++q)
+      if (base + q < n) sh[sel_slot(base + q)] = x[q];
+    __syncthreads();
+  }
+  uint32_t hi = 0u, lo = 0xffffffffu;
+#pragma unroll
+  for (int q = 0; q < kSelPerThread; ++q) {
+    const int i = base + q;
+    float v = 0.f;
+    if (i < n) v = fmaxf(sh[sel_slot(max(0, i - r))], sh[sel_slot(i)]);
+    x[q] = v;
+  }
+  __syncthreads();
+  uint32_t* key = reinterpret_cast<uint32_t*>(sh);
+#pragma unroll
+  for (int q = 0; q < kSelPerThread; ++q) {
+    const int i = base + q;
+    if (i < n) {
+      const uint32_t kk = ordered_key(x[q]);
+      key[sel_slot(i)] = kk;
+      hi = max(hi, kk);
+      lo = min(lo, kk);
+    }
+  }
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  if (lane == 0) {
+    wmax[warp] = hi;
+    wmin[warp] = lo;
+  }
+  __syncthreads();
+  hi = 0u;
+  lo = 0xffffffffu;
+  for (int w = 0; w < 32; ++w) {
+    hi = max(hi, wmax[w]);
+    lo = min(lo, wmin[w]);
+  }
+
+  // ---- radix select of the `want` largest (ties -> lower position) -----------------------
+  const int want = a.keep - W;
+  const uint32_t diff = hi ^ lo;
+  int start = diff ? 32 - __clz(diff) : 0;
+  uint32_t mask = start >= 32 ? 0u : ~((1u << start) - 1u);
+  uint32_t prefix = hi & mask;
+  int remaining = want;
+  bool inclusive = false;
+  while (start > 0 && !inclusive) {
+    const int nb = start < 11 ? start : 11;
+    const int shift = start - nb;
+    const uint32_t dmask = (1u << nb) - 1u;
+    // counts, one atomic per run of equal digits (pooling repeats maxima)
+    uint32_t run_d = 0u;
+    uint32_t run_c = 0u;
+#pragma unroll
+    for (int q = 0; q < kSelPerThread; ++q) {
+      const int i = base + q;
+      if (i < n) {
+        const uint32_t kk = key[sel_slot(i)];
+        if ((kk & mask) == prefix) {
+          const uint32_t d = (kk >> shift) & dmask;
+          if (run_c > 0u && d != run_d) {
+            atomicAdd(&hist[run_d], run_c);
+            run_c = 0u;
+          }
+          run_d = d;
+          ++run_c;
+        }
+      }
+    }
+    if (run_c > 0u) atomicAdd(&hist[run_d], run_c);
+    __syncthreads();
+    // thread t holds bins 2047 - 2t and 2046 - 2t (descending), and clears them for the next pass
+    const int c_hi = (int)hist[2047 - 2 * tid], c_lo = (int)hist[2046 - 2 * tid];
+    hist[2047 - 2 * tid] = 0u;
+    hist[2046 - 2 * tid] = 0u;
+    const int own = c_hi + c_lo;
+    const int incl_w = warp_incl_scan(own);
+    if (lane == 31) wsum[warp] = incl_w;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += wsum[w];
+    const int incl = before + incl_w, excl = incl - own;
+    if (excl < remaining && incl >= remaining) {
+      if (excl + c_hi >= remaining) {
+        found[0] = 2047 - 2 * tid;
+        found[1] = excl;
+        found[2] = c_hi;
+      } else {
+        found[0] = 2046 - 2 * tid;
+        found[1] = excl + c_hi;
+        found[2] = c_lo;
+      }
+    }
+    __syncthreads();
+    const int digit = found[0], above = found[1], in_bin = found[2];
+    prefix |= (uint32_t)digit << shift;
+    mask |= dmask << shift;
+    remaining -= above;
+    start = shift;
+    if (in_bin == remaining) inclusive = true;
+  }
+
+  // ---- compaction in position order: block scan of (above, equal) counts -----------------
+  const int need_eq = inclusive ? 0 : remaining;
+  int cg = 0, ce = 0;
+#pragma unroll
+  for (int q = 0; q < kSelPerThread; ++q) {
+    const int i = base + q;
+    if (i < n) {
+      const uint32_t kk = key[sel_slot(i)];
+      cg += (inclusive ? kk >= prefix : kk > prefix) ? 1 : 0;
+      ce += (!inclusive && kk == prefix) ? 1 : 0;
+    }
+  }
+  const int ig = warp_incl_scan(cg), ie = warp_incl_scan(ce);
+  if (lane == 31) {
+    wsum[warp] = ig;
+    wsum2[warp] = ie;
+  }
+  __syncthreads();
+  int gb = ig - cg, eb = ie - ce, gtot = 0, etot = 0;
+  for (int w = 0; w < 32; ++w) {
+    const int x1 = wsum[w], x2 = wsum2[w];
+    if (w < warp) {
+      gb += x1;
+      eb += x2;
+    }
+    gtot += x1;
+    etot += x2;
+  }
+#pragma unroll
+  for (int q = 0; q < kSelPerThread; ++q) {
+    const int i = base + q;
+    if (i < n) {
+      const uint32_t kk = key[sel_slot(i)];
+      const bool gsel = inclusive ? kk >= prefix : kk > prefix;
+      const bool esel = !inclusive && kk == prefix;
+      if (gsel) {
+        const int pos = gb + min(eb, need_eq);
+        if (pos < want) kept[pos] = i;
+        ++gb;
+      } else if (esel) {
+        if (eb < need_eq && gb + eb < want) kept[gb + eb] = i;
+        ++eb;
+      }
+    }
+  }
+  if (gtot + min(etot, need_eq) != want && tid == 0) set_status(a.status, RKV_DEV_SELECT_FAILED);
+  for (int j = tid; j < W; j += kSelThreads) kept[want + j] = L - W + j;
+  if (g == 0 && tid == 0) a.out_len[u] = a.keep;
+}
+
+// ------------------------------------------------------------------------------------------
 // compaction gather: CTA = 64 kept rows of one (unit, KV head); each thread copies 16-byte
 // chunks of K and V rows
 // ------------------------------------------------------------------------------------------
@@ -687,7 +902,17 @@ cudaError_t launch_snapkv(const SnapArgs& a, cudaStream_t s) {
   sp.reverse = 1;
   e = a.rows_pad == 128 ? launch_pass<2, 1>(km, qm, sp, s) : launch_pass<2, 2>(km, qm, sp, s);
   if (e != cudaSuccess) return e;
-  select_kernel<<<units, 1024, 0, s>>>(a);
+  // the whole-unit shared-memory select applies when every unit fits and the pooling kernel is
+  // 2^k - 1 (the adaptive sizes 7 / 15 / 31 all are)
+  const bool pow2_kernel = a.kernel_size <= 0 || ((a.kernel_size + 1) & a.kernel_size) == 0;
+  if (a.max_len - a.window <= kSelMaxN && pow2_kernel) {
+    const size_t smem = select_fast_smem_bytes();
+    e = ensure_dyn_smem((const void*)select_fast_kernel, smem);
+    if (e != cudaSuccess) return e;
+    select_fast_kernel<<<units, kSelThreads, smem, s>>>(a);
+  } else {
+    select_kernel<<<units, 1024, 0, s>>>(a);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   gather_kernel<<<dim3((a.keep + 63) / 64, units), 256, 0, s>>>(a);

@@ -123,6 +123,18 @@ def test_snapkv_adaptive_kernel_and_long_prompt():
         _check_unit(x, u, 0, 4, 32, 0, 2048, *res, tag=f"u{u}")
 
 
+@pytest.mark.parametrize("kernel", [1, 5, 31, 0])
+def test_snapkv_select_paths(kernel):
+    # the whole-unit shared-memory select (at most 32768 scores, pooling kernel 2^k - 1) at its
+    # size limit (32800 - 32 = 32768 scores), on ragged lengths and with a kernel wider than the
+    # 32 positions a thread owns; kernel 5 takes the general select
+    rkv = _lib()
+    wl, x = _inputs(3, 1, 4, [32800, 12345, 9000], 32, seed=107, needles=8)
+    res = _run(rkv, x, 32, kernel, 2048)
+    for u in range(3):
+        _check_unit(x, u, 0, 4, 32, kernel, 2048, *res, tag=f"kernel {kernel} u{u}")
+
+
 def test_snapkv_multiple_waves():
     # 6 units of 64K tokens: K of all units exceeds one L2-sized wave, so several waves run
     rkv = _lib()
