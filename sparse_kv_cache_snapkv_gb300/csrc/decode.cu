@@ -557,58 +557,80 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
 // ==========================================================================================
 constexpr int kSumPages = 32;
 
+// CTA = (unit, 32 pages). Thread t takes the 16-byte channel chunk t % 16 of pages t / 16 and
+// t / 16 + 16: its 2 PG row loads are all issued before any is used. Per-page (min, max) go
+// through shared memory so that each channel row of Kmin / Kmax is written 8 pages (16 bytes)
+// at a time.
+template <int PG>
 __global__ void __launch_bounds__(256) summaries_kernel(SummaryArgs a) {
-  __shared__ __align__(16) __nv_bfloat162 smin[kSumPages][kHeadDim / 2 + 1];
-  __shared__ __align__(16) __nv_bfloat162 smax[kSumPages][kHeadDim / 2 + 1];
+  __shared__ __align__(16) uint4 smin[kSumPages][kHeadDim / 8];
+  __shared__ __align__(16) uint4 smax[kSumPages][kHeadDim / 8];
   const int ukv = blockIdx.x;
   const int u = ukv / a.n_kv;
   const int len = a.len[u];
-  const int p = a.page;
-  const int P = (len + p - 1) / p;
+  const int P = (len + PG - 1) / PG;
   if (len < 0 || len > a.cap || P > a.page_cap) {
     if (threadIdx.x == 0 && blockIdx.y == 0) set_status(a.status, RKV_DEV_LEN_OVER_CAP);
     return;
   }
   const int pg0 = blockIdx.y * kSumPages;
-  const int first_page = a.first_token / p;
+  const int first_page = a.first_token / PG;
   if (pg0 >= P || pg0 + kSumPages <= first_page) return;
-  const int cp = threadIdx.x & 63, sub = threadIdx.x >> 6;
-  const __nv_bfloat162* kc =
-      reinterpret_cast<const __nv_bfloat162*>(a.k_cache + (size_t)ukv * a.cap * kHeadDim);
-  for (int j = sub; j < kSumPages; j += 4) {
-    const int pg = pg0 + j;
-    if (pg >= P) break;
-    const int t0 = pg * p, t1 = min(len, t0 + p);
-    __nv_bfloat162 mn = kc[(size_t)t0 * (kHeadDim / 2) + cp], mx = mn;
-    for (int t = t0 + 1; t < t1; ++t) {
-      const __nv_bfloat162 x = kc[(size_t)t * (kHeadDim / 2) + cp];
-      mn = __hmin2(mn, x);
-      mx = __hmax2(mx, x);
+  const int c = threadIdx.x & 15, pl = threadIdx.x >> 4;
+  const uint4* kc = reinterpret_cast<const uint4*>(a.k_cache + (size_t)ukv * a.cap * kHeadDim);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = pl + 16 * h;
+    const int t0 = (pg0 + j) * PG;
+    const int nt = min(PG, len - t0);  // rows of this page (<= 0: past the end)
+    if (nt > 0) {
+      const __nv_bfloat162 pinf = __halves2bfloat162(__ushort_as_bfloat16(0x7F80),
+                                                     __ushort_as_bfloat16(0x7F80));
+      const __nv_bfloat162 ninf = __halves2bfloat162(__ushort_as_bfloat16(0xFF80),
+                                                     __ushort_as_bfloat16(0xFF80));
+      __nv_bfloat162 mn[4] = {pinf, pinf, pinf, pinf}, mx[4] = {ninf, ninf, ninf, ninf};
+      constexpr int kB = PG < 8 ? PG : 8;  // rows in flight per batch
+#pragma unroll
+      for (int r0 = 0; r0 < PG; r0 += kB) {
+        uint4 x[kB];
+#pragma unroll
+        for (int b = 0; b < kB; ++b)
+          if (r0 + b < nt) x[b] = kc[(size_t)(t0 + r0 + b) * (kHeadDim / 8) + c];
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+          if (r0 + b < nt) {
+            const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&x[b]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              mn[e] = __hmin2(mn[e], y[e]);
+              mx[e] = __hmax2(mx[e], y[e]);
+            }
+          }
+        }
+      }
+      smin[j][c] = *reinterpret_cast<const uint4*>(mn);
+      smax[j][c] = *reinterpret_cast<const uint4*>(mx);
     }
-    smin[j][cp] = mn;
-    smax[j][cp] = mx;
   }
   __syncthreads();
-  // write: thread -> (channel c, 8-page group), pages [pg0, pg0 + 32) of channel row c
+  // write: thread -> (channel ch, 8-page group), pages [pg0, pg0 + 32) of channel row ch
   const int npg = min(kSumPages, P - pg0);
+  const int first_j = max(0, first_page - pg0);
+  const uint16_t* smin16 = reinterpret_cast<const uint16_t*>(&smin[0][0]);
+  const uint16_t* smax16 = reinterpret_cast<const uint16_t*>(&smax[0][0]);
+  uint16_t* kmin16 = reinterpret_cast<uint16_t*>(a.kmin);
+  uint16_t* kmax16 = reinterpret_cast<uint16_t*>(a.kmax);
   for (int i = threadIdx.x; i < kHeadDim * (kSumPages / 8); i += blockDim.x) {
-    const int c = i >> 2, grp = i & 3;
-    const int j0 = grp * 8;
+    const int ch = i >> 2, j0 = (i & 3) * 8;
     if (j0 >= npg) continue;
-    const size_t row = ((size_t)ukv * kHeadDim + c) * a.page_cap + pg0 + j0;
-    const int half = c & 1, cpair = c >> 1;
-    const int first_j = max(0, first_page - pg0);
+    const size_t row = ((size_t)ukv * kHeadDim + ch) * a.page_cap + pg0 + j0;
     uint16_t vmin[8], vmax[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
       const int j = min(j0 + t, npg - 1);
-      const __nv_bfloat162 a2 = smin[j][cpair], b2 = smax[j][cpair];
-      const bf16 x = half ? a2.y : a2.x, y = half ? b2.y : b2.x;
-      vmin[t] = *reinterpret_cast<const uint16_t*>(&x);
-      vmax[t] = *reinterpret_cast<const uint16_t*>(&y);
+      vmin[t] = smin16[j * kHeadDim + ch];
+      vmax[t] = smax16[j * kHeadDim + ch];
     }
-    uint16_t* kmin16 = reinterpret_cast<uint16_t*>(a.kmin);
-    uint16_t* kmax16 = reinterpret_cast<uint16_t*>(a.kmax);
     if (j0 + 8 <= npg && j0 >= first_j) {
       uint4 wmin, wmax;
       wmin.x = vmin[0] | ((uint32_t)vmin[1] << 16);
@@ -636,7 +658,22 @@ __global__ void __launch_bounds__(256) summaries_kernel(SummaryArgs a) {
 
 cudaError_t launch_summaries(const SummaryArgs& a, cudaStream_t s) {
   const dim3 grid(a.n * a.n_kv, (a.page_cap + kSumPages - 1) / kSumPages);
-  summaries_kernel<<<grid, 256, 0, s>>>(a);
+  switch (a.page) {
+#define RKV_SUM(PGV)                                    \
+  case PGV:                                             \
+    summaries_kernel<PGV><<<grid, 256, 0, s>>>(a);      \
+    break;
+    RKV_SUM(1)
+    RKV_SUM(2)
+    RKV_SUM(4)
+    RKV_SUM(8)
+    RKV_SUM(16)
+    RKV_SUM(32)
+    RKV_SUM(64)
+#undef RKV_SUM
+    default:
+      return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
