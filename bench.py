@@ -168,12 +168,13 @@ def _oracle_unit(args):
     return t1 - t0, (t2 - t1) / max(1, steps)
 
 
-def oracle_sample(wl, keep, kernel, units, cores, decode_sample, seed, pool):
-    """Time the oracle on `cores` units in parallel (one per core) and extrapolate a full step:
-    T = ceil(units / cores) * (t_compress + decode_steps * t_decode)."""
+def oracle_sample(wl, keep, kernel, units, cores, decode_sample, seed, pool, per_core=1):
+    """Time the oracle on `per_core` units per core in parallel (one worker per core) and
+    extrapolate a full step: T = ceil(units / cores) * (t_compress + decode_steps * t_decode)."""
     kernel = kernel or (7 if wl.max_len <= 8192 else 15 if wl.max_len <= 32768 else 31)
+    n_units = min(units, cores * per_core)
     args = [(wl.name, i, seed, keep, kernel, wl.budget, wl.page, wl.channels, decode_sample)
-            for i in range(cores)]
+            for i in range(n_units)]
     t0 = time.perf_counter()
     res = pool.map(_oracle_unit, args, chunksize=1)
     wall = time.perf_counter() - t0
@@ -353,14 +354,17 @@ def run_ours(args):
     cpu = None
     if pool is not None:
         oracle_sample(wl, hp.keep, wl.kernel, wl.n * wl.n_kv, cores, 1, args.seed, pool)
-        full_s, wall, tc, td = oracle_sample(wl, hp.keep, wl.kernel, wl.n * wl.n_kv, cores, 16,
-                                             args.seed, pool)
+        per_core = 6
+        full_s, wall, tc, td = oracle_sample(wl, hp.keep, wl.kernel, wl.n * wl.n_kv, cores,
+                                             wl.decode_steps, args.seed, pool, per_core)
         pool.close()
+        n_s = min(wl.n * wl.n_kv, cores * per_core)
         cpu = {"value": round(wl.decode_steps / full_s, 4), "unit": UNIT, "cores": cores,
                "kind": "oracle",
-               "sample": (f"{cores} (layer, KV head) units of the same workload, one per core, "
-                          f"each: compression + summaries + 16 decode steps; per-unit mean "
-                          f"{tc:.3f} s compress, {td * 1e3:.2f} ms per decode step; "
+               "sample": (f"{n_s} (layer, KV head) units of the same workload, {per_core} per "
+                          f"core, each: compression + summaries + {wl.decode_steps} decode steps "
+                          f"(~{n_s * (tc + wl.decode_steps * td):.1f} s of CPU work); per-unit "
+                          f"mean {tc:.3f} s compress, {td * 1e3:.2f} ms per decode step; "
                           f"extrapolated to {wl.n * wl.n_kv} units x {wl.decode_steps} steps"),
                "sample_wall_s": round(wall, 2)}
 
