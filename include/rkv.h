@@ -13,6 +13,8 @@
  *   [KSIZE] "Potential Sensitivity to Kernel Size in SnapKV++" -- adaptive pooling size
  *   [STEP]  "Are Different KV Tokens Retrieved at Each Decoding Step?" -- selection per step
  *   [SNAP++]"Novelty of SnapKV++"                          -- GQA-aware SnapKV scoring
+ *   [MT]    "SCBench Results"                              -- RocketKV-MT: nothing evicted, the
+ *                                                             decode selects among kept tokens
  * and [KEYPTS] = "Key points" of the summarizepaper.com summary (full-KV baseline, SnapKV++).
  *
  * Conventions shared by every call
@@ -59,6 +61,7 @@ typedef enum {
 #define RKV_DEV_BAD_WINDOW     0x2u  /* a sequence shorter than the window (unit skipped)     */
 #define RKV_DEV_WAIT_TIMEOUT   0x4u  /* a bounded mbarrier wait ran out (unit abandoned)      */
 #define RKV_DEV_SELECT_FAILED  0x8u  /* a top-k selection produced the wrong count            */
+#define RKV_DEV_BAD_INDEX      0x10u /* a kept index outside the valid rows (row 0 read)      */
 
 /* Human-readable name of a status code (static string). */
 const char* rkv_status_string(rkv_status s);
@@ -161,6 +164,54 @@ rkv_status rkv_hybrid_decode(const void* q, const void* new_k, const void* new_v
                              int budget, int page, int channels, float scale, void* out,
                              int32_t* sel_channels, int32_t* sel_pages, float* approx_scores,
                              void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------------ */
+/* RocketKV-MT: the full cache stays, the decode is restricted to the kept tokens ([MT])        */
+/* ------------------------------------------------------------------------------------------ */
+/* The multi-turn variant evicts nothing: every prompt token stays in the cache (the next turn
+ * re-filters the whole history), and the decode selects only among the tokens SnapKV++ kept.
+ * Here the kept tokens are named by an index list instead of being copied. For unit u and KV head
+ * g the kept sequence is kept_idx[u][g][j], j = 0 .. kept_len[u]-1: rows of the full cache, in
+ * the order the decode treats as token order (rkv_snapkv_compress writes such a list). Both calls
+ * compute exactly what rkv_build_page_summaries / rkv_hybrid_decode compute on the compact cache
+ * whose row j is k_full[u][g][kept_idx[u][g][j]] (same values, same order, same results); page
+ * numbers (sel_pages, approx_scores, kmin / kmax columns) count pages of the kept sequence.
+ *
+ * Page summaries of the kept sequence:
+ *   k_full [n][n_kv][full_cap][128] bf16; kept_idx [n][n_kv][kcap] int32; kept_len [n] int32
+ *   kmin, kmax [n][n_kv][128][page_cap] bf16; page, page_cap, first_token as for
+ *   rkv_build_page_summaries, with kept_len[u] <= kcap and <= page_cap * page (else
+ *   RKV_DEV_LEN_OVER_CAP, unit skipped). A kept index outside [0, full_cap) sets
+ *   RKV_DEV_BAD_INDEX and row 0 is read in its place. Workspace: rkv_summaries_workspace_bytes.
+ */
+rkv_status rkv_build_page_summaries_mt(const void* k_full, const int32_t* kept_idx,
+                                       const int32_t* kept_len, int n, int n_kv, int head_dim,
+                                       int full_cap, int kcap, int page, int page_cap,
+                                       int first_token, void* kmin, void* kmax, void* ws,
+                                       size_t ws_bytes, void* stream);
+
+/* One decode step over the kept sequence. If new_k / new_v are given, each unit's new token is
+ * first written to row full_len[u] of every KV head of the full cache, appended to the kept list
+ * (kept_idx[u][g][kept_len[u]] = full_len[u]) and folded into the page summary it lands in; then
+ * full_len[u] and kept_len[u] are incremented (RKV_DEV_LEN_OVER_CAP if full_len[u] = full_cap or
+ * kept_len[u] = kcap: nothing appended). The rest is rkv_hybrid_decode on the kept sequence:
+ * the dense path when kept_len[u] <= budget, else channel pick, page scores, page top-k and exact
+ * attention over the selected pages' kept tokens. A kept index outside [0, full_len[u]) sets
+ * RKV_DEV_BAD_INDEX and row 0 is read in its place.
+ *   q, out [n][n_kv*gqa][128] bf16; new_k, new_v NULL or [n][n_kv][128] bf16
+ *   k_full, v_full [n][n_kv][full_cap][128] bf16; full_len [n] int32
+ *   kept_idx [n][n_kv][kcap] int32; kept_len [n] int32
+ *   kmin, kmax, budget, page, page_cap, channels, gqa, sel_channels, sel_pages, approx_scores:
+ *   as for rkv_hybrid_decode (pages of the kept sequence). Workspace:
+ *   rkv_hybrid_decode_workspace_bytes.
+ */
+rkv_status rkv_hybrid_decode_mt(const void* q, const void* new_k, const void* new_v,
+                                void* k_full, void* v_full, int32_t* full_len, int32_t* kept_idx,
+                                int32_t* kept_len, void* kmin, void* kmax, int n, int n_kv,
+                                int gqa, int head_dim, int full_cap, int kcap, int page_cap,
+                                int budget, int page, int channels, float scale, void* out,
+                                int32_t* sel_channels, int32_t* sel_pages, float* approx_scores,
+                                void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------------ */
 /* Full-KV decode attention, the baseline the method is compared against ([KEYPTS])            */

@@ -39,6 +39,11 @@ Readings taken where the pages leave a step open (each restated at its function)
   R11 the summary of a partial last page is over its valid tokens only.
   R12 decode appends (when given) happen before attending; the new token is selectable.
   R13 attention scale as given (1/sqrt(d) by default); output kept in float64.
+  R14 RocketKV-MT ([P3] "SCBench Results"): nothing is evicted; the decode runs the stage-2 steps
+      on the sequence of kept tokens (stage 1's kept positions in its order, then the tokens
+      generated since), whose rows stay in the full cache. The pages do not say where generated
+      tokens go; they are appended to the full cache and to the kept sequence, and are selectable
+      (as in R12).
 """
 from __future__ import annotations
 
@@ -50,6 +55,7 @@ __all__ = [
     "plan", "adaptive_kernel_size", "window_scores", "pool_max", "topk_desc",
     "snapkv_compress", "page_summaries", "channel_pick", "approx_scores", "page_select",
     "attention", "dense_decode", "hybrid_decode", "group_topk_attention", "append_token",
+    "kept_view", "mt_page_summaries", "mt_hybrid_decode", "mt_append_token",
 ]
 
 
@@ -292,6 +298,58 @@ def append_token(kc: np.ndarray, vc: np.ndarray, length: int, kmin: np.ndarray,
         kmin[:, pg] = np.minimum(kmin[:, pg], new_k)
         kmax[:, pg] = np.maximum(kmax[:, pg], new_k)
     return length + 1
+
+
+# --------------------------------------------------------------------------------------------
+# RocketKV-MT: the full cache is kept, the decode sees only the kept tokens (reading R14)
+# --------------------------------------------------------------------------------------------
+def kept_view(full: np.ndarray, kept: np.ndarray, n_kept: int) -> np.ndarray:
+    """Rows of the kept sequence: full[kept[j]] for j < n_kept, in kept-list order.
+
+    [P3] "SCBench Results": in RocketKV-MT all input tokens stay in memory and the hybrid
+    attention selects only among the tokens SnapKV++ identified as important.
+    """
+    return full[np.asarray(kept[:n_kept], dtype=np.int64)]
+
+
+def mt_page_summaries(k_full: np.ndarray, kept: np.ndarray, n_kept: int, page: int):
+    """Kmin / Kmax over pages of the kept sequence (R14, then R11)."""
+    return page_summaries(kept_view(k_full, kept, n_kept), n_kept, page)
+
+
+def mt_hybrid_decode(q: np.ndarray, k_full: np.ndarray, v_full: np.ndarray, kept: np.ndarray,
+                     n_kept: int, kmin: np.ndarray, kmax: np.ndarray, budget: int, page: int,
+                     channels: int, scale: float):
+    """One RocketKV-MT decode step: `hybrid_decode` on the kept sequence (R14).
+
+    Pages and token ids in the result count positions of the kept sequence; "rows" gives the
+    attended rows of the full cache.
+    """
+    kc = kept_view(k_full, kept, n_kept)
+    vc = kept_view(v_full, kept, n_kept)
+    r = hybrid_decode(q, kc, vc, n_kept, kmin, kmax, budget, page, channels, scale)
+    r["rows"] = np.asarray(kept[:n_kept], dtype=np.int64)[r["tokens"]]
+    return r
+
+
+def mt_append_token(k_full: np.ndarray, v_full: np.ndarray, full_len: int, kept: np.ndarray,
+                    n_kept: int, kmin: np.ndarray, kmax: np.ndarray, new_k: np.ndarray,
+                    new_v: np.ndarray, page: int):
+    """Append one generated token in RocketKV-MT (R14): it takes row full_len of the full cache
+    and position n_kept of the kept sequence, whose page summary absorbs it as in
+    `append_token`. Arrays are modified in place; returns (full_len + 1, n_kept + 1).
+    """
+    k_full[full_len] = new_k
+    v_full[full_len] = new_v
+    kept[n_kept] = full_len
+    pg = n_kept // page
+    if n_kept % page == 0:
+        kmin[:, pg] = new_k
+        kmax[:, pg] = new_k
+    else:
+        kmin[:, pg] = np.minimum(kmin[:, pg], new_k)
+        kmax[:, pg] = np.maximum(kmax[:, pg], new_k)
+    return full_len + 1, n_kept + 1
 
 
 def default_scale(head_dim: int) -> float:

@@ -163,30 +163,51 @@ rkv_status rkv_snapkv_compress(const void* k, const void* v, const int32_t* seq_
 // ------------------------------------------------------------------------------- summaries
 size_t rkv_summaries_workspace_bytes(void) { return kStatusBytes; }
 
-rkv_status rkv_build_page_summaries(const void* k_cache, const int32_t* len, int n, int n_kv,
-                                    int head_dim, int cap, int page, int page_cap,
-                                    int first_token, void* kmin, void* kmax, void* ws,
-                                    size_t ws_bytes, void* stream) {
+// Summaries of the cache (kept == nullptr) or of the kept sequence of the full cache.
+static rkv_status summaries_impl(const void* k_cache, const int32_t* len, const int32_t* kept,
+                                 int n, int n_kv, int head_dim, int cap, int vcap, int page,
+                                 int page_cap, int first_token, void* kmin, void* kmax, void* ws,
+                                 size_t ws_bytes, void* stream) {
   if (head_dim != kHeadDim) return RKV_ERR_UNSUPPORTED;
   if (!k_cache || !len || !kmin || !kmax) return RKV_ERR_INVALID_ARG;
   if (!aligned16(k_cache) || !aligned16(kmin) || !aligned16(kmax)) return RKV_ERR_INVALID_ARG;
-  if (n <= 0 || n_kv <= 0 || cap <= 0 || !pow2(page) || page > 64 || page_cap <= 0 ||
-      page_cap % 8 != 0 || first_token < 0)
+  if (n <= 0 || n_kv <= 0 || cap <= 0 || vcap <= 0 || !pow2(page) || page > 64 ||
+      page_cap <= 0 || page_cap % 8 != 0 || first_token < 0)
     return RKV_ERR_INVALID_ARG;
   if (!ws || !aligned16(ws) || ws_bytes < kStatusBytes) return RKV_ERR_WORKSPACE;
   SummaryArgs a{};
   a.k_cache = static_cast<const bf16*>(k_cache);
   a.len = len;
+  a.kept = kept;
   a.kmin = static_cast<bf16*>(kmin);
   a.kmax = static_cast<bf16*>(kmax);
   a.n = n;
   a.n_kv = n_kv;
   a.cap = cap;
+  a.vcap = vcap;
   a.page = page;
   a.page_cap = page_cap;
   a.first_token = first_token;
   a.status = status_ptr(ws);
   return from_cuda(launch_summaries(a, as_stream(stream)));
+}
+
+rkv_status rkv_build_page_summaries(const void* k_cache, const int32_t* len, int n, int n_kv,
+                                    int head_dim, int cap, int page, int page_cap,
+                                    int first_token, void* kmin, void* kmax, void* ws,
+                                    size_t ws_bytes, void* stream) {
+  return summaries_impl(k_cache, len, nullptr, n, n_kv, head_dim, cap, cap, page, page_cap,
+                        first_token, kmin, kmax, ws, ws_bytes, stream);
+}
+
+rkv_status rkv_build_page_summaries_mt(const void* k_full, const int32_t* kept_idx,
+                                       const int32_t* kept_len, int n, int n_kv, int head_dim,
+                                       int full_cap, int kcap, int page, int page_cap,
+                                       int first_token, void* kmin, void* kmax, void* ws,
+                                       size_t ws_bytes, void* stream) {
+  if (!kept_idx) return RKV_ERR_INVALID_ARG;
+  return summaries_impl(k_full, kept_len, kept_idx, n, n_kv, head_dim, full_cap, kcap, page,
+                        page_cap, first_token, kmin, kmax, ws, ws_bytes, stream);
 }
 
 // ------------------------------------------------------------------------------- hybrid
@@ -201,12 +222,14 @@ size_t rkv_hybrid_decode_workspace_bytes(int n, int n_kv, int gqa, int page_cap,
   return kStatusBytes;
 }
 
-rkv_status rkv_hybrid_decode(const void* q, const void* new_k, const void* new_v,
-                             void* k_cache, void* v_cache, int32_t* len, void* kmin, void* kmax,
-                             int n, int n_kv, int gqa, int head_dim, int cap, int page_cap,
-                             int budget, int page, int channels, float scale, void* out,
-                             int32_t* sel_channels, int32_t* sel_pages, float* approx_scores,
-                             void* ws, size_t ws_bytes, void* stream) {
+// One decode step over the cache (kept == nullptr) or over the kept sequence of the full cache.
+static rkv_status hybrid_impl(const void* q, const void* new_k, const void* new_v,
+                              void* k_cache, void* v_cache, int32_t* len, int32_t* kept,
+                              int32_t* full_len, void* kmin, void* kmax, int n, int n_kv,
+                              int gqa, int head_dim, int cap, int vcap, int page_cap, int budget,
+                              int page, int channels, float scale, void* out,
+                              int32_t* sel_channels, int32_t* sel_pages, float* approx_scores,
+                              void* ws, size_t ws_bytes, void* stream) {
   if (head_dim != kHeadDim) return RKV_ERR_UNSUPPORTED;
   if (!gqa_ok(gqa)) return RKV_ERR_UNSUPPORTED;
   if (!q || !k_cache || !v_cache || !len || !kmin || !kmax || !out) return RKV_ERR_INVALID_ARG;
@@ -214,9 +237,9 @@ rkv_status rkv_hybrid_decode(const void* q, const void* new_k, const void* new_v
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(kmin) ||
       !aligned16(kmax) || !aligned16(out))
     return RKV_ERR_INVALID_ARG;
-  if (n <= 0 || n_kv <= 0 || cap <= 0 || page_cap <= 0 || page_cap % 8 != 0 || !pow2(page) ||
-      page > 64 || budget <= 0 || budget % 2 != 0 || budget / 2 < page || channels < 1 ||
-      channels > kHeadDim || !(scale > 0.f) || !std::isfinite(scale))
+  if (n <= 0 || n_kv <= 0 || cap <= 0 || vcap <= 0 || page_cap <= 0 || page_cap % 8 != 0 ||
+      !pow2(page) || page > 64 || budget <= 0 || budget % 2 != 0 || budget / 2 < page ||
+      channels < 1 || channels > kHeadDim || !(scale > 0.f) || !std::isfinite(scale))
     return RKV_ERR_INVALID_ARG;
   const size_t smem = hybrid_smem_bytes(gqa, page_cap, budget, page);
   if (smem > 200 * 1024) return RKV_ERR_UNSUPPORTED;
@@ -233,26 +256,32 @@ rkv_status rkv_hybrid_decode(const void* q, const void* new_k, const void* new_v
     ap.len = len;
     ap.kmin = static_cast<bf16*>(kmin);
     ap.kmax = static_cast<bf16*>(kmax);
+    ap.kept = kept;
+    ap.full_len = full_len;
     ap.n = n;
     ap.n_kv = n_kv;
     ap.cap = cap;
+    ap.vcap = vcap;
     ap.page_cap = page_cap;
     ap.page = page;
     ap.status = status_ptr(ws);
     cudaError_t e = launch_append(ap, s);
     if (e != cudaSuccess) return RKV_ERR_CUDA;
   }
-  HybridArgs a{};
+  HybridArgsMT a{};
   a.q = static_cast<const bf16*>(q);
   a.k_cache = static_cast<const bf16*>(k_cache);
   a.v_cache = static_cast<const bf16*>(v_cache);
   a.len = len;
   a.kmin = static_cast<const bf16*>(kmin);
   a.kmax = static_cast<const bf16*>(kmax);
+  a.kept = kept;
+  a.full_len = full_len;
   a.n = n;
   a.n_kv = n_kv;
   a.gqa = gqa;
   a.cap = cap;
+  a.vcap = vcap;
   a.page_cap = page_cap;
   a.budget = budget;
   a.page = page;
@@ -264,6 +293,30 @@ rkv_status rkv_hybrid_decode(const void* q, const void* new_k, const void* new_v
   a.approx = approx_scores;
   a.status = status_ptr(ws);
   return from_cuda(launch_hybrid(a, s));
+}
+
+rkv_status rkv_hybrid_decode(const void* q, const void* new_k, const void* new_v,
+                             void* k_cache, void* v_cache, int32_t* len, void* kmin, void* kmax,
+                             int n, int n_kv, int gqa, int head_dim, int cap, int page_cap,
+                             int budget, int page, int channels, float scale, void* out,
+                             int32_t* sel_channels, int32_t* sel_pages, float* approx_scores,
+                             void* ws, size_t ws_bytes, void* stream) {
+  return hybrid_impl(q, new_k, new_v, k_cache, v_cache, len, nullptr, nullptr, kmin, kmax, n,
+                     n_kv, gqa, head_dim, cap, cap, page_cap, budget, page, channels, scale, out,
+                     sel_channels, sel_pages, approx_scores, ws, ws_bytes, stream);
+}
+
+rkv_status rkv_hybrid_decode_mt(const void* q, const void* new_k, const void* new_v,
+                                void* k_full, void* v_full, int32_t* full_len, int32_t* kept_idx,
+                                int32_t* kept_len, void* kmin, void* kmax, int n, int n_kv,
+                                int gqa, int head_dim, int full_cap, int kcap, int page_cap,
+                                int budget, int page, int channels, float scale, void* out,
+                                int32_t* sel_channels, int32_t* sel_pages, float* approx_scores,
+                                void* ws, size_t ws_bytes, void* stream) {
+  if (!kept_idx || !full_len) return RKV_ERR_INVALID_ARG;
+  return hybrid_impl(q, new_k, new_v, k_full, v_full, kept_len, kept_idx, full_len, kmin, kmax,
+                     n, n_kv, gqa, head_dim, full_cap, kcap, page_cap, budget, page, channels,
+                     scale, out, sel_channels, sel_pages, approx_scores, ws, ws_bytes, stream);
 }
 
 // ------------------------------------------------------------------------------- dense

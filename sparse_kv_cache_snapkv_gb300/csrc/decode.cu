@@ -246,8 +246,10 @@ size_t hybrid_smem_bytes(int gqa, int page_cap, int budget, int page) {
   return b;
 }
 
-template <int G>
-__global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(HybridArgs a) {
+// MT: the sequence is the kept list of the full cache (A = HybridArgsMT), else the cache itself
+// (A = HybridArgs, whose smaller parameter block keeps the plain launch cheaper).
+template <int G, bool MT, typename A>
+__global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(A a) {
   extern __shared__ __align__(1024) unsigned char smem[];
   __shared__ float qs[G * kHeadDim];
   __shared__ __align__(16) uint32_t umag[kHeadDim];
@@ -276,12 +278,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
   uint4 qraw = make_uint4(0u, 0u, 0u, 0u);
   if (tid < G * 16) qraw = *reinterpret_cast<const uint4*>(qgroup + tid * 8);
   const int len = a.len[u];
+  int flen = a.cap;  // rows a kept index may name
+  int vcap = a.cap;  // bound of len
+  if constexpr (MT) {
+    flen = a.full_len[u];
+    vcap = a.vcap;
+  }
   const int p = a.page;
   const int P = (len + p - 1) / p;
   const int S = (a.budget / 2) / p;
   const bool dense = len <= a.budget;
 
-  if (len <= 0 || len > a.cap || P > a.page_cap) {
+  if (len <= 0 || len > vcap || P > a.page_cap) {
     if (tid == 0 && len != 0) set_status(a.status, RKV_DEV_LEN_OVER_CAP);
     return;
   }
@@ -428,10 +436,28 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(Hybrid
     const int half = (lane >> 4) & 1, c16 = lane & 15;
     const bf16* cache = half ? a.v_cache : a.k_cache;
     bf16* dst = (half ? Vw : Kw) + c16 * 8;
-    for (int r = 0; r < nt; ++r) {
-      const int v = v0 + r;
-      const size_t tok = ((size_t)sel[v >> lp] << lp) + (v & (p - 1));
-      cp_async16(dst + r * kRowPad, cache + (cache_base + tok) * kHeadDim + c16 * 8);
+    if constexpr (MT) {
+      // lane r fetches the cache row of the unit's token r from the kept list, checked
+      int krow = 0;
+      if (lane < nt) {
+        const int v = v0 + lane;
+        const int t = (sel[v >> lp] << lp) + (v & (p - 1));
+        krow = a.kept[(size_t)ukv * vcap + t];
+        if (krow < 0 || krow >= flen) {
+          set_status(a.status, RKV_DEV_BAD_INDEX);
+          krow = 0;
+        }
+      }
+      for (int r = 0; r < nt; ++r) {
+        const size_t tok = (size_t)__shfl_sync(0xffffffffu, krow, r);
+        cp_async16(dst + r * kRowPad, cache + (cache_base + tok) * kHeadDim + c16 * 8);
+      }
+    } else {
+      for (int r = 0; r < nt; ++r) {
+        const int v = v0 + r;
+        const size_t tok = ((size_t)sel[v >> lp] << lp) + (v & (p - 1));
+        cp_async16(dst + r * kRowPad, cache + (cache_base + tok) * kHeadDim + c16 * 8);
+      }
     }
     cp_async_commit();
     // V rows past the unit's tokens meet P = 0: make them zero, not stale bits (0 * NaN)
@@ -487,16 +513,25 @@ static cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-cudaError_t launch_hybrid(const HybridArgs& a, cudaStream_t s) {
+cudaError_t launch_hybrid(const HybridArgsMT& a, cudaStream_t s) {
+  const HybridArgs& plain = a;
   const size_t smem = hybrid_smem_bytes(a.gqa, a.page_cap, a.budget, a.page);
   const dim3 grid(a.n * a.n_kv), block(kDecodeThreads);
   cudaError_t e = cudaSuccess;
   switch (a.gqa) {
 #define RKV_CASE(GG)                                                                         \
   case GG:                                                                                   \
-    e = ensure_dyn_smem((const void*)hybrid_decode_kernel<GG>, smem);                        \
-    if (e != cudaSuccess) return e;                                                          \
-    e = launch_pdl(hybrid_decode_kernel<GG>, grid, block, smem, s, a);                       \
+    if (a.kept) {                                                                            \
+      auto* k = hybrid_decode_kernel<GG, true, HybridArgsMT>;                                \
+      e = ensure_dyn_smem((const void*)k, smem);                                             \
+      if (e != cudaSuccess) return e;                                                        \
+      e = launch_pdl(k, grid, block, smem, s, a);                                            \
+    } else {                                                                                 \
+      auto* k = hybrid_decode_kernel<GG, false, HybridArgs>;                                 \
+      e = ensure_dyn_smem((const void*)k, smem);                                             \
+      if (e != cudaSuccess) return e;                                                        \
+      e = launch_pdl(k, grid, block, smem, s, plain);                                        \
+    }                                                                                        \
     if (e != cudaSuccess) return e;                                                          \
     break;
     RKV_CASE(1)
@@ -512,19 +547,23 @@ cudaError_t launch_hybrid(const HybridArgs& a, cudaStream_t s) {
 
 // ==========================================================================================
 // Decode-token append: one CTA per unit writes the new row of every KV head and folds it into
-// the page summary it lands in, then bumps len[u].
+// the page summary it lands in, then bumps len[u]. With a kept list (RocketKV-MT) the row goes to
+// row full_len[u] of the full cache, its position is appended to the kept list, and both
+// counters advance.
 // ==========================================================================================
 __global__ void append_kernel(AppendArgs a) {
   const int u = blockIdx.x, c = threadIdx.x;  // 128 threads: one channel each
   const int len = a.len[u];
+  const int row = a.kept ? a.full_len[u] : len;  // cache row receiving the token
   const int pg = len / a.page;
-  const bool fits = len >= 0 && len < a.cap && pg < a.page_cap;
+  const bool fits = len >= 0 && len < a.vcap && pg < a.page_cap && row >= 0 && row < a.cap;
   if (fits) {
     for (int g = 0; g < a.n_kv; ++g) {
       const size_t ukv = (size_t)u * a.n_kv + g;
       const bf16 kval = a.new_k[ukv * kHeadDim + c];
-      a.k_cache[(ukv * a.cap + len) * kHeadDim + c] = kval;
-      a.v_cache[(ukv * a.cap + len) * kHeadDim + c] = a.new_v[ukv * kHeadDim + c];
+      a.k_cache[(ukv * a.cap + row) * kHeadDim + c] = kval;
+      a.v_cache[(ukv * a.cap + row) * kHeadDim + c] = a.new_v[ukv * kHeadDim + c];
+      if (a.kept && c == 0) a.kept[ukv * a.vcap + len] = row;
       const size_t si = (ukv * kHeadDim + c) * a.page_cap + pg;
       if (len % a.page == 0) {
         a.kmin[si] = kval;
@@ -538,10 +577,12 @@ __global__ void append_kernel(AppendArgs a) {
   }
   __syncthreads();
   if (c == 0) {
-    if (fits)
+    if (fits) {
       a.len[u] = len + 1;
-    else
+      if (a.kept) a.full_len[u] = row + 1;
+    } else {
       set_status(a.status, RKV_DEV_LEN_OVER_CAP);
+    }
   }
 }
 
@@ -569,7 +610,7 @@ __global__ void __launch_bounds__(256) summaries_kernel(SummaryArgs a) {
   const int u = ukv / a.n_kv;
   const int len = a.len[u];
   const int P = (len + PG - 1) / PG;
-  if (len < 0 || len > a.cap || P > a.page_cap) {
+  if (len < 0 || len > a.vcap || P > a.page_cap) {
     if (threadIdx.x == 0 && blockIdx.y == 0) set_status(a.status, RKV_DEV_LEN_OVER_CAP);
     return;
   }
@@ -578,6 +619,17 @@ __global__ void __launch_bounds__(256) summaries_kernel(SummaryArgs a) {
   if (pg0 >= P || pg0 + kSumPages <= first_page) return;
   const int c = threadIdx.x & 15, pl = threadIdx.x >> 4;
   const uint4* kc = reinterpret_cast<const uint4*>(a.k_cache + (size_t)ukv * a.cap * kHeadDim);
+  const int32_t* kept = a.kept ? a.kept + (size_t)ukv * a.vcap : nullptr;
+  // cache row of sequence token t: itself, or its kept index (checked; row 0 if out of range)
+  auto row_of = [&](int t) -> int {
+    if (!kept) return t;
+    const int r = kept[t];
+    if (r < 0 || r >= a.cap) {
+      set_status(a.status, RKV_DEV_BAD_INDEX);
+      return 0;
+    }
+    return r;
+  };
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int j = pl + 16 * h;
@@ -593,9 +645,12 @@ __global__ void __launch_bounds__(256) summaries_kernel(SummaryArgs a) {
 #pragma unroll
       for (int r0 = 0; r0 < PG; r0 += kB) {
         uint4 x[kB];
+        int rw[kB];
+#pragma unroll
+        for (int b = 0; b < kB; ++b) rw[b] = (r0 + b < nt) ? row_of(t0 + r0 + b) : 0;
 #pragma unroll
         for (int b = 0; b < kB; ++b)
-          if (r0 + b < nt) x[b] = kc[(size_t)(t0 + r0 + b) * (kHeadDim / 8) + c];
+          if (r0 + b < nt) x[b] = kc[(size_t)rw[b] * (kHeadDim / 8) + c];
 #pragma unroll
         for (int b = 0; b < kB; ++b) {
           if (r0 + b < nt) {

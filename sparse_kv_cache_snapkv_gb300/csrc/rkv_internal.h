@@ -19,6 +19,9 @@ typedef __nv_bfloat16 bf16;
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // ---------------------------------------------------------------------------- decode side
+// `len` counts the tokens of the sequence the decode sees; `cap` is the row capacity of k_cache.
+// The plain decode's parameters stay within 128 bytes: a larger parameter block was measured to
+// add 0.34 us to every launch, whatever the kernel reads.
 struct HybridArgs {
   const bf16* q;
   const bf16* k_cache;
@@ -34,7 +37,18 @@ struct HybridArgs {
   float* approx;
   uint32_t* status;
 };
+static_assert(sizeof(HybridArgs) <= 128, "plain-decode parameters must fit in 128 bytes");
 
+// RocketKV-MT: the sequence is kept[ukv][0 .. len-1], rows of the full cache (k_cache, cap rows,
+// valid below full_len[u]); vcap (the kept list's capacity) bounds len.
+struct HybridArgsMT : HybridArgs {
+  const int32_t* kept;
+  const int32_t* full_len;
+  int vcap;
+};
+
+// Appends token `len` of every unit. With `kept` set, the row goes to row full_len[u] of the
+// full cache and kept[ukv][len] = full_len[u]; both counters advance.
 struct AppendArgs {
   const bf16* new_k;
   const bf16* new_v;
@@ -43,16 +57,21 @@ struct AppendArgs {
   int32_t* len;
   bf16* kmin;
   bf16* kmax;
-  int n, n_kv, cap, page_cap, page;
+  int32_t* kept;
+  int32_t* full_len;
+  int n, n_kv, cap, vcap, page_cap, page;
   uint32_t* status;
 };
 
+// Summaries of the sequence of `len` tokens: cache rows, or with `kept` set the rows
+// kept[ukv][0 .. len-1] of the full cache (len <= vcap).
 struct SummaryArgs {
   const bf16* k_cache;
   const int32_t* len;
+  const int32_t* kept;
   bf16* kmin;
   bf16* kmax;
-  int n, n_kv, cap, page, page_cap, first_token;
+  int n, n_kv, cap, vcap, page, page_cap, first_token;
   uint32_t* status;
 };
 
@@ -79,7 +98,7 @@ void dense_plan(int n, int n_kv, int max_len, int* nsplit, int* tokens_per_split
 size_t dense_partials_bytes(int n, int n_kv, int gqa, int max_len);
 
 size_t hybrid_smem_bytes(int gqa, int page_cap, int budget, int page);
-cudaError_t launch_hybrid(const HybridArgs& a, cudaStream_t s);
+cudaError_t launch_hybrid(const HybridArgsMT& a, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_summaries(const SummaryArgs& a, cudaStream_t s);
 cudaError_t launch_dense(const DenseArgs& a, cudaStream_t s);

@@ -29,6 +29,7 @@ SYMBOLS = [
     "rkv_snapkv_compress", "rkv_summaries_workspace_bytes", "rkv_build_page_summaries",
     "rkv_hybrid_decode_workspace_bytes", "rkv_hybrid_decode",
     "rkv_dense_decode_workspace_bytes", "rkv_dense_decode", "rkv_dense_decode_noalloc",
+    "rkv_build_page_summaries_mt", "rkv_hybrid_decode_mt",
 ]
 
 
@@ -77,6 +78,11 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
                              i32),
         "rkv_dense_decode_noalloc": ([vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp],
                                      i32),
+        "rkv_build_page_summaries_mt": ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp,
+                                         vp, vp, sz, vp], i32),
+        "rkv_hybrid_decode_mt": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                  i32, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, sz, vp],
+                                 i32),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -205,6 +211,46 @@ def rkv_hybrid_decode(q, k_cache, v_cache, length, kmin, kmax, budget: int, page
         float(scale), _ptr(out), _ptr(sel_channels), _ptr(sel_pages), _ptr(approx_scores),
         _ptr(ws), ws.numel(), _stream(stream))
     _check("rkv_hybrid_decode", code)
+    return ws
+
+
+def rkv_build_page_summaries_mt(k_full, kept_idx, kept_len, page: int, kmin, kmax,
+                                first_token: int = 0, ws=None, stream=None):
+    """Page summaries of the kept sequence k_full[u][g][kept_idx[u][g][j]] (RocketKV-MT)."""
+    _bf16(k_full, "k_full"), _i32(kept_idx, "kept_idx"), _i32(kept_len, "kept_len")
+    n, n_kv, full_cap, d = k_full.shape
+    kcap = kept_idx.shape[-1]
+    page_cap = kmin.shape[-1]
+    if ws is None:
+        ws = workspace(STATUS_BYTES, k_full.device)
+    code = load().rkv_build_page_summaries_mt(
+        _ptr(k_full), _ptr(kept_idx), _ptr(kept_len), n, n_kv, d, full_cap, kcap, page, page_cap,
+        first_token, _ptr(kmin), _ptr(kmax), _ptr(ws), ws.numel(), _stream(stream))
+    _check("rkv_build_page_summaries_mt", code)
+    return ws
+
+
+def rkv_hybrid_decode_mt(q, k_full, v_full, full_len, kept_idx, kept_len, kmin, kmax,
+                         budget: int, page: int, channels: int, scale: float, out, new_k=None,
+                         new_v=None, sel_channels=None, sel_pages=None, approx_scores=None,
+                         ws=None, stream=None):
+    """One hybrid decode step over the kept sequence of the full cache (RocketKV-MT),
+    optionally appending new_k / new_v to the full cache and the kept list first."""
+    _bf16(q, "q"), _bf16(k_full, "k_full"), _i32(full_len, "full_len")
+    _i32(kept_idx, "kept_idx"), _i32(kept_len, "kept_len")
+    n, n_kv, full_cap, d = k_full.shape
+    gqa = q.shape[1] // n_kv
+    kcap = kept_idx.shape[-1]
+    page_cap = kmin.shape[-1]
+    if ws is None:
+        ws = workspace(rkv_hybrid_decode_workspace_bytes(n, n_kv, gqa, page_cap, budget, page),
+                       q.device)
+    code = load().rkv_hybrid_decode_mt(
+        _ptr(q), _ptr(new_k), _ptr(new_v), _ptr(k_full), _ptr(v_full), _ptr(full_len),
+        _ptr(kept_idx), _ptr(kept_len), _ptr(kmin), _ptr(kmax), n, n_kv, gqa, d, full_cap, kcap,
+        page_cap, budget, page, channels, float(scale), _ptr(out), _ptr(sel_channels),
+        _ptr(sel_pages), _ptr(approx_scores), _ptr(ws), ws.numel(), _stream(stream))
+    _check("rkv_hybrid_decode_mt", code)
     return ws
 
 

@@ -105,6 +105,37 @@ def test_validation_rejects_before_launch(lib):
                                    None) == 3
 
 
+
+def test_mt_validation_rejects_before_launch(lib):
+    vp = FAKE
+    # (q, new_k, new_v, k_full, v_full, full_len, kept_idx, kept_len, kmin, kmax)
+    ptrs = (vp, None, None, vp, vp, vp, vp, vp, vp, vp)
+    tail = (0.1, vp, None, None, None, vp, 256, None)
+    # n, n_kv, gqa, head_dim, full_cap, kcap, page_cap, budget, page, channels
+    ok = (1, 1, 4, 128, 4096, 64, 16, 256, 4, 32)
+    bad_cases = [
+        ((1, 1, 4, 64, 4096, 64, 16, 256, 4, 32), 2),    # head_dim
+        ((1, 1, 4, 128, 4096, 0, 16, 256, 4, 32), 1),    # kcap
+        ((1, 1, 4, 128, 0, 64, 16, 256, 4, 32), 1),      # full_cap
+        ((1, 1, 4, 128, 4096, 64, 12, 256, 4, 32), 1),   # page_cap % 8
+        ((1, 1, 4, 128, 4096, 64, 16, 256, 4, 0), 1),    # channels
+    ]
+    for sizes, code in bad_cases:
+        assert lib.rkv_hybrid_decode_mt(*ptrs, *sizes, *tail) == code, sizes
+    no_kept = (vp, None, None, vp, vp, vp, None, vp, vp, vp)
+    assert lib.rkv_hybrid_decode_mt(*no_kept, *ok, *tail) == 1
+    no_full_len = (vp, None, None, vp, vp, None, vp, vp, vp, vp)
+    assert lib.rkv_hybrid_decode_mt(*no_full_len, *ok, *tail) == 1
+    assert lib.rkv_hybrid_decode_mt(*ptrs, *ok, 0.1, vp, None, None, None, vp, 8, None) == 3
+    # summaries over a kept list: no list, bad page, small workspace
+    assert lib.rkv_build_page_summaries_mt(vp, None, vp, 1, 1, 128, 4096, 64, 4, 16, 0, vp, vp,
+                                           vp, 256, None) == 1
+    assert lib.rkv_build_page_summaries_mt(vp, vp, vp, 1, 1, 128, 4096, 64, 3, 16, 0, vp, vp,
+                                           vp, 256, None) == 1
+    assert lib.rkv_build_page_summaries_mt(vp, vp, vp, 1, 1, 128, 4096, 64, 4, 16, 0, vp, vp,
+                                           vp, 4, None) == 3
+
+
 def test_workspace_sizes_monotone(lib):
     a = lib.rkv_dense_decode_workspace_bytes(32, 8, 4, 32768)
     b = lib.rkv_dense_decode_workspace_bytes(32, 8, 4, 131072)

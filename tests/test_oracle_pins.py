@@ -342,3 +342,74 @@ def test_hybrid_token_count_is_half_budget():
     q2 = _bf16_values((4, d), rng)
     r2 = O.hybrid_decode(q2, kc, vc, L, kmin, kmax, budget=B, page=p, channels=8, scale=0.2)
     assert not np.array_equal(r["pages"], r2["pages"])
+
+
+# ---------------------------------------------------------------- RocketKV-MT (reading R14)
+def test_mt_identity_kept_list_is_plain_decode():
+    # keeping every token in order is RocketKV's decode on the full cache
+    rng = np.random.default_rng(17)
+    L, d, B, p = 700, 32, 128, 4
+    kf = _bf16_values((L, d), rng)
+    vf = _bf16_values((L, d), rng)
+    q = _bf16_values((4, d), rng)
+    kept = np.arange(L)
+    kmin, kmax = O.mt_page_summaries(kf, kept, L, p)
+    kmin0, kmax0 = O.page_summaries(kf, L, p)
+    assert np.array_equal(kmin, kmin0) and np.array_equal(kmax, kmax0)
+    r = O.mt_hybrid_decode(q, kf, vf, kept, L, kmin, kmax, B, p, 8, 0.2)
+    r0 = O.hybrid_decode(q, kf, vf, L, kmin0, kmax0, B, p, 8, 0.2)
+    assert np.array_equal(r["pages"], r0["pages"]) and np.array_equal(r["rows"], r0["tokens"])
+    np.testing.assert_array_equal(r["out"], r0["out"])
+
+
+def test_mt_evicted_rows_never_matter():
+    # "all KV tokens are kept in memory but [decode] only selects among the important tokens":
+    # rows outside the kept list may hold anything without changing the step
+    rng = np.random.default_rng(18)
+    L, d, B, p, n_kept = 2000, 32, 128, 4, 500
+    kf = _bf16_values((L, d), rng)
+    vf = _bf16_values((L, d), rng)
+    q = _bf16_values((4, d), rng)
+    kept = np.sort(rng.choice(L, n_kept, replace=False))
+    kmin, kmax = O.mt_page_summaries(kf, kept, n_kept, p)
+    r = O.mt_hybrid_decode(q, kf, vf, kept, n_kept, kmin, kmax, B, p, 8, 0.2)
+    assert set(r["rows"].tolist()) <= set(kept.tolist())
+    assert len(r["rows"]) == B // 2
+    others = np.setdiff1d(np.arange(L), kept)
+    kf2, vf2 = kf.copy(), vf.copy()
+    kf2[others] = 1e3 * _bf16_values((len(others), d), rng)
+    vf2[others] = -7.0
+    kmin2, kmax2 = O.mt_page_summaries(kf2, kept, n_kept, p)
+    r2 = O.mt_hybrid_decode(q, kf2, vf2, kept, n_kept, kmin2, kmax2, B, p, 8, 0.2)
+    assert np.array_equal(r["rows"], r2["rows"])
+    np.testing.assert_array_equal(r["out"], r2["out"])
+
+
+def test_mt_append_matches_rebuild():
+    # generated tokens go to the end of the full cache and of the kept sequence; the summaries
+    # kept incrementally equal those rebuilt from the final kept sequence
+    rng = np.random.default_rng(19)
+    L, d, p, n_kept, steps, cap = 600, 16, 4, 101, 9, 640
+    kf = np.zeros((cap, d))
+    vf = np.zeros((cap, d))
+    kf[:L] = _bf16_values((L, d), rng)
+    vf[:L] = _bf16_values((L, d), rng)
+    kept = np.full(n_kept + steps, -1)
+    kept[:n_kept] = np.sort(rng.choice(L, n_kept, replace=False))
+    P_cap = (n_kept + steps + p - 1) // p
+    kmin = np.zeros((d, P_cap))
+    kmax = np.zeros((d, P_cap))
+    a, b = O.mt_page_summaries(kf, kept, n_kept, p)
+    kmin[:, :a.shape[1]], kmax[:, :a.shape[1]] = a, b
+    full_len, nk = L, n_kept
+    new = []
+    for _ in range(steps):
+        nkv = _bf16_values((2, d), rng)
+        new.append(nkv)
+        full_len, nk = O.mt_append_token(kf, vf, full_len, kept, nk, kmin, kmax, nkv[0], nkv[1], p)
+    assert (full_len, nk) == (L + steps, n_kept + steps)
+    assert np.array_equal(kept[n_kept:], np.arange(L, L + steps))
+    assert np.array_equal(kf[L:L + steps], np.stack([x[0] for x in new]))
+    ra, rb = O.mt_page_summaries(kf, kept, nk, p)
+    P = (nk + p - 1) // p
+    assert np.array_equal(kmin[:, :P], ra) and np.array_equal(kmax[:, :P], rb)
