@@ -39,7 +39,8 @@ Readings taken where the pages leave a step open (each restated at its function)
   R11 the summary of a partial last page is over its valid tokens only.
   R12 decode appends (when given) happen before attending; the new token is selectable.
   R13 attention scale as given (1/sqrt(d) by default); output kept in float64.
-  R14 RocketKV-MT ([P3] "SCBench Results"): nothing is evicted; the decode runs the stage-2 steps
+  (R14-R16 concern the seeded synthetic inputs, not this module.)
+  R17 RocketKV-MT ([P3] "SCBench Results"): nothing is evicted; the decode runs the stage-2 steps
       on the sequence of kept tokens (stage 1's kept positions in its order, then the tokens
       generated since), whose rows stay in the full cache. The pages do not say where generated
       tokens go; they are appended to the full cache and to the kept sequence, and are selectable
@@ -301,7 +302,7 @@ def append_token(kc: np.ndarray, vc: np.ndarray, length: int, kmin: np.ndarray,
 
 
 # --------------------------------------------------------------------------------------------
-# RocketKV-MT: the full cache is kept, the decode sees only the kept tokens (reading R14)
+# RocketKV-MT: the full cache is kept, the decode sees only the kept tokens (reading R17)
 # --------------------------------------------------------------------------------------------
 def kept_view(full: np.ndarray, kept: np.ndarray, n_kept: int) -> np.ndarray:
     """Rows of the kept sequence: full[kept[j]] for j < n_kept, in kept-list order.
@@ -313,14 +314,14 @@ def kept_view(full: np.ndarray, kept: np.ndarray, n_kept: int) -> np.ndarray:
 
 
 def mt_page_summaries(k_full: np.ndarray, kept: np.ndarray, n_kept: int, page: int):
-    """Kmin / Kmax over pages of the kept sequence (R14, then R11)."""
+    """Kmin / Kmax over pages of the kept sequence (R17, then R11)."""
     return page_summaries(kept_view(k_full, kept, n_kept), n_kept, page)
 
 
 def mt_hybrid_decode(q: np.ndarray, k_full: np.ndarray, v_full: np.ndarray, kept: np.ndarray,
                      n_kept: int, kmin: np.ndarray, kmax: np.ndarray, budget: int, page: int,
                      channels: int, scale: float):
-    """One RocketKV-MT decode step: `hybrid_decode` on the kept sequence (R14).
+    """One RocketKV-MT decode step: `hybrid_decode` on the kept sequence (R17).
 
     Pages and token ids in the result count positions of the kept sequence; "rows" gives the
     attended rows of the full cache.
@@ -335,7 +336,7 @@ def mt_hybrid_decode(q: np.ndarray, k_full: np.ndarray, v_full: np.ndarray, kept
 def mt_append_token(k_full: np.ndarray, v_full: np.ndarray, full_len: int, kept: np.ndarray,
                     n_kept: int, kmin: np.ndarray, kmax: np.ndarray, new_k: np.ndarray,
                     new_v: np.ndarray, page: int):
-    """Append one generated token in RocketKV-MT (R14): it takes row full_len of the full cache
+    """Append one generated token in RocketKV-MT (R17): it takes row full_len of the full cache
     and position n_kept of the kept sequence, whose page summary absorbs it as in
     `append_token`. Arrays are modified in place; returns (full_len + 1, n_kept + 1).
     """

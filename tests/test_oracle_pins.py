@@ -344,7 +344,7 @@ def test_hybrid_token_count_is_half_budget():
     assert not np.array_equal(r["pages"], r2["pages"])
 
 
-# ---------------------------------------------------------------- RocketKV-MT (reading R14)
+# ---------------------------------------------------------------- RocketKV-MT (reading R17)
 def test_mt_identity_kept_list_is_plain_decode():
     # keeping every token in order is RocketKV's decode on the full cache
     rng = np.random.default_rng(17)
