@@ -81,6 +81,16 @@ rkv_status rkv_check_status(void* ws, void* stream, uint32_t* bits);
 rkv_status rkv_plan(int ctx, int budget, int head_dim, int page, int channels,
                     int* keep, int* page_out, int* channels_out, int* kernel_size);
 
+/* The even split of [PAGE] for any ratio: with R = ctx / budget, each stage gets sqrt(R), and
+ * stage 2's share is split evenly between the page size and the channel reduction, so that
+ * page ~ R^(1/4) and head_dim / channels ~ R^(1/4) (128K tokens at budget 512: R = 256, page 4,
+ * channels head_dim / 4, keep 8192). Where R^(1/4) is not a power of two the page is the power
+ * of two nearest to it on a log2 scale (halves round up), within [1, min(64, budget / 2)];
+ * channels = round(head_dim * page / sqrt(R)) within [1, head_dim]; keep and kernel_size as for
+ * rkv_plan. Errors: RKV_ERR_INVALID_ARG for ctx <= 0, budget < 2 or odd, head_dim <= 0. */
+rkv_status rkv_plan_even_split(int ctx, int budget, int head_dim, int* keep, int* page,
+                               int* channels, int* kernel_size);
+
 /* ------------------------------------------------------------------------------------------ */
 /* Stage 1: SnapKV++ eviction ([SNAP++], [EVICT], [KSIZE], [KEYPTS])                            */
 /* ------------------------------------------------------------------------------------------ */
@@ -112,6 +122,22 @@ rkv_status rkv_snapkv_compress(const void* k, const void* v, const int32_t* seq_
                                void* k_out, void* v_out, int cap, int32_t* kept_idx,
                                int32_t* out_len, float* scores_out, void* ws, size_t ws_bytes,
                                void* stream);
+
+/* The ablation without the GQA enhancement ([SNAP++], [KEYPTS] "original SnapKV"): every query
+ * head is scored and filtered on its own -- its W window rows only, no sum over the group -- and
+ * keeps its own copy of the selected rows of its K/V head h / gqa. Same arguments as
+ * rkv_snapkv_compress, with the per-unit outputs per query head:
+ *   k_out, v_out [n][n_kv*gqa][cap][128] bf16; kept_idx [n][n_kv*gqa][keep] int32;
+ *   scores_out NULL or [n][n_kv*gqa][max_len - window] fp32; out_len [n] int32.
+ * window <= 256. Workspace: rkv_snapkv_per_head_workspace_bytes. The result is a cache that the
+ * decode calls use with n_kv*gqa K/V heads and gqa = 1. */
+size_t rkv_snapkv_per_head_workspace_bytes(int n, int n_kv, int gqa, int max_len, int window);
+rkv_status rkv_snapkv_compress_per_head(const void* k, const void* v, const int32_t* seq_lens,
+                                        const void* q_win, int n, int n_kv, int gqa,
+                                        int head_dim, int max_len, int window, int kernel_size,
+                                        int keep, float scale, void* k_out, void* v_out, int cap,
+                                        int32_t* kept_idx, int32_t* out_len, float* scores_out,
+                                        void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------------ */
 /* Stage 2: page summaries ([APPROX])                                                          */

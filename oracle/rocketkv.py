@@ -40,6 +40,12 @@ Readings taken where the pages leave a step open (each restated at its function)
   R12 decode appends (when given) happen before attending; the new token is selectable.
   R13 attention scale as given (1/sqrt(d) by default); output kept in float64.
   (R14-R16 concern the seeded synthetic inputs, not this module.)
+  R18 the even split of "Is Page Always Divided Into 4?" for any ratio R = ctx / B: sqrt(R) per
+      stage, stage 2's share split evenly between page size and channel reduction; the page is the
+      power of two nearest R^(1/4) on a log2 scale (halves round up) within [1, min(64, B/2)],
+      channels = round(d * page / sqrt(R)) within [1, d], keep as in R1.
+  R19 SnapKV without the GQA enhancement ([P1] "Key points": the ablation against "original
+      SnapKV"): each query head scores with its own W window rows only, and keeps its own top-k.
   R17 RocketKV-MT ([P3] "SCBench Results"): nothing is evicted; the decode runs the stage-2 steps
       on the sequence of kept tokens (stage 1's kept positions in its order, then the tokens
       generated since), whose rows stay in the full cache. The pages do not say where generated
@@ -57,6 +63,7 @@ __all__ = [
     "snapkv_compress", "page_summaries", "channel_pick", "approx_scores", "page_select",
     "attention", "dense_decode", "hybrid_decode", "group_topk_attention", "append_token",
     "kept_view", "mt_page_summaries", "mt_hybrid_decode", "mt_append_token",
+    "plan_even_split", "snapkv_compress_per_head",
 ]
 
 
@@ -91,6 +98,26 @@ def plan(ctx: int, budget: int, head_dim: int, page: int = 0, channels: int = 0)
         page = 4
     if channels == 0:
         channels = head_dim // 4
+    keep = min(ctx, budget * page * head_dim // channels)
+    return keep, page, channels, adaptive_kernel_size(ctx)
+
+
+def plan_even_split(ctx: int, budget: int, head_dim: int):
+    """(keep, page, channels, kernel) from the even split of the ratio (reading R18).
+
+    [P3] "Is Page Always Divided Into 4?": ctx / B is split evenly between the two stages and
+    stage 2's share evenly between the sequence and head dimensions; the page size "can vary for
+    other compression ratios".
+    """
+    ratio = ctx / budget
+    stage2 = math.sqrt(ratio)
+    steps = math.floor(math.log2(stage2) / 2.0 + 0.5) if stage2 > 0 else 0
+    page = 1
+    for _ in range(max(0, steps)):
+        if page >= 64 or page * 2 > budget // 2:
+            break
+        page *= 2
+    channels = min(head_dim, max(1, round(head_dim * page / stage2)))
     keep = min(ctx, budget * page * head_dim // channels)
     return keep, page, channels, adaptive_kernel_size(ctx)
 
@@ -172,9 +199,20 @@ def snapkv_compress(k: np.ndarray, v: np.ndarray, q_win: np.ndarray, keep: int, 
     return kept, k[kept], v[kept], score, pooled
 
 
+def snapkv_compress_per_head(k: np.ndarray, v: np.ndarray, q_win: np.ndarray, keep: int,
+                             kernel: int, scale: float):
+    """SnapKV without the GQA enhancement (reading R19): `snapkv_compress` run for each query head
+    of the group alone (its W window rows), each keeping its own rows of the shared K/V head.
+    q_win: [G, W, d]. Returns one snapkv_compress result per query head.
+    """
+    return [snapkv_compress(k, v, q_win[h:h + 1], keep, kernel, scale)
+            for h in range(q_win.shape[0])]
+
+
 # --------------------------------------------------------------------------------------------
 # Stage 2: hybrid sparse decode attention
 # --------------------------------------------------------------------------------------------
+
 def page_summaries(kc: np.ndarray, length: int, page: int):
     """Element-wise Kmin / Kmax per page of consecutive tokens, channel-major [d, P].
 

@@ -97,18 +97,41 @@ rkv_status rkv_plan(int ctx, int budget, int head_dim, int page, int channels, i
   return RKV_OK;
 }
 
+// The overall ratio R = ctx / budget split evenly: sqrt(R) to each stage, and stage 2's share
+// evenly between page size and channel reduction, the page rounded to the nearest power of two
+// (in log2) within [1, min(64, budget / 2)] and the channels to the nearest integer in [1, d].
+rkv_status rkv_plan_even_split(int ctx, int budget, int head_dim, int* keep, int* page_out,
+                               int* channels_out, int* kernel_size) {
+  if (ctx <= 0 || budget <= 1 || budget % 2 != 0 || head_dim <= 0) return RKV_ERR_INVALID_ARG;
+  const double stage2 = std::sqrt((double)ctx / (double)budget);
+  const double lp = std::floor(std::log2(stage2) / 2.0 + 0.5);
+  int page = 1;
+  for (int i = 0; i < (int)lp && page < 64 && page * 2 <= budget / 2; ++i) page *= 2;
+  long long ch = std::llround((double)head_dim * page / stage2);
+  if (ch < 1) ch = 1;
+  if (ch > head_dim) ch = head_dim;
+  const long long want = (long long)budget * page * head_dim / ch;
+  if (keep) *keep = (int)(want < ctx ? want : ctx);
+  if (page_out) *page_out = page;
+  if (channels_out) *channels_out = (int)ch;
+  if (kernel_size) *kernel_size = ctx <= 8192 ? 7 : (ctx <= 32768 ? 15 : 31);
+  return RKV_OK;
+}
+
 // ------------------------------------------------------------------------------- stage 1
 size_t rkv_snapkv_workspace_bytes(int n, int n_kv, int gqa, int max_len, int window) {
   if (n <= 0 || n_kv <= 0 || gqa <= 0 || max_len <= window || window <= 0) return 0;
   return kStatusBytes + snapkv_scratch_bytes(n, n_kv, gqa, max_len, window);
 }
 
-rkv_status rkv_snapkv_compress(const void* k, const void* v, const int32_t* seq_lens,
-                               const void* q_win, int n, int n_kv, int gqa, int head_dim,
-                               int max_len, int window, int kernel_size, int keep, float scale,
-                               void* k_out, void* v_out, int cap, int32_t* kept_idx,
-                               int32_t* out_len, float* scores_out, void* ws, size_t ws_bytes,
-                               void* stream) {
+// per_head: every query head is its own unit (gqa units per K/V head, window rows of one head,
+// own kept set); else the units are the K/V heads and their groups' rows are summed.
+static rkv_status snapkv_impl(const void* k, const void* v, const int32_t* seq_lens,
+                              const void* q_win, int n, int n_kv, int gqa, int head_dim,
+                              int max_len, int window, int kernel_size, int keep, float scale,
+                              void* k_out, void* v_out, int cap, int32_t* kept_idx,
+                              int32_t* out_len, float* scores_out, void* ws, size_t ws_bytes,
+                              void* stream, bool per_head) {
   if (head_dim != kHeadDim) return RKV_ERR_UNSUPPORTED;
   if (!k || !v || !seq_lens || !q_win || !k_out || !v_out || !kept_idx || !out_len)
     return RKV_ERR_INVALID_ARG;
@@ -119,6 +142,11 @@ rkv_status rkv_snapkv_compress(const void* k, const void* v, const int32_t* seq_
       keep > cap || cap <= 0 || !(scale > 0.f) || !std::isfinite(scale))
     return RKV_ERR_INVALID_ARG;
   if (kernel_size < 0 || (kernel_size > 0 && kernel_size % 2 == 0)) return RKV_ERR_INVALID_ARG;
+  const int kv_div = per_head ? gqa : 1;
+  if (per_head) {  // the kernels see n_kv * gqa units of one query head each
+    n_kv *= gqa;
+    gqa = 1;
+  }
   if (gqa * window > 256) return RKV_ERR_UNSUPPORTED;
   const size_t need = rkv_snapkv_workspace_bytes(n, n_kv, gqa, max_len, window);
   if (!ws || !aligned16(ws) || ws_bytes < need) return RKV_ERR_WORKSPACE;
@@ -131,6 +159,7 @@ rkv_status rkv_snapkv_compress(const void* k, const void* v, const int32_t* seq_
   a.n = n;
   a.n_kv = n_kv;
   a.gqa = gqa;
+  a.kv_div = kv_div;
   a.max_len = max_len;
   a.window = window;
   a.kernel_size = kernel_size;
@@ -158,6 +187,34 @@ rkv_status rkv_snapkv_compress(const void* k, const void* v, const int32_t* seq_
   a.nlse = reinterpret_cast<float*>(p);
   a.status = status_ptr(ws);
   return from_cuda(launch_snapkv(a, as_stream(stream)));
+}
+
+rkv_status rkv_snapkv_compress(const void* k, const void* v, const int32_t* seq_lens,
+                               const void* q_win, int n, int n_kv, int gqa, int head_dim,
+                               int max_len, int window, int kernel_size, int keep, float scale,
+                               void* k_out, void* v_out, int cap, int32_t* kept_idx,
+                               int32_t* out_len, float* scores_out, void* ws, size_t ws_bytes,
+                               void* stream) {
+  return snapkv_impl(k, v, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window,
+                     kernel_size, keep, scale, k_out, v_out, cap, kept_idx, out_len, scores_out,
+                     ws, ws_bytes, stream, false);
+}
+
+size_t rkv_snapkv_per_head_workspace_bytes(int n, int n_kv, int gqa, int max_len, int window) {
+  if (gqa <= 0) return 0;
+  return rkv_snapkv_workspace_bytes(n, n_kv * gqa, 1, max_len, window);
+}
+
+rkv_status rkv_snapkv_compress_per_head(const void* k, const void* v, const int32_t* seq_lens,
+                                        const void* q_win, int n, int n_kv, int gqa,
+                                        int head_dim, int max_len, int window, int kernel_size,
+                                        int keep, float scale, void* k_out, void* v_out, int cap,
+                                        int32_t* kept_idx, int32_t* out_len, float* scores_out,
+                                        void* ws, size_t ws_bytes, void* stream) {
+  if (gqa <= 0) return RKV_ERR_INVALID_ARG;
+  return snapkv_impl(k, v, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window,
+                     kernel_size, keep, scale, k_out, v_out, cap, kept_idx, out_len, scores_out,
+                     ws, ws_bytes, stream, true);
 }
 
 // ------------------------------------------------------------------------------- summaries

@@ -120,6 +120,7 @@ struct SnapArgs {
   float* part_ml;      // workspace: [n*n_kv][nsplit][rows_pad][2] (max, sum) per split
   float* nlse;         // workspace: [n*n_kv][rows_pad] merged negated log2-sum-exp per row
   int nsplit, tokens_per_split, rows_pad;
+  int kv_div;  // units per K/V head: 1, or gqa when every query head is its own unit
   uint32_t* status;
 };
 

@@ -123,6 +123,7 @@ struct ScoreParams {
   int n_kv, gqa, window, max_len, hq;
   int units, nsplit, tiles_per_split;
   int reverse;     // walk the units last-to-first (pass 2 starts where pass 1 ended: L2-warm)
+  int kv_div;      // a unit reads the K rows of K/V head ukv / kv_div
   float scale_log2;
   const int32_t* seq_lens;
   float* part_ml;  // [units][nsplit][RP][2]: per-split (max, sum) of every window row (pass 1)
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           for (int rb = 0; rb < RB; ++rb)
             tma_load_2d(qdst + (size_t)h * RP * 128 + (size_t)rb * 128 * 128, &qmap, 64 * h,
                         qrow0 + rb * 128, &qfull[qb]);
-        const int krow0 = itm.ukv * p.max_len;
+        const int krow0 = (itm.ukv / p.kv_div) * p.max_len;
         for (int t = 0; t < itm.ntiles; ++t, ++it) {
           const int s = it % kKStages;
           if (it >= kKStages && !mbar_wait(&empty[s], (uint32_t)(((it / kKStages) - 1) & 1))) {
@@ -752,8 +753,9 @@ __global__ void __launch_bounds__(256) gather_kernel(SnapArgs a) {
   const int row0 = blockIdx.x * 64;
   if (row0 >= cnt) return;
   const int32_t* kept = a.kept_idx + (size_t)ukv * a.keep;
-  const uint4* ksrc = reinterpret_cast<const uint4*>(a.k + (size_t)ukv * a.max_len * kHeadDim);
-  const uint4* vsrc = reinterpret_cast<const uint4*>(a.v + (size_t)ukv * a.max_len * kHeadDim);
+  const size_t src_unit = (size_t)(ukv / a.kv_div);
+  const uint4* ksrc = reinterpret_cast<const uint4*>(a.k + src_unit * a.max_len * kHeadDim);
+  const uint4* vsrc = reinterpret_cast<const uint4*>(a.v + src_unit * a.max_len * kHeadDim);
   uint4* kdst = reinterpret_cast<uint4*>(a.k_out + (size_t)ukv * a.cap * kHeadDim);
   uint4* vdst = reinterpret_cast<uint4*>(a.v_out + (size_t)ukv * a.cap * kHeadDim);
   uint4 kv[4], vv[4];
@@ -873,7 +875,7 @@ static cudaError_t launch_pass(const CUtensorMap& km, const CUtensorMap& qm,
 
 cudaError_t launch_snapkv(const SnapArgs& a, cudaStream_t s) {
   CUtensorMap km, qm;
-  const uint64_t krows = (uint64_t)a.n * a.n_kv * a.max_len;
+  const uint64_t krows = (uint64_t)a.n * (a.n_kv / a.kv_div) * a.max_len;
   const uint64_t qrows = (uint64_t)a.n * a.n_kv * a.gqa * a.window;
   if (!make_rows_map(&km, a.k, krows) || !make_rows_map(&qm, a.q_win, qrows))
     return cudaErrorInvalidValue;
@@ -886,6 +888,7 @@ cudaError_t launch_snapkv(const SnapArgs& a, cudaStream_t s) {
   sp.hq = a.n_kv * a.gqa;
   sp.units = units;
   sp.nsplit = a.nsplit;
+  sp.kv_div = a.kv_div;
   sp.tiles_per_split = a.tokens_per_split;
   sp.scale_log2 = a.scale_log2;
   sp.seq_lens = a.seq_lens;

@@ -29,7 +29,8 @@ SYMBOLS = [
     "rkv_snapkv_compress", "rkv_summaries_workspace_bytes", "rkv_build_page_summaries",
     "rkv_hybrid_decode_workspace_bytes", "rkv_hybrid_decode",
     "rkv_dense_decode_workspace_bytes", "rkv_dense_decode", "rkv_dense_decode_noalloc",
-    "rkv_build_page_summaries_mt", "rkv_hybrid_decode_mt",
+    "rkv_build_page_summaries_mt", "rkv_hybrid_decode_mt", "rkv_plan_even_split",
+    "rkv_snapkv_per_head_workspace_bytes", "rkv_snapkv_compress_per_head",
 ]
 
 
@@ -78,6 +79,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
                              i32),
         "rkv_dense_decode_noalloc": ([vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp],
                                      i32),
+        "rkv_plan_even_split": ([i32, i32, i32, ip, ip, ip, ip], i32),
+        "rkv_snapkv_per_head_workspace_bytes": ([i32, i32, i32, i32, i32], sz),
+        "rkv_snapkv_compress_per_head": ([vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
+                                          f32, vp, vp, i32, vp, vp, vp, vp, sz, vp], i32),
         "rkv_build_page_summaries_mt": ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp,
                                          vp, vp, sz, vp], i32),
         "rkv_hybrid_decode_mt": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
@@ -149,6 +154,14 @@ def rkv_plan(ctx: int, budget: int, head_dim: int = HEAD_DIM, page: int = 0, cha
     return tuple(o.value for o in out)
 
 
+def rkv_plan_even_split(ctx: int, budget: int, head_dim: int = HEAD_DIM):
+    """(keep, page, channels, kernel_size) from the even split of ctx / budget."""
+    out = [ctypes.c_int(0) for _ in range(4)]
+    code = load().rkv_plan_even_split(ctx, budget, head_dim, *[ctypes.byref(o) for o in out])
+    _check("rkv_plan_even_split", code)
+    return tuple(o.value for o in out)
+
+
 # ------------------------------------------------------------------------------- stage 1
 def rkv_snapkv_workspace_bytes(n: int, n_kv: int, gqa: int, max_len: int, window: int) -> int:
     return int(load().rkv_snapkv_workspace_bytes(n, n_kv, gqa, max_len, window))
@@ -171,6 +184,33 @@ def rkv_snapkv_compress(k, v, seq_lens, q_win, kernel_size: int, keep: int, scal
         kernel_size, keep, float(scale), _ptr(k_out), _ptr(v_out), cap, _ptr(kept_idx),
         _ptr(out_len), _ptr(scores_out), _ptr(ws), ws.numel(), _stream(stream))
     _check("rkv_snapkv_compress", code)
+    return ws
+
+
+def rkv_snapkv_per_head_workspace_bytes(n: int, n_kv: int, gqa: int, max_len: int,
+                                        window: int) -> int:
+    return int(load().rkv_snapkv_per_head_workspace_bytes(n, n_kv, gqa, max_len, window))
+
+
+def rkv_snapkv_compress_per_head(k, v, seq_lens, q_win, kernel_size: int, keep: int,
+                                 scale: float, k_out, v_out, kept_idx, out_len, scores_out=None,
+                                 ws=None, stream=None):
+    """SnapKV without the GQA sum: every query head scored and filtered on its own; outputs per
+    query head ([n][n_kv*gqa][...]); see include/rkv.h."""
+    _bf16(k, "k"), _bf16(v, "v"), _bf16(q_win, "q_win"), _i32(seq_lens, "seq_lens")
+    _i32(kept_idx, "kept_idx"), _i32(out_len, "out_len")
+    n, n_kv, max_len, d = k.shape
+    hq, window = q_win.shape[1], q_win.shape[2]
+    gqa = hq // n_kv
+    cap = k_out.shape[2]
+    if ws is None:
+        ws = workspace(rkv_snapkv_per_head_workspace_bytes(n, n_kv, gqa, max_len, window),
+                       k.device)
+    code = load().rkv_snapkv_compress_per_head(
+        _ptr(k), _ptr(v), _ptr(seq_lens), _ptr(q_win), n, n_kv, gqa, d, max_len, window,
+        kernel_size, keep, float(scale), _ptr(k_out), _ptr(v_out), cap, _ptr(kept_idx),
+        _ptr(out_len), _ptr(scores_out), _ptr(ws), ws.numel(), _stream(stream))
+    _check("rkv_snapkv_compress_per_head", code)
     return ws
 
 

@@ -106,6 +106,32 @@ def test_validation_rejects_before_launch(lib):
 
 
 
+@pytest.mark.parametrize("ctx", [100, 4096, 8192, 30000, 32768, 65536, 131072, 1 << 20])
+@pytest.mark.parametrize("budget", [64, 256, 512, 1024, 4096])
+def test_plan_even_split_matches_oracle(lib, ctx, budget):
+    from sparse_kv_cache_snapkv_gb300 import rkv
+    assert rkv.rkv_plan_even_split(ctx, budget) == O.plan_even_split(ctx, budget, 128)
+
+
+def test_per_head_compress_validation(lib):
+    vp = FAKE
+    args = (vp, vp, vp, vp, 1, 2, 4, 128, 4096, 32)
+    big = 1 << 30
+    # window over 256 rows, even kernel, keep <= window, gqa 0, small workspace
+    assert lib.rkv_snapkv_compress_per_head(vp, vp, vp, vp, 1, 2, 4, 128, 4096, 300, 7, 512, 0.1,
+                                            vp, vp, 512, vp, vp, None, vp, big, None) == 2
+    assert lib.rkv_snapkv_compress_per_head(*args, 6, 256, 0.1, vp, vp, 256, vp, vp, None, vp,
+                                            big, None) == 1
+    assert lib.rkv_snapkv_compress_per_head(*args, 7, 32, 0.1, vp, vp, 256, vp, vp, None, vp,
+                                            big, None) == 1
+    assert lib.rkv_snapkv_compress_per_head(vp, vp, vp, vp, 1, 2, 0, 128, 4096, 32, 7, 256, 0.1,
+                                            vp, vp, 256, vp, vp, None, vp, big, None) == 1
+    assert lib.rkv_snapkv_compress_per_head(*args, 7, 256, 0.1, vp, vp, 256, vp, vp, None, vp, 64,
+                                            None) == 3
+    # the per-head workspace is the one of n_kv * gqa single-head units
+    assert lib.rkv_snapkv_per_head_workspace_bytes(2, 8, 4, 32768, 32) == \
+        lib.rkv_snapkv_workspace_bytes(2, 32, 1, 32768, 32)
+
 def test_mt_validation_rejects_before_launch(lib):
     vp = FAKE
     # (q, new_k, new_v, k_full, v_full, full_len, kept_idx, kept_len, kmin, kmax)

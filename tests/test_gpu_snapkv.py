@@ -135,6 +135,46 @@ def test_snapkv_select_paths(kernel):
         _check_unit(x, u, 0, 4, 32, kernel, 2048, *res, tag=f"kernel {kernel} u{u}")
 
 
+def test_snapkv_per_head_without_group_sum():
+    # SnapKV without the GQA enhancement: each query head is scored with its own window rows and
+    # keeps its own rows of its K/V head; ragged lengths, one prompt shorter than keep
+    rkv = _lib()
+    gqa, W, keep, kernel = 4, 32, 1024, 15
+    wl, x = _inputs(3, 2, gqa, [5000, 3001, 900], W, seed=108, needles=4)
+    k, v, q, lens = x["k"], x["v"], x["q_win"], x["seq_lens"]
+    n, n_kv, max_len, _ = k.shape
+    hq = n_kv * gqa
+    scale = 1.0 / math.sqrt(D)
+    k_out = torch.zeros(n, hq, keep, D, dtype=torch.bfloat16, device="cuda")
+    v_out = torch.zeros_like(k_out)
+    kept = torch.full((n, hq, keep), -9, dtype=torch.int32, device="cuda")
+    out_len = torch.full((n,), -9, dtype=torch.int32, device="cuda")
+    scores = torch.full((n, hq, max_len - W), -1.0, dtype=torch.float32, device="cuda")
+    ws = rkv.rkv_snapkv_compress_per_head(k, v, lens, q, kernel, keep, scale, k_out, v_out, kept,
+                                          out_len, scores_out=scores)
+    rkv.rkv_check_status(ws)
+    for (u, h) in [(0, 0), (0, 5), (1, 3), (1, 6), (2, 2)]:
+        g, L = h // gqa, int(lens[u])
+        tag = f"unit {u} q head {h}"
+        kk, vv = _f64(k[u, g, :L]), _f64(v[u, g, :L])
+        ref = O.window_scores(kk, _f64(q[u, h:h + 1]), scale)
+        gs = scores[u, h, :L - W].cpu().numpy().astype(np.float64)
+        assert (np.abs(gs - ref) <= SCORE_REL * np.abs(ref) + 1e-30).all(), tag
+        got = kept[u, h].cpu().numpy()
+        cnt = min(L, keep)
+        assert int(out_len[u]) == cnt, tag
+        if L <= keep:
+            assert np.array_equal(got[:L], np.arange(L)), tag
+        else:
+            assert np.array_equal(got[keep - W:], np.arange(L - W, L)), tag
+            parity.check_selection(got[:keep - W], O.pool_max(ref, kernel), keep - W, tag)
+        idx = got[:cnt]
+        assert np.array_equal(_f64(k_out[u, h, :cnt]), kk[idx]), tag
+        assert np.array_equal(_f64(v_out[u, h, :cnt]), vv[idx]), tag
+    # heads of one group select differently (they are no longer summed)
+    assert not torch.equal(kept[0, 0], kept[0, 1])
+
+
 def test_snapkv_multiple_waves():
     # 6 units of 64K tokens: K of all units exceeds one L2-sized wave, so several waves run
     rkv = _lib()

@@ -413,3 +413,50 @@ def test_mt_append_matches_rebuild():
     ra, rb = O.mt_page_summaries(kf, kept, nk, p)
     P = (nk + p - 1) // p
     assert np.array_equal(kmin[:, :P], ra) and np.array_equal(kmax[:, :P], rb)
+
+
+# ---------------------------------------------------------------- even-split planner (R18)
+def test_plan_even_split_worked_example():
+    g = _golden("planner_worked_example.json")
+    keep, page, channels, _ = O.plan_even_split(g["ctx"], g["budget"], g["head_dim"])
+    assert page == g["page"]
+    assert g["head_dim"] // channels == g["head_dim_ratio"]
+    assert g["ctx"] // keep == g["per_stage_ratio"]
+
+
+@pytest.mark.parametrize("ctx,budget", [(131072, 512), (32768, 256), (65536, 512), (1 << 20, 64),
+                                        (8192, 1024), (100, 256), (4096, 4096), (131072, 64)])
+def test_plan_even_split_identities(ctx, budget):
+    d = 128
+    keep, page, channels, _ = O.plan_even_split(ctx, budget, d)
+    ratio = ctx / budget
+    assert page & (page - 1) == 0 and 1 <= page <= min(64, budget // 2)
+    assert 1 <= channels <= d
+    assert keep == min(ctx, budget * page * d // channels)
+    if ratio > 1 and page < min(64, budget // 2):
+        # the page is the power of two nearest R^(1/4) (log2 scale), unless clamped
+        assert abs(math.log2(page) - math.log2(ratio) / 4) <= 0.5 + 1e-12
+    if 1 < channels < d:
+        # page * d / channels approximates the stage-2 ratio sqrt(R) up to channel rounding
+        assert abs(d * page / channels - math.sqrt(ratio)) <= d * page / channels / (2 * channels - 1) + 1e-9
+    if ratio >= 1 and math.log2(ratio) % 4 == 0 and page < min(64, budget // 2):
+        # ratios 16^k split exactly: page = d / channels = R^(1/4)
+        assert page == round(ratio ** 0.25) and d // channels == page
+
+
+# ---------------------------------------------------------------- SnapKV without the GQA sum (R19)
+def test_per_head_scores_sum_to_group_scores():
+    rng = np.random.default_rng(20)
+    L, W, G, d = 300, 8, 4, 16
+    k = _bf16_values((L, d), rng)
+    q = _bf16_values((G, W, d), rng)
+    group = O.window_scores(k, q, 0.25)
+    per_head = [O.window_scores(k, q[h:h + 1], 0.25) for h in range(G)]
+    np.testing.assert_allclose(np.sum(per_head, axis=0), group, rtol=1e-12)
+    res = O.snapkv_compress_per_head(k, _bf16_values((L, d), rng), q, 64, 7, 0.25)
+    assert len(res) == G
+    for h, (kept, kc, _, score, _) in enumerate(res):
+        np.testing.assert_array_equal(score, per_head[h])
+        assert np.array_equal(kept[-W:], np.arange(L - W, L)) and np.array_equal(kc, k[kept])
+    # heads that look at different parts of the prompt keep different tokens
+    assert not all(np.array_equal(res[0][0], r[0]) for r in res[1:])
