@@ -240,6 +240,47 @@ rkv_status rkv_hybrid_decode_mt(const void* q, const void* new_k, const void* ne
                                 void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------------ */
+/* Paged (block-table) compact cache, for serving engines that page their KV cache             */
+/* ------------------------------------------------------------------------------------------ */
+/* The same three steps -- stage 1 with its gather, page summaries, decode -- on a compact cache
+ * held in fixed-size blocks of a shared pool instead of one contiguous region per unit (a
+ * storage layout of the serving engine; the computation is that of the non-paged calls, with
+ * identical results):
+ *   k_pool, v_pool [num_blocks][n_kv][block][128] bf16; block a power of two <= 65536;
+ *   block_table [n][max_blocks] int32: token t of unit u (every K/V head g) is row t % block of
+ *   block block_table[u][t / block]; capacity = max_blocks * block tokens per unit.
+ * Blocks are the caller's: every block a call may write (stage 1: tokens < keep; an append:
+ * token len[u]) must be listed in the table beforehand. A table entry outside [0, num_blocks)
+ * that a kernel meets sets RKV_DEV_BAD_INDEX and block 0 is used in its place.
+ *
+ * rkv_snapkv_compress_paged: rkv_snapkv_compress (workspace rkv_snapkv_workspace_bytes) whose
+ *   kept rows go to the pools; keep <= capacity.
+ * rkv_build_page_summaries_paged: rkv_build_page_summaries over the paged cache (len[u] <=
+ *   capacity, else RKV_DEV_LEN_OVER_CAP); workspace rkv_summaries_workspace_bytes.
+ * rkv_hybrid_decode_paged: rkv_hybrid_decode over the paged cache, appends included (len[u] <
+ *   capacity to append); workspace rkv_hybrid_decode_workspace_bytes. */
+rkv_status rkv_snapkv_compress_paged(const void* k, const void* v, const int32_t* seq_lens,
+                                     const void* q_win, int n, int n_kv, int gqa, int head_dim,
+                                     int max_len, int window, int kernel_size, int keep,
+                                     float scale, void* k_pool, void* v_pool, int num_blocks,
+                                     int block, const int32_t* block_table, int max_blocks,
+                                     int32_t* kept_idx, int32_t* out_len, float* scores_out,
+                                     void* ws, size_t ws_bytes, void* stream);
+rkv_status rkv_build_page_summaries_paged(const void* k_pool, const int32_t* block_table,
+                                          const int32_t* len, int n, int n_kv, int head_dim,
+                                          int num_blocks, int block, int max_blocks, int page,
+                                          int page_cap, int first_token, void* kmin, void* kmax,
+                                          void* ws, size_t ws_bytes, void* stream);
+rkv_status rkv_hybrid_decode_paged(const void* q, const void* new_k, const void* new_v,
+                                   void* k_pool, void* v_pool, const int32_t* block_table,
+                                   int32_t* len, void* kmin, void* kmax, int n, int n_kv, int gqa,
+                                   int head_dim, int num_blocks, int block, int max_blocks,
+                                   int page_cap, int budget, int page, int channels, float scale,
+                                   void* out, int32_t* sel_channels, int32_t* sel_pages,
+                                   float* approx_scores, void* ws, size_t ws_bytes,
+                                   void* stream);
+
+/* ------------------------------------------------------------------------------------------ */
 /* Full-KV decode attention, the baseline the method is compared against ([KEYPTS])            */
 /* ------------------------------------------------------------------------------------------ */
 size_t rkv_dense_decode_workspace_bytes(int n, int n_kv, int gqa, int max_len);

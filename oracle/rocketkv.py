@@ -44,6 +44,8 @@ Readings taken where the pages leave a step open (each restated at its function)
       stage, stage 2's share split evenly between page size and channel reduction; the page is the
       power of two nearest R^(1/4) on a log2 scale (halves round up) within [1, min(64, B/2)],
       channels = round(d * page / sqrt(R)) within [1, d], keep as in R1.
+  R20 a paged (block-table) compact cache is a storage layout only: every step computes on the
+      rows the table names, in token order, exactly as on the contiguous cache.
   R19 SnapKV without the GQA enhancement ([P1] "Key points": the ablation against "original
       SnapKV"): each query head scores with its own W window rows only, and keeps its own top-k.
   R17 RocketKV-MT ([P3] "SCBench Results"): nothing is evicted; the decode runs the stage-2 steps
@@ -63,7 +65,7 @@ __all__ = [
     "snapkv_compress", "page_summaries", "channel_pick", "approx_scores", "page_select",
     "attention", "dense_decode", "hybrid_decode", "group_topk_attention", "append_token",
     "kept_view", "mt_page_summaries", "mt_hybrid_decode", "mt_append_token",
-    "plan_even_split", "snapkv_compress_per_head",
+    "plan_even_split", "snapkv_compress_per_head", "paged_view", "paged_scatter",
 ]
 
 
@@ -389,6 +391,24 @@ def mt_append_token(k_full: np.ndarray, v_full: np.ndarray, full_len: int, kept:
         kmin[:, pg] = np.minimum(kmin[:, pg], new_k)
         kmax[:, pg] = np.maximum(kmax[:, pg], new_k)
     return full_len + 1, n_kept + 1
+
+
+# --------------------------------------------------------------------------------------------
+# Paged compact cache (reading R20)
+# --------------------------------------------------------------------------------------------
+def paged_view(pool: np.ndarray, table: np.ndarray, n_tok: int, g: int) -> np.ndarray:
+    """Rows of tokens 0 .. n_tok-1 of K/V head g from a pool [blocks][n_kv][block][d] whose token
+    t sits in block table[t // block], row t % block."""
+    block = pool.shape[2]
+    t = np.arange(n_tok)
+    return pool[np.asarray(table, dtype=np.int64)[t // block], g, t % block]
+
+
+def paged_scatter(pool: np.ndarray, table: np.ndarray, rows: np.ndarray, g: int) -> None:
+    """Write rows (token order) of K/V head g into their blocks (in place)."""
+    block = pool.shape[2]
+    t = np.arange(rows.shape[0])
+    pool[np.asarray(table, dtype=np.int64)[t // block], g, t % block] = rows
 
 
 def default_scale(head_dim: int) -> float:

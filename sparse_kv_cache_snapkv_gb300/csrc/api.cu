@@ -131,7 +131,7 @@ static rkv_status snapkv_impl(const void* k, const void* v, const int32_t* seq_l
                               int max_len, int window, int kernel_size, int keep, float scale,
                               void* k_out, void* v_out, int cap, int32_t* kept_idx,
                               int32_t* out_len, float* scores_out, void* ws, size_t ws_bytes,
-                              void* stream, bool per_head) {
+                              void* stream, bool per_head, const PagedMap& out_pm) {
   if (head_dim != kHeadDim) return RKV_ERR_UNSUPPORTED;
   if (!k || !v || !seq_lens || !q_win || !k_out || !v_out || !kept_idx || !out_len)
     return RKV_ERR_INVALID_ARG;
@@ -160,6 +160,7 @@ static rkv_status snapkv_impl(const void* k, const void* v, const int32_t* seq_l
   a.n_kv = n_kv;
   a.gqa = gqa;
   a.kv_div = kv_div;
+  a.out_pm = out_pm;
   a.max_len = max_len;
   a.window = window;
   a.kernel_size = kernel_size;
@@ -197,7 +198,7 @@ rkv_status rkv_snapkv_compress(const void* k, const void* v, const int32_t* seq_
                                void* stream) {
   return snapkv_impl(k, v, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window,
                      kernel_size, keep, scale, k_out, v_out, cap, kept_idx, out_len, scores_out,
-                     ws, ws_bytes, stream, false);
+                     ws, ws_bytes, stream, false, PagedMap{});
 }
 
 size_t rkv_snapkv_per_head_workspace_bytes(int n, int n_kv, int gqa, int max_len, int window) {
@@ -214,7 +215,7 @@ rkv_status rkv_snapkv_compress_per_head(const void* k, const void* v, const int3
   if (gqa <= 0) return RKV_ERR_INVALID_ARG;
   return snapkv_impl(k, v, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window,
                      kernel_size, keep, scale, k_out, v_out, cap, kept_idx, out_len, scores_out,
-                     ws, ws_bytes, stream, true);
+                     ws, ws_bytes, stream, true, PagedMap{});
 }
 
 // ------------------------------------------------------------------------------- summaries
@@ -222,9 +223,9 @@ size_t rkv_summaries_workspace_bytes(void) { return kStatusBytes; }
 
 // Summaries of the cache (kept == nullptr) or of the kept sequence of the full cache.
 static rkv_status summaries_impl(const void* k_cache, const int32_t* len, const int32_t* kept,
-                                 int n, int n_kv, int head_dim, int cap, int vcap, int page,
-                                 int page_cap, int first_token, void* kmin, void* kmax, void* ws,
-                                 size_t ws_bytes, void* stream) {
+                                 const PagedMap& pm, int n, int n_kv, int head_dim, int cap,
+                                 int vcap, int page, int page_cap, int first_token, void* kmin,
+                                 void* kmax, void* ws, size_t ws_bytes, void* stream) {
   if (head_dim != kHeadDim) return RKV_ERR_UNSUPPORTED;
   if (!k_cache || !len || !kmin || !kmax) return RKV_ERR_INVALID_ARG;
   if (!aligned16(k_cache) || !aligned16(kmin) || !aligned16(kmax)) return RKV_ERR_INVALID_ARG;
@@ -236,6 +237,7 @@ static rkv_status summaries_impl(const void* k_cache, const int32_t* len, const 
   a.k_cache = static_cast<const bf16*>(k_cache);
   a.len = len;
   a.kept = kept;
+  a.pm = pm;
   a.kmin = static_cast<bf16*>(kmin);
   a.kmax = static_cast<bf16*>(kmax);
   a.n = n;
@@ -253,8 +255,8 @@ rkv_status rkv_build_page_summaries(const void* k_cache, const int32_t* len, int
                                     int head_dim, int cap, int page, int page_cap,
                                     int first_token, void* kmin, void* kmax, void* ws,
                                     size_t ws_bytes, void* stream) {
-  return summaries_impl(k_cache, len, nullptr, n, n_kv, head_dim, cap, cap, page, page_cap,
-                        first_token, kmin, kmax, ws, ws_bytes, stream);
+  return summaries_impl(k_cache, len, nullptr, PagedMap{}, n, n_kv, head_dim, cap, cap, page,
+                        page_cap, first_token, kmin, kmax, ws, ws_bytes, stream);
 }
 
 rkv_status rkv_build_page_summaries_mt(const void* k_full, const int32_t* kept_idx,
@@ -263,8 +265,8 @@ rkv_status rkv_build_page_summaries_mt(const void* k_full, const int32_t* kept_i
                                        int first_token, void* kmin, void* kmax, void* ws,
                                        size_t ws_bytes, void* stream) {
   if (!kept_idx) return RKV_ERR_INVALID_ARG;
-  return summaries_impl(k_full, kept_len, kept_idx, n, n_kv, head_dim, full_cap, kcap, page,
-                        page_cap, first_token, kmin, kmax, ws, ws_bytes, stream);
+  return summaries_impl(k_full, kept_len, kept_idx, PagedMap{}, n, n_kv, head_dim, full_cap, kcap,
+                        page, page_cap, first_token, kmin, kmax, ws, ws_bytes, stream);
 }
 
 // ------------------------------------------------------------------------------- hybrid
@@ -282,7 +284,8 @@ size_t rkv_hybrid_decode_workspace_bytes(int n, int n_kv, int gqa, int page_cap,
 // One decode step over the cache (kept == nullptr) or over the kept sequence of the full cache.
 static rkv_status hybrid_impl(const void* q, const void* new_k, const void* new_v,
                               void* k_cache, void* v_cache, int32_t* len, int32_t* kept,
-                              int32_t* full_len, void* kmin, void* kmax, int n, int n_kv,
+                              int32_t* full_len, const PagedMap& pm, void* kmin, void* kmax, int n,
+                              int n_kv,
                               int gqa, int head_dim, int cap, int vcap, int page_cap, int budget,
                               int page, int channels, float scale, void* out,
                               int32_t* sel_channels, int32_t* sel_pages, float* approx_scores,
@@ -315,6 +318,7 @@ static rkv_status hybrid_impl(const void* q, const void* new_k, const void* new_
     ap.kmax = static_cast<bf16*>(kmax);
     ap.kept = kept;
     ap.full_len = full_len;
+    ap.pm = pm;
     ap.n = n;
     ap.n_kv = n_kv;
     ap.cap = cap;
@@ -325,7 +329,8 @@ static rkv_status hybrid_impl(const void* q, const void* new_k, const void* new_
     cudaError_t e = launch_append(ap, s);
     if (e != cudaSuccess) return RKV_ERR_CUDA;
   }
-  HybridArgsMT a{};
+  HybridArgsAll a{};
+  a.pm = pm;
   a.q = static_cast<const bf16*>(q);
   a.k_cache = static_cast<const bf16*>(k_cache);
   a.v_cache = static_cast<const bf16*>(v_cache);
@@ -358,9 +363,9 @@ rkv_status rkv_hybrid_decode(const void* q, const void* new_k, const void* new_v
                              int budget, int page, int channels, float scale, void* out,
                              int32_t* sel_channels, int32_t* sel_pages, float* approx_scores,
                              void* ws, size_t ws_bytes, void* stream) {
-  return hybrid_impl(q, new_k, new_v, k_cache, v_cache, len, nullptr, nullptr, kmin, kmax, n,
-                     n_kv, gqa, head_dim, cap, cap, page_cap, budget, page, channels, scale, out,
-                     sel_channels, sel_pages, approx_scores, ws, ws_bytes, stream);
+  return hybrid_impl(q, new_k, new_v, k_cache, v_cache, len, nullptr, nullptr, PagedMap{}, kmin,
+                     kmax, n, n_kv, gqa, head_dim, cap, cap, page_cap, budget, page, channels,
+                     scale, out, sel_channels, sel_pages, approx_scores, ws, ws_bytes, stream);
 }
 
 rkv_status rkv_hybrid_decode_mt(const void* q, const void* new_k, const void* new_v,
@@ -371,8 +376,57 @@ rkv_status rkv_hybrid_decode_mt(const void* q, const void* new_k, const void* ne
                                 int32_t* sel_channels, int32_t* sel_pages, float* approx_scores,
                                 void* ws, size_t ws_bytes, void* stream) {
   if (!kept_idx || !full_len) return RKV_ERR_INVALID_ARG;
-  return hybrid_impl(q, new_k, new_v, k_full, v_full, kept_len, kept_idx, full_len, kmin, kmax,
-                     n, n_kv, gqa, head_dim, full_cap, kcap, page_cap, budget, page, channels,
+  return hybrid_impl(q, new_k, new_v, k_full, v_full, kept_len, kept_idx, full_len, PagedMap{},
+                     kmin, kmax, n, n_kv, gqa, head_dim, full_cap, kcap, page_cap, budget, page,
+                     channels, scale, out, sel_channels, sel_pages, approx_scores, ws, ws_bytes,
+                     stream);
+}
+
+// ------------------------------------------------------------------------------- paged
+static bool paged_ok(const void* table, int num_blocks, int block, int max_blocks) {
+  return table && num_blocks > 0 && max_blocks > 0 && pow2(block) && block <= 65536 &&
+         (long long)max_blocks * block <= (1ll << 30);
+}
+
+rkv_status rkv_snapkv_compress_paged(const void* k, const void* v, const int32_t* seq_lens,
+                                     const void* q_win, int n, int n_kv, int gqa, int head_dim,
+                                     int max_len, int window, int kernel_size, int keep,
+                                     float scale, void* k_pool, void* v_pool, int num_blocks,
+                                     int block, const int32_t* block_table, int max_blocks,
+                                     int32_t* kept_idx, int32_t* out_len, float* scores_out,
+                                     void* ws, size_t ws_bytes, void* stream) {
+  if (!paged_ok(block_table, num_blocks, block, max_blocks)) return RKV_ERR_INVALID_ARG;
+  const PagedMap pm{block_table, max_blocks, block, num_blocks};
+  return snapkv_impl(k, v, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window,
+                     kernel_size, keep, scale, k_pool, v_pool, max_blocks * block, kept_idx,
+                     out_len, scores_out, ws, ws_bytes, stream, false, pm);
+}
+
+rkv_status rkv_build_page_summaries_paged(const void* k_pool, const int32_t* block_table,
+                                          const int32_t* len, int n, int n_kv, int head_dim,
+                                          int num_blocks, int block, int max_blocks, int page,
+                                          int page_cap, int first_token, void* kmin, void* kmax,
+                                          void* ws, size_t ws_bytes, void* stream) {
+  if (!paged_ok(block_table, num_blocks, block, max_blocks)) return RKV_ERR_INVALID_ARG;
+  const PagedMap pm{block_table, max_blocks, block, num_blocks};
+  const int capacity = max_blocks * block;
+  return summaries_impl(k_pool, len, nullptr, pm, n, n_kv, head_dim, capacity, capacity, page,
+                        page_cap, first_token, kmin, kmax, ws, ws_bytes, stream);
+}
+
+rkv_status rkv_hybrid_decode_paged(const void* q, const void* new_k, const void* new_v,
+                                   void* k_pool, void* v_pool, const int32_t* block_table,
+                                   int32_t* len, void* kmin, void* kmax, int n, int n_kv, int gqa,
+                                   int head_dim, int num_blocks, int block, int max_blocks,
+                                   int page_cap, int budget, int page, int channels, float scale,
+                                   void* out, int32_t* sel_channels, int32_t* sel_pages,
+                                   float* approx_scores, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  if (!paged_ok(block_table, num_blocks, block, max_blocks)) return RKV_ERR_INVALID_ARG;
+  const PagedMap pm{block_table, max_blocks, block, num_blocks};
+  const int capacity = max_blocks * block;
+  return hybrid_impl(q, new_k, new_v, k_pool, v_pool, len, nullptr, nullptr, pm, kmin, kmax, n,
+                     n_kv, gqa, head_dim, capacity, capacity, page_cap, budget, page, channels,
                      scale, out, sel_channels, sel_pages, approx_scores, ws, ws_bytes, stream);
 }
 

@@ -24,6 +24,25 @@ __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
 }
 
 // ------------------------------------------------------------------------------------------
+// paged cache addressing
+// ------------------------------------------------------------------------------------------
+// Block of token t of unit u, checked against the pool size (block 0 and RKV_DEV_BAD_INDEX if a
+// table entry is out of range). t / block < max_blocks is the caller's bound (len <= capacity).
+__device__ __forceinline__ int paged_block(const PagedMap& m, int u, int t, uint32_t* status) {
+  int blk = m.table[(size_t)u * m.max_blocks + t / m.block];
+  if (blk < 0 || blk >= m.num_blocks) {
+    set_status(status, RKV_DEV_BAD_INDEX);
+    blk = 0;
+  }
+  return blk;
+}
+
+// Row (128 elements) of a pool [num_blocks][n_kv][block][128] holding token t of head g in blk.
+__device__ __forceinline__ size_t paged_row(const PagedMap& m, int blk, int n_kv, int g, int t) {
+  return ((size_t)blk * n_kv + g) * m.block + (t % m.block);
+}
+
+// ------------------------------------------------------------------------------------------
 // bf16 helpers
 // ------------------------------------------------------------------------------------------
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

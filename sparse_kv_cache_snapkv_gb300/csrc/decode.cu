@@ -246,9 +246,10 @@ size_t hybrid_smem_bytes(int gqa, int page_cap, int budget, int page) {
   return b;
 }
 
-// MT: the sequence is the kept list of the full cache (A = HybridArgsMT), else the cache itself
-// (A = HybridArgs, whose smaller parameter block keeps the plain launch cheaper).
-template <int G, bool MT, typename A>
+// MODE 0: the sequence is the cache itself (A = HybridArgs, whose smaller parameter block keeps
+// the plain launch cheaper); 1: the kept list of the full cache (RocketKV-MT, A = HybridArgsMT);
+// 2: a paged cache (A = HybridArgsPaged).
+template <int G, int MODE, typename A>
 __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(A a) {
   extern __shared__ __align__(1024) unsigned char smem[];
   __shared__ float qs[G * kHeadDim];
@@ -280,10 +281,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(A a) {
   const int len = a.len[u];
   int flen = a.cap;  // rows a kept index may name
   int vcap = a.cap;  // bound of len
-  if constexpr (MT) {
+  if constexpr (MODE == 1) {
     flen = a.full_len[u];
     vcap = a.vcap;
   }
+  if constexpr (MODE == 2) vcap = a.pm.max_blocks * a.pm.block;
   const int p = a.page;
   const int P = (len + p - 1) / p;
   const int S = (a.budget / 2) / p;
@@ -436,7 +438,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(A a) {
     const int half = (lane >> 4) & 1, c16 = lane & 15;
     const bf16* cache = half ? a.v_cache : a.k_cache;
     bf16* dst = (half ? Vw : Kw) + c16 * 8;
-    if constexpr (MT) {
+    if constexpr (MODE == 2) {
+      // lane r looks up (and checks) the block of the unit's token r in the page table
+      int kblk = 0;
+      if (lane < nt) {
+        const int v = v0 + lane;
+        kblk = paged_block(a.pm, u, (sel[v >> lp] << lp) + (v & (p - 1)), a.status);
+      }
+      for (int r = 0; r < nt; ++r) {
+        const int v = v0 + r;
+        const int blk = __shfl_sync(0xffffffffu, kblk, r);
+        const size_t row = paged_row(a.pm, blk, a.n_kv, g, (sel[v >> lp] << lp) + (v & (p - 1)));
+        cp_async16(dst + r * kRowPad, cache + row * kHeadDim + c16 * 8);
+      }
+    } else if constexpr (MODE == 1) {
       // lane r fetches the cache row of the unit's token r from the kept list, checked
       int krow = 0;
       if (lane < nt) {
@@ -513,21 +528,30 @@ static cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-cudaError_t launch_hybrid(const HybridArgsMT& a, cudaStream_t s) {
+cudaError_t launch_hybrid(const HybridArgsAll& a, cudaStream_t s) {
   const HybridArgs& plain = a;
+  const HybridArgsMT& mt = a;
+  HybridArgsPaged pg;
+  static_cast<HybridArgs&>(pg) = plain;
+  pg.pm = a.pm;
   const size_t smem = hybrid_smem_bytes(a.gqa, a.page_cap, a.budget, a.page);
   const dim3 grid(a.n * a.n_kv), block(kDecodeThreads);
   cudaError_t e = cudaSuccess;
   switch (a.gqa) {
 #define RKV_CASE(GG)                                                                         \
   case GG:                                                                                   \
-    if (a.kept) {                                                                            \
-      auto* k = hybrid_decode_kernel<GG, true, HybridArgsMT>;                                \
+    if (a.pm.table) {                                                                        \
+      auto* k = hybrid_decode_kernel<GG, 2, HybridArgsPaged>;                                \
       e = ensure_dyn_smem((const void*)k, smem);                                             \
       if (e != cudaSuccess) return e;                                                        \
-      e = launch_pdl(k, grid, block, smem, s, a);                                            \
+      e = launch_pdl(k, grid, block, smem, s, pg);                                           \
+    } else if (a.kept) {                                                                     \
+      auto* k = hybrid_decode_kernel<GG, 1, HybridArgsMT>;                                   \
+      e = ensure_dyn_smem((const void*)k, smem);                                             \
+      if (e != cudaSuccess) return e;                                                        \
+      e = launch_pdl(k, grid, block, smem, s, mt);                                           \
     } else {                                                                                 \
-      auto* k = hybrid_decode_kernel<GG, false, HybridArgs>;                                 \
+      auto* k = hybrid_decode_kernel<GG, 0, HybridArgs>;                                     \
       e = ensure_dyn_smem((const void*)k, smem);                                             \
       if (e != cudaSuccess) return e;                                                        \
       e = launch_pdl(k, grid, block, smem, s, plain);                                        \
@@ -558,11 +582,13 @@ __global__ void append_kernel(AppendArgs a) {
   const int pg = len / a.page;
   const bool fits = len >= 0 && len < a.vcap && pg < a.page_cap && row >= 0 && row < a.cap;
   if (fits) {
+    const int blk = a.pm.table ? paged_block(a.pm, u, len, a.status) : 0;
     for (int g = 0; g < a.n_kv; ++g) {
       const size_t ukv = (size_t)u * a.n_kv + g;
       const bf16 kval = a.new_k[ukv * kHeadDim + c];
-      a.k_cache[(ukv * a.cap + row) * kHeadDim + c] = kval;
-      a.v_cache[(ukv * a.cap + row) * kHeadDim + c] = a.new_v[ukv * kHeadDim + c];
+      const size_t dst = a.pm.table ? paged_row(a.pm, blk, a.n_kv, g, len) : ukv * a.cap + row;
+      a.k_cache[dst * kHeadDim + c] = kval;
+      a.v_cache[dst * kHeadDim + c] = a.new_v[ukv * kHeadDim + c];
       if (a.kept && c == 0) a.kept[ukv * a.vcap + len] = row;
       const size_t si = (ukv * kHeadDim + c) * a.page_cap + pg;
       if (len % a.page == 0) {
@@ -618,17 +644,22 @@ __global__ void __launch_bounds__(256) summaries_kernel(SummaryArgs a) {
   const int first_page = a.first_token / PG;
   if (pg0 >= P || pg0 + kSumPages <= first_page) return;
   const int c = threadIdx.x & 15, pl = threadIdx.x >> 4;
-  const uint4* kc = reinterpret_cast<const uint4*>(a.k_cache + (size_t)ukv * a.cap * kHeadDim);
+  const bool paged = a.pm.table != nullptr;
+  const int g = ukv - u * a.n_kv;
+  const uint4* kc = reinterpret_cast<const uint4*>(
+      paged ? a.k_cache : a.k_cache + (size_t)ukv * a.cap * kHeadDim);
   const int32_t* kept = a.kept ? a.kept + (size_t)ukv * a.vcap : nullptr;
-  // cache row of sequence token t: itself, or its kept index (checked; row 0 if out of range)
-  auto row_of = [&](int t) -> int {
-    if (!kept) return t;
+  // row (from kc) of sequence token t: itself, its kept index or its page's row (checked; row 0
+  // of the unit, or block 0, if out of range)
+  auto row_of = [&](int t) -> size_t {
+    if (paged) return paged_row(a.pm, paged_block(a.pm, u, t, a.status), a.n_kv, g, t);
+    if (!kept) return (size_t)t;
     const int r = kept[t];
     if (r < 0 || r >= a.cap) {
       set_status(a.status, RKV_DEV_BAD_INDEX);
       return 0;
     }
-    return r;
+    return (size_t)r;
   };
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -645,12 +676,12 @@ __global__ void __launch_bounds__(256) summaries_kernel(SummaryArgs a) {
 #pragma unroll
       for (int r0 = 0; r0 < PG; r0 += kB) {
         uint4 x[kB];
-        int rw[kB];
+        size_t rw[kB];
 #pragma unroll
         for (int b = 0; b < kB; ++b) rw[b] = (r0 + b < nt) ? row_of(t0 + r0 + b) : 0;
 #pragma unroll
         for (int b = 0; b < kB; ++b)
-          if (r0 + b < nt) x[b] = kc[(size_t)rw[b] * (kHeadDim / 8) + c];
+          if (r0 + b < nt) x[b] = kc[rw[b] * (kHeadDim / 8) + c];
 #pragma unroll
         for (int b = 0; b < kB; ++b) {
           if (r0 + b < nt) {

@@ -47,6 +47,23 @@ struct HybridArgsMT : HybridArgs {
   int vcap;
 };
 
+// Paged K/V cache: k_cache / v_cache are pools [num_blocks][n_kv][block][128]; token t of unit u
+// (every K/V head g) lives in block table[u * max_blocks + t / block], row t % block. A table
+// entry outside [0, num_blocks) is reported (RKV_DEV_BAD_INDEX) and block 0 used instead.
+struct PagedMap {
+  const int32_t* table;
+  int max_blocks, block, num_blocks;
+};
+
+struct HybridArgsPaged : HybridArgs {
+  PagedMap pm;
+};
+
+// Launch-side view of every decode variant (only the fields of the chosen one are read).
+struct HybridArgsAll : HybridArgsMT {
+  PagedMap pm;
+};
+
 // Appends token `len` of every unit. With `kept` set, the row goes to row full_len[u] of the
 // full cache and kept[ukv][len] = full_len[u]; both counters advance.
 struct AppendArgs {
@@ -59,6 +76,7 @@ struct AppendArgs {
   bf16* kmax;
   int32_t* kept;
   int32_t* full_len;
+  PagedMap pm;  // table == nullptr: not paged
   int n, n_kv, cap, vcap, page_cap, page;
   uint32_t* status;
 };
@@ -69,6 +87,7 @@ struct SummaryArgs {
   const bf16* k_cache;
   const int32_t* len;
   const int32_t* kept;
+  PagedMap pm;  // table == nullptr: not paged
   bf16* kmin;
   bf16* kmax;
   int n, n_kv, cap, vcap, page, page_cap, first_token;
@@ -98,7 +117,7 @@ void dense_plan(int n, int n_kv, int max_len, int* nsplit, int* tokens_per_split
 size_t dense_partials_bytes(int n, int n_kv, int gqa, int max_len);
 
 size_t hybrid_smem_bytes(int gqa, int page_cap, int budget, int page);
-cudaError_t launch_hybrid(const HybridArgsMT& a, cudaStream_t s);
+cudaError_t launch_hybrid(const HybridArgsAll& a, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_summaries(const SummaryArgs& a, cudaStream_t s);
 cudaError_t launch_dense(const DenseArgs& a, cudaStream_t s);
@@ -121,6 +140,7 @@ struct SnapArgs {
   float* nlse;         // workspace: [n*n_kv][rows_pad] merged negated log2-sum-exp per row
   int nsplit, tokens_per_split, rows_pad;
   int kv_div;  // units per K/V head: 1, or gqa when every query head is its own unit
+  PagedMap out_pm;  // table != nullptr: k_out / v_out are pools and rows go through the table
   uint32_t* status;
 };
 

@@ -756,27 +756,36 @@ __global__ void __launch_bounds__(256) gather_kernel(SnapArgs a) {
   const size_t src_unit = (size_t)(ukv / a.kv_div);
   const uint4* ksrc = reinterpret_cast<const uint4*>(a.k + src_unit * a.max_len * kHeadDim);
   const uint4* vsrc = reinterpret_cast<const uint4*>(a.v + src_unit * a.max_len * kHeadDim);
-  uint4* kdst = reinterpret_cast<uint4*>(a.k_out + (size_t)ukv * a.cap * kHeadDim);
-  uint4* vdst = reinterpret_cast<uint4*>(a.v_out + (size_t)ukv * a.cap * kHeadDim);
+  // destination: the unit's rows of k_out / v_out, or (paged) its pages in the pools
+  const bool paged = a.out_pm.table != nullptr;
+  const int g = ukv - u * a.n_kv;
+  uint4* kdst = reinterpret_cast<uint4*>(paged ? a.k_out : a.k_out + (size_t)ukv * a.cap * kHeadDim);
+  uint4* vdst = reinterpret_cast<uint4*>(paged ? a.v_out : a.v_out + (size_t)ukv * a.cap * kHeadDim);
   uint4 kv[4], vv[4];
-  int dst[4];
+  size_t dst[4];
+  bool ok[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int idx = threadIdx.x + 256 * i;  // 64 rows x 16 chunks
     const int row = row0 + (idx >> 4), ch = idx & 15;
-    dst[i] = -1;
+    ok[i] = false;
+    dst[i] = 0;
     if (row < cnt) {
       const int src = kept[row];
       if (src >= 0 && src < L) {
         kv[i] = ksrc[(size_t)src * 16 + ch];
         vv[i] = vsrc[(size_t)src * 16 + ch];
-        dst[i] = row * 16 + ch;
+        const size_t r = paged ? paged_row(a.out_pm, paged_block(a.out_pm, u, row, a.status),
+                                           a.n_kv, g, row)
+                               : (size_t)row;
+        dst[i] = r * 16 + ch;
+        ok[i] = true;
       }
     }
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    if (dst[i] >= 0) {
+    if (ok[i]) {
       kdst[dst[i]] = kv[i];
       vdst[dst[i]] = vv[i];
     }

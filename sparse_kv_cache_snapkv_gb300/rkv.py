@@ -31,6 +31,7 @@ SYMBOLS = [
     "rkv_dense_decode_workspace_bytes", "rkv_dense_decode", "rkv_dense_decode_noalloc",
     "rkv_build_page_summaries_mt", "rkv_hybrid_decode_mt", "rkv_plan_even_split",
     "rkv_snapkv_per_head_workspace_bytes", "rkv_snapkv_compress_per_head",
+    "rkv_snapkv_compress_paged", "rkv_build_page_summaries_paged", "rkv_hybrid_decode_paged",
 ]
 
 
@@ -83,6 +84,14 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         "rkv_snapkv_per_head_workspace_bytes": ([i32, i32, i32, i32, i32], sz),
         "rkv_snapkv_compress_per_head": ([vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
                                           f32, vp, vp, i32, vp, vp, vp, vp, sz, vp], i32),
+        "rkv_snapkv_compress_paged": ([vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
+                                       f32, vp, vp, i32, i32, vp, i32, vp, vp, vp, vp, sz, vp],
+                                      i32),
+        "rkv_build_page_summaries_paged": ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
+                                            i32, vp, vp, vp, sz, vp], i32),
+        "rkv_hybrid_decode_paged": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                     i32, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, sz,
+                                     vp], i32),
         "rkv_build_page_summaries_mt": ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp,
                                          vp, vp, sz, vp], i32),
         "rkv_hybrid_decode_mt": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
@@ -291,6 +300,67 @@ def rkv_hybrid_decode_mt(q, k_full, v_full, full_len, kept_idx, kept_len, kmin, 
         page_cap, budget, page, channels, float(scale), _ptr(out), _ptr(sel_channels),
         _ptr(sel_pages), _ptr(approx_scores), _ptr(ws), ws.numel(), _stream(stream))
     _check("rkv_hybrid_decode_mt", code)
+    return ws
+
+
+# ------------------------------------------------------------------------------- paged cache
+def rkv_snapkv_compress_paged(k, v, seq_lens, q_win, kernel_size: int, keep: int, scale: float,
+                              k_pool, v_pool, block_table, kept_idx, out_len, scores_out=None,
+                              ws=None, stream=None):
+    """SnapKV++ compression whose kept rows go to the pools through the block table."""
+    _bf16(k, "k"), _bf16(k_pool, "k_pool"), _i32(block_table, "block_table")
+    _i32(kept_idx, "kept_idx"), _i32(out_len, "out_len"), _i32(seq_lens, "seq_lens")
+    n, n_kv, max_len, d = k.shape
+    hq, window = q_win.shape[1], q_win.shape[2]
+    gqa = hq // n_kv
+    num_blocks, _, block, _ = k_pool.shape
+    max_blocks = block_table.shape[-1]
+    if ws is None:
+        ws = workspace(rkv_snapkv_workspace_bytes(n, n_kv, gqa, max_len, window), k.device)
+    code = load().rkv_snapkv_compress_paged(
+        _ptr(k), _ptr(v), _ptr(seq_lens), _ptr(q_win), n, n_kv, gqa, d, max_len, window,
+        kernel_size, keep, float(scale), _ptr(k_pool), _ptr(v_pool), num_blocks, block,
+        _ptr(block_table), max_blocks, _ptr(kept_idx), _ptr(out_len), _ptr(scores_out), _ptr(ws),
+        ws.numel(), _stream(stream))
+    _check("rkv_snapkv_compress_paged", code)
+    return ws
+
+
+def rkv_build_page_summaries_paged(k_pool, block_table, length, page: int, kmin, kmax,
+                                   first_token: int = 0, ws=None, stream=None):
+    _bf16(k_pool, "k_pool"), _i32(block_table, "block_table"), _i32(length, "len")
+    num_blocks, n_kv, block, d = k_pool.shape
+    n, max_blocks = block_table.shape
+    page_cap = kmin.shape[-1]
+    if ws is None:
+        ws = workspace(STATUS_BYTES, k_pool.device)
+    code = load().rkv_build_page_summaries_paged(
+        _ptr(k_pool), _ptr(block_table), _ptr(length), n, n_kv, d, num_blocks, block, max_blocks,
+        page, page_cap, first_token, _ptr(kmin), _ptr(kmax), _ptr(ws), ws.numel(),
+        _stream(stream))
+    _check("rkv_build_page_summaries_paged", code)
+    return ws
+
+
+def rkv_hybrid_decode_paged(q, k_pool, v_pool, block_table, length, kmin, kmax, budget: int,
+                            page: int, channels: int, scale: float, out, new_k=None, new_v=None,
+                            sel_channels=None, sel_pages=None, approx_scores=None, ws=None,
+                            stream=None):
+    """One hybrid decode step over a paged cache (appending new_k / new_v first if given)."""
+    _bf16(q, "q"), _bf16(k_pool, "k_pool"), _i32(block_table, "block_table"), _i32(length, "len")
+    num_blocks, n_kv, block, d = k_pool.shape
+    n, max_blocks = block_table.shape
+    gqa = q.shape[1] // n_kv
+    page_cap = kmin.shape[-1]
+    if ws is None:
+        ws = workspace(rkv_hybrid_decode_workspace_bytes(n, n_kv, gqa, page_cap, budget, page),
+                       q.device)
+    code = load().rkv_hybrid_decode_paged(
+        _ptr(q), _ptr(new_k), _ptr(new_v), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+        _ptr(length), _ptr(kmin), _ptr(kmax), n, n_kv, gqa, d, num_blocks, block, max_blocks,
+        page_cap, budget, page, channels, float(scale), _ptr(out), _ptr(sel_channels),
+        _ptr(sel_pages), _ptr(approx_scores), _ptr(ws), ws.numel(), _stream(stream))
+    _check("rkv_hybrid_decode_paged", code)
     return ws
 
 

@@ -460,3 +460,31 @@ def test_per_head_scores_sum_to_group_scores():
         assert np.array_equal(kept[-W:], np.arange(L - W, L)) and np.array_equal(kc, k[kept])
     # heads that look at different parts of the prompt keep different tokens
     assert not all(np.array_equal(res[0][0], r[0]) for r in res[1:])
+
+
+# ---------------------------------------------------------------- paged cache (R20)
+def test_paged_round_trip_and_decode():
+    rng = np.random.default_rng(21)
+    L, d, n_kv, block, B, p = 700, 16, 2, 64, 128, 4
+    kc = _bf16_values((n_kv, L, d), rng)
+    vc = _bf16_values((n_kv, L, d), rng)
+    nb = (L + block - 1) // block
+    table = rng.permutation(3 * nb)[:nb]              # scattered, non-contiguous blocks
+    kp = np.full((3 * nb, n_kv, block, d), np.nan)
+    vp = np.full_like(kp, np.nan)
+    for g in range(n_kv):
+        O.paged_scatter(kp, table, kc[g], g)
+        O.paged_scatter(vp, table, vc[g], g)
+        assert np.array_equal(O.paged_view(kp, table, L, g), kc[g])
+    # token 65 with blocks of 64 is row 1 of the table's second block; token 699 row 59 of the
+    # eleventh
+    assert np.array_equal(kp[table[1], 1, 1], kc[1, 65])
+    assert np.array_equal(kp[table[10], 0, 59], kc[0, 699])
+    q = _bf16_values((4, d), rng)
+    kv0 = O.paged_view(kp, table, L, 1)
+    kmin, kmax = O.page_summaries(kv0, L, p)
+    r = O.hybrid_decode(q, kv0, O.paged_view(vp, table, L, 1), L, kmin, kmax, B, p, 8, 0.2)
+    k1min, k1max = O.page_summaries(kc[1], L, p)
+    r1 = O.hybrid_decode(q, kc[1], vc[1], L, k1min, k1max, B, p, 8, 0.2)
+    assert np.array_equal(r["tokens"], r1["tokens"])
+    np.testing.assert_array_equal(r["out"], r1["out"])
