@@ -2,8 +2,8 @@
 """Benchmark of the RocketKV hot path on GB300: decode steps/s of one full pass per step.
 
 One step = one pass of the whole hot path over one batch of synthetic input:
-  SnapKV++ compression of every (layer, KV head) of the prompt  (score passes, select, gather)
-  + page summaries of the compact cache
+  SnapKV++ compression of every (layer, KV head) of the prompt  (score passes, select, gather;
+    the gather also builds the page summaries of the compact cache)
   + `decode_steps` hybrid sparse decode steps (each one launch over all layers and KV heads).
 Default workload: Llama-3.1-8B attention shapes (32 layers, 32 query / 8 KV heads, d 128, bf16),
 batch 1, 32K prompt, window 32, pooling 15, budget 256 (page 4, 32 of 128 channels, keep 4096),
@@ -265,9 +265,14 @@ def run_ours(args):
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
     graphs = []
+    # the summaries phase is empty when the compression builds them and nothing is appended
+    sum_empty = hp.fuse_summaries and not wl.append
     with torch.cuda.stream(stream):
-        for fn in (hp.compress, hp.summaries,
+        for fn in (hp.compress, None if sum_empty else hp.summaries,
                    lambda: [hp.decode(t) for t in range(wl.decode_steps)]):
+            if fn is None:
+                graphs.append(None)
+                continue
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 fn()
@@ -277,7 +282,8 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             for g in graphs:
-                g.replay()
+                if g is not None:
+                    g.replay()
         torch.cuda.synchronize()
         hp.check_status()
         barrier(world)
@@ -291,7 +297,8 @@ def run_ours(args):
             ev[i][0].record(stream)
             graphs[0].replay()
             ev[i][1].record(stream)
-            graphs[1].replay()
+            if graphs[1] is not None:
+                graphs[1].replay()
             ev[i][2].record(stream)
             graphs[2].replay()
             ev[i][3].record(stream)

@@ -123,6 +123,21 @@ rkv_status rkv_snapkv_compress(const void* k, const void* v, const int32_t* seq_
                                int32_t* out_len, float* scores_out, void* ws, size_t ws_bytes,
                                void* stream);
 
+/* rkv_snapkv_compress followed by rkv_build_page_summaries(k_out, out_len, page, page_cap,
+ * first_token = 0, kmin, kmax) in one pass: the gather builds the page summaries of the rows it
+ * writes ([APPROX]), so the compact cache is not read back. Same outputs, bit for bit. page a
+ * power of two <= 64; page_cap a multiple of 8 with page_cap * page >= keep; kmin, kmax
+ * [n][n_kv][128][page_cap] bf16 (pages past ceil(out_len[u] / page) untouched). Workspace:
+ * rkv_snapkv_workspace_bytes. */
+rkv_status rkv_snapkv_compress_summarized(const void* k, const void* v,
+                                          const int32_t* seq_lens, const void* q_win, int n,
+                                          int n_kv, int gqa, int head_dim, int max_len,
+                                          int window, int kernel_size, int keep, float scale,
+                                          void* k_out, void* v_out, int cap, int32_t* kept_idx,
+                                          int32_t* out_len, float* scores_out, int page,
+                                          int page_cap, void* kmin, void* kmax, void* ws,
+                                          size_t ws_bytes, void* stream);
+
 /* The ablation without the GQA enhancement ([SNAP++], [KEYPTS] "original SnapKV"): every query
  * head is scored and filtered on its own -- its W window rows only, no sum over the group -- and
  * keeps its own copy of the selected rows of its K/V head h / gqa. Same arguments as

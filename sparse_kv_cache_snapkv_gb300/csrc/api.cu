@@ -131,7 +131,9 @@ static rkv_status snapkv_impl(const void* k, const void* v, const int32_t* seq_l
                               int max_len, int window, int kernel_size, int keep, float scale,
                               void* k_out, void* v_out, int cap, int32_t* kept_idx,
                               int32_t* out_len, float* scores_out, void* ws, size_t ws_bytes,
-                              void* stream, bool per_head, const PagedMap& out_pm) {
+                              void* stream, bool per_head, const PagedMap& out_pm,
+                              int page = 0, int page_cap = 0, void* kmin = nullptr,
+                              void* kmax = nullptr) {
   if (head_dim != kHeadDim) return RKV_ERR_UNSUPPORTED;
   if (!k || !v || !seq_lens || !q_win || !k_out || !v_out || !kept_idx || !out_len)
     return RKV_ERR_INVALID_ARG;
@@ -142,6 +144,11 @@ static rkv_status snapkv_impl(const void* k, const void* v, const int32_t* seq_l
       keep > cap || cap <= 0 || !(scale > 0.f) || !std::isfinite(scale))
     return RKV_ERR_INVALID_ARG;
   if (kernel_size < 0 || (kernel_size > 0 && kernel_size % 2 == 0)) return RKV_ERR_INVALID_ARG;
+  if (kmin || kmax) {  // page summaries built by the gather
+    if (!kmin || !kmax || !aligned16(kmin) || !aligned16(kmax) || !pow2(page) || page > 64 ||
+        page_cap <= 0 || page_cap % 8 != 0 || (keep + page - 1) / page > page_cap)
+      return RKV_ERR_INVALID_ARG;
+  }
   const int kv_div = per_head ? gqa : 1;
   if (per_head) {  // the kernels see n_kv * gqa units of one query head each
     n_kv *= gqa;
@@ -161,6 +168,10 @@ static rkv_status snapkv_impl(const void* k, const void* v, const int32_t* seq_l
   a.gqa = gqa;
   a.kv_div = kv_div;
   a.out_pm = out_pm;
+  a.kmin = static_cast<bf16*>(kmin);
+  a.kmax = static_cast<bf16*>(kmax);
+  a.page = page;
+  a.page_cap = page_cap;
   a.max_len = max_len;
   a.window = window;
   a.kernel_size = kernel_size;
@@ -199,6 +210,20 @@ rkv_status rkv_snapkv_compress(const void* k, const void* v, const int32_t* seq_
   return snapkv_impl(k, v, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window,
                      kernel_size, keep, scale, k_out, v_out, cap, kept_idx, out_len, scores_out,
                      ws, ws_bytes, stream, false, PagedMap{});
+}
+
+rkv_status rkv_snapkv_compress_summarized(const void* k, const void* v,
+                                          const int32_t* seq_lens, const void* q_win, int n,
+                                          int n_kv, int gqa, int head_dim, int max_len,
+                                          int window, int kernel_size, int keep, float scale,
+                                          void* k_out, void* v_out, int cap, int32_t* kept_idx,
+                                          int32_t* out_len, float* scores_out, int page,
+                                          int page_cap, void* kmin, void* kmax, void* ws,
+                                          size_t ws_bytes, void* stream) {
+  if (!kmin || !kmax) return RKV_ERR_INVALID_ARG;
+  return snapkv_impl(k, v, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window,
+                     kernel_size, keep, scale, k_out, v_out, cap, kept_idx, out_len, scores_out,
+                     ws, ws_bytes, stream, false, PagedMap{}, page, page_cap, kmin, kmax);
 }
 
 size_t rkv_snapkv_per_head_workspace_bytes(int n, int n_kv, int gqa, int max_len, int window) {

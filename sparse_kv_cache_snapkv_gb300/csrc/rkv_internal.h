@@ -141,6 +141,9 @@ struct SnapArgs {
   int nsplit, tokens_per_split, rows_pad;
   int kv_div;  // units per K/V head: 1, or gqa when every query head is its own unit
   PagedMap out_pm;  // table != nullptr: k_out / v_out are pools and rows go through the table
+  bf16* kmin;       // != nullptr: page summaries of the compact cache, built by the gather
+  bf16* kmax;
+  int page, page_cap;
   uint32_t* status;
 };
 

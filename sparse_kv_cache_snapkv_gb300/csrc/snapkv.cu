@@ -744,7 +744,89 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_fast_kernel(SnapArgs a)
 // compaction gather: CTA = 64 kept rows of one (unit, KV head); each thread copies 16-byte
 // chunks of K and V rows
 // ------------------------------------------------------------------------------------------
+// Page summaries of rows row0 .. min(cnt, row0 + 64) - 1 of a unit's compact cache, from the
+// rows this CTA holds (kv[i] = row row0 + (tid >> 4) + 16 i, chunk tid & 15, valid where ok[i]).
+__device__ __forceinline__ void gather_summaries(const SnapArgs& a, int ukv, int row0, int cnt,
+                                                 const uint4 (&kv)[4], const bool (&ok)[4],
+                                                 uint4* gsm) {
+  const int tid = threadIdx.x, p = a.page;
+  uint4* srow = gsm;                        // [64][16]
+  uint4* smin = gsm + 64 * 16;              // [64 / p][16]
+  uint4* smax = smin + (64 / p) * 16;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (ok[i]) srow[((tid >> 4) + 16 * i) * 16 + (tid & 15)] = kv[i];
+  __syncthreads();
+  const int nrows = min(64, cnt - row0);
+  const int npg = (nrows + p - 1) / p;      // pages (the last may be partial)
+  const __nv_bfloat162 pinf = __halves2bfloat162(__ushort_as_bfloat16(0x7F80),
+                                                 __ushort_as_bfloat16(0x7F80));
+  const __nv_bfloat162 ninf = __halves2bfloat162(__ushort_as_bfloat16(0xFF80),
+                                                 __ushort_as_bfloat16(0xFF80));
+  for (int it = tid; it < npg * 16; it += 256) {
+    const int j = it >> 4, c = it & 15;
+    const int r1 = min(nrows, (j + 1) * p);
+    __nv_bfloat162 mn[4] = {pinf, pinf, pinf, pinf}, mx[4] = {ninf, ninf, ninf, ninf};
+    for (int r = j * p; r < r1; ++r) {
+      const uint4 x = srow[r * 16 + c];
+      const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        mn[e] = __hmin2(mn[e], y[e]);
+        mx[e] = __hmax2(mx[e], y[e]);
+      }
+    }
+    smin[j * 16 + c] = *reinterpret_cast<const uint4*>(mn);
+    smax[j * 16 + c] = *reinterpret_cast<const uint4*>(mx);
+  }
+  __syncthreads();
+  // channel-major rows: thread -> (channel, group of 8 pages)
+  const int pg0 = row0 / p;
+  const int ngrp = (npg + 7) / 8;
+  const uint16_t* smin16 = reinterpret_cast<const uint16_t*>(smin);
+  const uint16_t* smax16 = reinterpret_cast<const uint16_t*>(smax);
+  uint16_t* kmin16 = reinterpret_cast<uint16_t*>(a.kmin);
+  uint16_t* kmax16 = reinterpret_cast<uint16_t*>(a.kmax);
+  for (int it = tid; it < kHeadDim * ngrp; it += 256) {
+    const int ch = it / ngrp, j0 = (it - ch * ngrp) * 8;
+    const size_t row = ((size_t)ukv * kHeadDim + ch) * a.page_cap + pg0 + j0;
+    uint16_t vmin[8], vmax[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int j = min(j0 + t, npg - 1);
+      vmin[t] = smin16[j * kHeadDim + ch];
+      vmax[t] = smax16[j * kHeadDim + ch];
+    }
+    if (j0 + 8 <= npg && (pg0 & 7) == 0) {
+      uint4 wmin, wmax;
+      wmin.x = vmin[0] | ((uint32_t)vmin[1] << 16);
+      wmin.y = vmin[2] | ((uint32_t)vmin[3] << 16);
+      wmin.z = vmin[4] | ((uint32_t)vmin[5] << 16);
+      wmin.w = vmin[6] | ((uint32_t)vmin[7] << 16);
+      wmax.x = vmax[0] | ((uint32_t)vmax[1] << 16);
+      wmax.y = vmax[2] | ((uint32_t)vmax[3] << 16);
+      wmax.z = vmax[4] | ((uint32_t)vmax[5] << 16);
+      wmax.w = vmax[6] | ((uint32_t)vmax[7] << 16);
+      *reinterpret_cast<uint4*>(kmin16 + row) = wmin;
+      *reinterpret_cast<uint4*>(kmax16 + row) = wmax;
+    } else {
+      for (int t = 0; t < 8 && j0 + t < npg; ++t) {
+        kmin16[row + t] = vmin[t];
+        kmax16[row + t] = vmax[t];
+      }
+    }
+  }
+}
+
+// With a.kmin set the gather also builds the page summaries of the rows it writes: its 64 rows
+// are whole pages (page | 64), staged in shared memory, reduced per (page, 16-byte chunk) and
+// written channel-major like summaries_kernel. Dynamic shared memory: gather_smem_bytes(page).
+size_t gather_smem_bytes(int page) {
+  return (size_t)64 * 256 + 2 * (size_t)(64 / page) * 256;
+}
+
 __global__ void __launch_bounds__(256) gather_kernel(SnapArgs a) {
+  extern __shared__ __align__(16) uint4 gsm[];
   const int ukv = blockIdx.y;
   const int u = ukv / a.n_kv;
   const int L = a.seq_lens[u];
@@ -790,6 +872,7 @@ __global__ void __launch_bounds__(256) gather_kernel(SnapArgs a) {
       vdst[dst[i]] = vv[i];
     }
   }
+  if (a.kmin) gather_summaries(a, ukv, row0, cnt, kv, ok, gsm);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -927,7 +1010,12 @@ cudaError_t launch_snapkv(const SnapArgs& a, cudaStream_t s) {
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  gather_kernel<<<dim3((a.keep + 63) / 64, units), 256, 0, s>>>(a);
+  const size_t gsmem = a.kmin ? gather_smem_bytes(a.page) : 0;
+  if (gsmem) {
+    e = ensure_dyn_smem((const void*)gather_kernel, gsmem);
+    if (e != cudaSuccess) return e;
+  }
+  gather_kernel<<<dim3((a.keep + 63) / 64, units), 256, gsmem, s>>>(a);
   return cudaGetLastError();
 }
 

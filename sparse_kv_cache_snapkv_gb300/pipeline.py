@@ -19,8 +19,9 @@ D = 128
 
 class HotPath:
     def __init__(self, wl: Workload, k, v, q_win, seq_lens, dec_q, new_k=None, new_v=None,
-                 scale: float = 1.0 / math.sqrt(D)):
+                 scale: float = 1.0 / math.sqrt(D), fuse_summaries: bool = True):
         rkv.load()
+        self.fuse_summaries = fuse_summaries  # the gather builds the page summaries
         self.wl = wl
         self.k, self.v, self.q_win, self.seq_lens = k, v, q_win, seq_lens
         self.dec_q = dec_q            # [steps, n, Hq, d]
@@ -50,9 +51,15 @@ class HotPath:
 
     # individual phases ------------------------------------------------------------------
     def compress(self):
-        rkv.rkv_snapkv_compress(self.k, self.v, self.seq_lens, self.q_win, self.wl.kernel,
-                                self.keep, self.scale, self.k_out, self.v_out, self.kept,
-                                self.out_len, ws=self.ws_snap)
+        if self.fuse_summaries:
+            rkv.rkv_snapkv_compress_summarized(self.k, self.v, self.seq_lens, self.q_win,
+                                               self.wl.kernel, self.keep, self.scale, self.k_out,
+                                               self.v_out, self.kept, self.out_len, self.page,
+                                               self.kmin, self.kmax, ws=self.ws_snap)
+        else:
+            rkv.rkv_snapkv_compress(self.k, self.v, self.seq_lens, self.q_win, self.wl.kernel,
+                                    self.keep, self.scale, self.k_out, self.v_out, self.kept,
+                                    self.out_len, ws=self.ws_snap)
 
     def summaries(self):
         # The decode-time length starts at the stage-1 length. With appends it grows, so it
@@ -61,8 +68,9 @@ class HotPath:
             self.length.copy_(self.out_len)
         else:
             self.length = self.out_len
-        rkv.rkv_build_page_summaries(self.k_out, self.length, self.page, self.kmin, self.kmax,
-                                     ws=self.ws_sum)
+        if not self.fuse_summaries:
+            rkv.rkv_build_page_summaries(self.k_out, self.length, self.page, self.kmin,
+                                         self.kmax, ws=self.ws_sum)
 
     def decode(self, t: int):
         nk = self.new_k[t] if self.new_k is not None else None
@@ -84,10 +92,11 @@ class HotPath:
     # accounting ---------------------------------------------------------------------------
     def launches_per_step(self) -> int:
         """Kernel launches of one step: compression = score pass 1, LSE merge, score pass 2,
-        select, gather; then the summaries; then one decode launch per step (two with appends:
-        the append kernel and the decode)."""
+        select, gather (which also builds the page summaries unless fuse_summaries is off: then
+        one summaries launch more); then one decode launch per step (two with appends: the
+        append kernel and the decode)."""
         per_decode = 2 if self.wl.append else 1
-        return 5 + 1 + per_decode * self.dec_q.shape[0]
+        return 5 + (0 if self.fuse_summaries else 1) + per_decode * self.dec_q.shape[0]
 
     def decode_bytes_per_launch(self) -> int:
         """Algorithmic HBM bytes of one hybrid decode launch (all units), budget-implied:
@@ -100,10 +109,12 @@ class HotPath:
 
     def compress_bytes(self) -> int:
         """Algorithmic bytes of one compression: K read once, V rows of kept tokens read, kept
-        K / V rows written, window queries read."""
+        K / V rows written, window queries read; with fused summaries also Kmin / Kmax written."""
         wl = self.wl
         units = wl.n * wl.n_kv
-        return units * (wl.max_len * D * 2 + 3 * self.keep * D * 2) + wl.n * wl.n_q * wl.window * D * 2
+        summaries = 2 * D * (-(-self.keep // self.page)) * 2 if self.fuse_summaries else 0
+        return (units * (wl.max_len * D * 2 + 3 * self.keep * D * 2 + summaries)
+                + wl.n * wl.n_q * wl.window * D * 2)
 
     def compress_flops(self) -> int:
         """Tensor-core flops of the two score passes (2 GEMMs of (G*W) x L x d per unit)."""

@@ -32,6 +32,7 @@ SYMBOLS = [
     "rkv_build_page_summaries_mt", "rkv_hybrid_decode_mt", "rkv_plan_even_split",
     "rkv_snapkv_per_head_workspace_bytes", "rkv_snapkv_compress_per_head",
     "rkv_snapkv_compress_paged", "rkv_build_page_summaries_paged", "rkv_hybrid_decode_paged",
+    "rkv_snapkv_compress_summarized",
 ]
 
 
@@ -84,6 +85,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         "rkv_snapkv_per_head_workspace_bytes": ([i32, i32, i32, i32, i32], sz),
         "rkv_snapkv_compress_per_head": ([vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
                                           f32, vp, vp, i32, vp, vp, vp, vp, sz, vp], i32),
+        "rkv_snapkv_compress_summarized": ([vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                            i32, f32, vp, vp, i32, vp, vp, vp, i32, i32, vp, vp,
+                                            vp, sz, vp], i32),
         "rkv_snapkv_compress_paged": ([vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
                                        f32, vp, vp, i32, i32, vp, i32, vp, vp, vp, vp, sz, vp],
                                       i32),
@@ -220,6 +224,28 @@ def rkv_snapkv_compress_per_head(k, v, seq_lens, q_win, kernel_size: int, keep: 
         kernel_size, keep, float(scale), _ptr(k_out), _ptr(v_out), cap, _ptr(kept_idx),
         _ptr(out_len), _ptr(scores_out), _ptr(ws), ws.numel(), _stream(stream))
     _check("rkv_snapkv_compress_per_head", code)
+    return ws
+
+
+def rkv_snapkv_compress_summarized(k, v, seq_lens, q_win, kernel_size: int, keep: int,
+                                   scale: float, k_out, v_out, kept_idx, out_len, page: int,
+                                   kmin, kmax, scores_out=None, ws=None, stream=None):
+    """rkv_snapkv_compress + page summaries of the compact cache in one pass."""
+    _bf16(k, "k"), _bf16(v, "v"), _bf16(q_win, "q_win"), _i32(seq_lens, "seq_lens")
+    _i32(kept_idx, "kept_idx"), _i32(out_len, "out_len"), _bf16(kmin, "kmin")
+    n, n_kv, max_len, d = k.shape
+    hq, window = q_win.shape[1], q_win.shape[2]
+    gqa = hq // n_kv
+    cap = k_out.shape[2]
+    page_cap = kmin.shape[-1]
+    if ws is None:
+        ws = workspace(rkv_snapkv_workspace_bytes(n, n_kv, gqa, max_len, window), k.device)
+    code = load().rkv_snapkv_compress_summarized(
+        _ptr(k), _ptr(v), _ptr(seq_lens), _ptr(q_win), n, n_kv, gqa, d, max_len, window,
+        kernel_size, keep, float(scale), _ptr(k_out), _ptr(v_out), cap, _ptr(kept_idx),
+        _ptr(out_len), _ptr(scores_out), page, page_cap, _ptr(kmin), _ptr(kmax), _ptr(ws),
+        ws.numel(), _stream(stream))
+    _check("rkv_snapkv_compress_summarized", code)
     return ws
 
 

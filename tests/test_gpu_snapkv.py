@@ -175,6 +175,43 @@ def test_snapkv_per_head_without_group_sum():
     assert not torch.equal(kept[0, 0], kept[0, 1])
 
 
+@pytest.mark.parametrize("page", [1, 4, 16, 64])
+def test_snapkv_summarized_equals_separate_summaries(page):
+    # the gather's page summaries equal compress + rkv_build_page_summaries bit for bit: ragged
+    # lengths (partial last pages), one prompt shorter than keep, one shorter than the window
+    rkv = _lib()
+    wl, x = _inputs(4, 2, 4, [5000, 3001, 1030, 20], 32, seed=109)
+    k, v, q, lens = x["k"], x["v"], x["q_win"], x["seq_lens"]
+    n, n_kv, max_len, _ = k.shape
+    keep = 1024
+    page_cap = ((keep + page - 1) // page + 7) // 8 * 8
+    scale = 1.0 / math.sqrt(D)
+    outs = []
+    for fused in (False, True):
+        k_out = torch.zeros(n, n_kv, keep, D, dtype=torch.bfloat16, device="cuda")
+        v_out = torch.zeros_like(k_out)
+        kept = torch.empty(n, n_kv, keep, dtype=torch.int32, device="cuda")
+        out_len = torch.empty(n, dtype=torch.int32, device="cuda")
+        kmin = torch.full((n, n_kv, D, page_cap), 7.0, dtype=torch.bfloat16, device="cuda")
+        kmax = torch.full_like(kmin, 7.0)
+        def status(ws):
+            try:
+                rkv.rkv_check_status(ws)
+            except rkv.RkvError as e:
+                assert e.bits == 0x2, e  # only the prompt shorter than the window is flagged
+
+        if fused:
+            status(rkv.rkv_snapkv_compress_summarized(k, v, lens, q, 7, keep, scale, k_out,
+                                                      v_out, kept, out_len, page, kmin, kmax))
+        else:
+            status(rkv.rkv_snapkv_compress(k, v, lens, q, 7, keep, scale, k_out, v_out, kept,
+                                           out_len))
+            status(rkv.rkv_build_page_summaries(k_out, out_len, page, kmin, kmax))
+        outs.append((k_out, kept, out_len, kmin, kmax))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
 def test_snapkv_multiple_waves():
     # 6 units of 64K tokens: K of all units exceeds one L2-sized wave, so several waves run
     rkv = _lib()
