@@ -1,11 +1,12 @@
 // Device-side building blocks shared by the RocketKV kernels (sm_103a).
 //
-//  * bf16 unpacking (exact widening to fp32)
-//  * mbarrier + cp.async.bulk wrappers (non-tensor bulk copies global -> shared), with waits
-//    bounded by the global timer so that no kernel can spin forever
-//  * block-wide exclusive scan
-//  * block-wide top-k radix select (largest keys first, ties -> lower index), emitting the
-//    selected indices in ascending order
+//  * paged-cache addressing, bf16 unpacking (exact widening to fp32)
+//  * mbarrier wrappers with waits bounded by the global timer, so that no kernel can spin
+//    forever; 16-byte cp.async copies; programmatic-dependent-launch controls
+//  * warp / block scans
+//  * top-k selects (largest keys first, ties -> lower index, indices emitted in ascending order):
+//    a general block radix select, a low-latency block select for <= NK * 256 keys, and a
+//    one-warp select for 128 keys
 #pragma once
 
 #include <cstdint>
@@ -121,16 +122,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait(a, parity)) return true;
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
-}
-
-// 1-D bulk copy global -> shared of `bytes` (multiple of 16, both addresses 16-byte aligned),
-// completing `bytes` transactions on `bar`.
-__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes,
-                                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(smem_addr(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
 }
 
 // 16-byte asynchronous global -> shared copies (LDGSTS). A thread waits for its own copies with

@@ -618,9 +618,10 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
 }
 
 // ==========================================================================================
-// Page summaries: CTA = (unit, KV head) x 32 pages. Reads rows coalesced (64 threads per
-// 256-byte row, bf16x2 each), reduces with exact bf16 min / max, transposes through shared
-// memory and writes 64-byte channel rows.
+// Page summaries: CTA = (unit, KV head) x 32 pages. Reads rows coalesced (16 threads per
+// 256-byte row, 16 bytes each), reduces with exact bf16 min / max, transposes through shared
+// memory and writes channel rows 8 pages (16 bytes) at a time. Rows come from the cache, a kept
+// list (RocketKV-MT) or a paged pool.
 // ==========================================================================================
 constexpr int kSumPages = 32;
 
@@ -765,7 +766,8 @@ cudaError_t launch_summaries(const SummaryArgs& a, cudaStream_t s) {
 
 // ==========================================================================================
 // Dense decode (flash-decoding split-K): CTA = (unit, KV head, split). Each split's tokens are
-// staged 64 rows at a time (one bulk copy per row) and consumed by the same MMA warp code;
+// staged 64 rows at a time (16-byte cp.async copies, two warp groups with one stage each) and
+// consumed by the same MMA warp code;
 // per-split partials are merged by a second kernel.
 // ==========================================================================================
 void dense_plan(int n, int n_kv, int max_len, int* nsplit, int* tokens_per_split) {
