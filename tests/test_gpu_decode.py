@@ -160,6 +160,12 @@ def test_hybrid_budget_page_channel_variants(budget, page, channels):
     _hybrid_case(2, 2, 4, [8191, 5000], 8192, budget, page, channels, seed=31 + page)
 
 
+def test_hybrid_more_than_4096_pages_general_select():
+    # 20,001 cached tokens in pages of 4 (5001 pages): the page select takes the general block
+    # select instead of the register-resident one (<= 4096 pages); a second unit stays below it
+    _hybrid_case(2, 1, 4, [20001, 3000], 20480, 512, 4, 32, seed=41, steps=1)
+
+
 def test_hybrid_page1_all_channels_is_exact_group_topk():
     # the reduction the method's approximation collapses to (exact group top-k attention)
     rkv = _lib()
