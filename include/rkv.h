@@ -123,6 +123,19 @@ rkv_status rkv_snapkv_compress(const void* k, const void* v, const int32_t* seq_
                                int32_t* out_len, float* scores_out, void* ws, size_t ws_bytes,
                                void* stream);
 
+/* rkv_snapkv_compress with average pooling in place of max pooling (a SnapKV pooling variant;
+ * the pages describe max pooling only): each prefix score is replaced by the mean of the scores
+ * over the in-range positions of its clipped window [max(0, i - r), min(n - 1, i + r)],
+ * r = kernel_size / 2, before the top-k. The window sums are exact (fixed point), so the result
+ * depends only on the fp32 scores. kernel_size odd in [1, 1048575], or 0 as above. Other
+ * arguments, outputs, workspace and errors as rkv_snapkv_compress. */
+rkv_status rkv_snapkv_compress_avg_pool(const void* k, const void* v, const int32_t* seq_lens,
+                                        const void* q_win, int n, int n_kv, int gqa,
+                                        int head_dim, int max_len, int window, int kernel_size,
+                                        int keep, float scale, void* k_out, void* v_out, int cap,
+                                        int32_t* kept_idx, int32_t* out_len, float* scores_out,
+                                        void* ws, size_t ws_bytes, void* stream);
+
 /* rkv_snapkv_compress followed by rkv_build_page_summaries(k_out, out_len, page, page_cap,
  * first_token = 0, kmin, kmax) in one pass: the gather builds the page summaries of the rows it
  * writes ([APPROX]), so the compact cache is not read back. Same outputs, bit for bit. page a

@@ -44,6 +44,8 @@ Readings taken where the pages leave a step open (each restated at its function)
       stage, stage 2's share split evenly between page size and channel reduction; the page is the
       power of two nearest R^(1/4) on a log2 scale (halves round up) within [1, min(64, B/2)],
       channels = round(d * page / sqrt(R)) within [1, d], keep as in R1.
+  R21 average pooling (an ablation variant; the pages describe max pooling only): the mean over
+      the in-range positions of the clipped window.
   R20 a paged (block-table) compact cache is a storage layout only: every step computes on the
       rows the table names, in token order, exactly as on the contiguous cache.
   R19 SnapKV without the GQA enhancement ([P1] "Key points": the ablation against "original
@@ -61,7 +63,7 @@ import math
 import numpy as np
 
 __all__ = [
-    "plan", "adaptive_kernel_size", "window_scores", "pool_max", "topk_desc",
+    "plan", "adaptive_kernel_size", "window_scores", "pool_max", "pool_avg", "topk_desc",
     "snapkv_compress", "page_summaries", "channel_pick", "approx_scores", "page_select",
     "attention", "dense_decode", "hybrid_decode", "group_topk_attention", "append_token",
     "kept_view", "mt_page_summaries", "mt_hybrid_decode", "mt_append_token",
@@ -170,6 +172,18 @@ def pool_max(x: np.ndarray, kernel: int) -> np.ndarray:
     return out
 
 
+def pool_avg(x: np.ndarray, kernel: int) -> np.ndarray:
+    """1-D average pooling, stride 1, same length: the mean over the in-range positions of the
+    window (reading R21; the pages describe max pooling only, this is the ablation variant)."""
+    assert kernel % 2 == 1 and kernel >= 1
+    r = kernel // 2
+    n = x.shape[0]
+    out = np.empty_like(x)
+    for i in range(n):
+        out[i] = x[max(0, i - r): min(n, i + r + 1)].mean()
+    return out
+
+
 def topk_desc(keys: np.ndarray, k: int) -> np.ndarray:
     """Indices of the k largest keys; equal keys -> lower index first (reading R5).
 
@@ -181,7 +195,7 @@ def topk_desc(keys: np.ndarray, k: int) -> np.ndarray:
 
 
 def snapkv_compress(k: np.ndarray, v: np.ndarray, q_win: np.ndarray, keep: int, kernel: int,
-                    scale: float):
+                    scale: float, pooling: str = "max"):
     """SnapKV++ for one (sequence, layer, KV head): score, pool, top-k, gather.
 
     [P3] "Is Needle Among Evicted Tokens": eviction is independent per head and per layer.
@@ -192,7 +206,7 @@ def snapkv_compress(k: np.ndarray, v: np.ndarray, q_win: np.ndarray, keep: int, 
     L = k.shape[0]
     W = q_win.shape[1]
     score = window_scores(k, q_win, scale)
-    pooled = pool_max(score, kernel)
+    pooled = pool_avg(score, kernel) if pooling == "avg" else pool_max(score, kernel)
     if keep >= L:
         kept = np.arange(L)
     else:

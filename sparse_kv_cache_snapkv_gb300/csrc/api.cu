@@ -49,6 +49,7 @@ inline uint32_t* status_ptr(void* ws) { return reinterpret_cast<uint32_t*>(ws); 
 inline rkv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA; }
 inline bool gqa_ok(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxAvgKernel = (1 << 20) - 1;  // keeps a fixed-point window sum below 2^60
 
 }  // namespace
 
@@ -133,7 +134,7 @@ static rkv_status snapkv_impl(const void* k, const void* v, const int32_t* seq_l
                               int32_t* out_len, float* scores_out, void* ws, size_t ws_bytes,
                               void* stream, bool per_head, const PagedMap& out_pm,
                               int page = 0, int page_cap = 0, void* kmin = nullptr,
-                              void* kmax = nullptr) {
+                              void* kmax = nullptr, bool pool_avg = false) {
   if (head_dim != kHeadDim) return RKV_ERR_UNSUPPORTED;
   if (!k || !v || !seq_lens || !q_win || !k_out || !v_out || !kept_idx || !out_len)
     return RKV_ERR_INVALID_ARG;
@@ -144,6 +145,7 @@ static rkv_status snapkv_impl(const void* k, const void* v, const int32_t* seq_l
       keep > cap || cap <= 0 || !(scale > 0.f) || !std::isfinite(scale))
     return RKV_ERR_INVALID_ARG;
   if (kernel_size < 0 || (kernel_size > 0 && kernel_size % 2 == 0)) return RKV_ERR_INVALID_ARG;
+  if (pool_avg && kernel_size > kMaxAvgKernel) return RKV_ERR_INVALID_ARG;
   if (kmin || kmax) {  // page summaries built by the gather
     if (!kmin || !kmax || !aligned16(kmin) || !aligned16(kmax) || !pow2(page) || page > 64 ||
         page_cap <= 0 || page_cap % 8 != 0 || (keep + page - 1) / page > page_cap)
@@ -175,6 +177,7 @@ static rkv_status snapkv_impl(const void* k, const void* v, const int32_t* seq_l
   a.max_len = max_len;
   a.window = window;
   a.kernel_size = kernel_size;
+  a.pool_avg = pool_avg ? 1 : 0;
   a.keep = keep;
   a.cap = cap;
   a.scale_log2 = scale * kLog2e;
@@ -210,6 +213,17 @@ rkv_status rkv_snapkv_compress(const void* k, const void* v, const int32_t* seq_
   return snapkv_impl(k, v, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window,
                      kernel_size, keep, scale, k_out, v_out, cap, kept_idx, out_len, scores_out,
                      ws, ws_bytes, stream, false, PagedMap{});
+}
+
+rkv_status rkv_snapkv_compress_avg_pool(const void* k, const void* v, const int32_t* seq_lens,
+                                        const void* q_win, int n, int n_kv, int gqa,
+                                        int head_dim, int max_len, int window, int kernel_size,
+                                        int keep, float scale, void* k_out, void* v_out, int cap,
+                                        int32_t* kept_idx, int32_t* out_len, float* scores_out,
+                                        void* ws, size_t ws_bytes, void* stream) {
+  return snapkv_impl(k, v, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window,
+                     kernel_size, keep, scale, k_out, v_out, cap, kept_idx, out_len, scores_out,
+                     ws, ws_bytes, stream, false, PagedMap{}, 0, 0, nullptr, nullptr, true);
 }
 
 rkv_status rkv_snapkv_compress_summarized(const void* k, const void* v,

@@ -144,6 +144,7 @@ struct SnapArgs {
   bf16* kmin;       // != nullptr: page summaries of the compact cache, built by the gather
   bf16* kmax;
   int page, page_cap;
+  int pool_avg;     // 1: average pooling over the clipped window instead of max pooling
   uint32_t* status;
 };
 

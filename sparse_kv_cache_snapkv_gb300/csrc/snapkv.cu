@@ -19,7 +19,8 @@
 // 4-stage mbarrier ring; one thread issues MMAs, eight warps run the epilogue; TMEM holds two
 // accumulator buffers so the epilogue of tile i overlaps the MMA of tile i+1. Units are
 // processed in waves small enough that pass 2 re-reads K from L2.
-//   select  max-pool (odd kernel, clipped ends) + block radix top-k, ascending kept positions
+//   select  max-pool (odd kernel, clipped ends; or the average over the clipped window) + block
+//           radix top-k, ascending kept positions
 //   gather  kept K / V rows -> compact cache (16-byte vector copies)
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -487,6 +488,18 @@ __global__ void lse_merge_kernel(ScoreParams p, int rp) {
 }
 
 // ------------------------------------------------------------------------------------------
+// average pooling: window sums in 32.32 fixed point. Scores lie in [0, G * W] with G * W <= 256
+// and a window holds at most 2^20 - 1 of them, so a sum stays below 2^60: exact, independent of
+// the order of its terms, and equal between the sliding sum of the shared-memory select and the
+// direct sums of the general one.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ long long to_fixed(float v) { return __float2ll_rn(v * 4294967296.f); }
+
+__device__ __forceinline__ float fixed_mean(long long s, int count) {
+  return __fdiv_rn(__ll2float_rn(s) * 2.3283064365386963e-10f, (float)count);
+}
+
+// ------------------------------------------------------------------------------------------
 // pooling + top-k selection: one CTA of 1024 threads per (unit, KV head)
 // ------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) select_kernel(SnapArgs a) {
@@ -512,9 +525,16 @@ __global__ void __launch_bounds__(1024) select_kernel(SnapArgs a) {
   const float* in = a.scores + (size_t)ukv * (a.max_len - W);
   float* pooled = a.pooled + (size_t)ukv * (a.max_len - W);
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    float m = in[i];
     const int lo = max(0, i - r), hi = min(n - 1, i + r);
-    for (int j = lo; j <= hi; ++j) m = fmaxf(m, in[j]);
+    float m;
+    if (a.pool_avg) {
+      long long sum = 0;
+      for (int j = lo; j <= hi; ++j) sum += to_fixed(in[j]);
+      m = fixed_mean(sum, hi - lo + 1);
+    } else {
+      m = in[i];
+      for (int j = lo; j <= hi; ++j) m = fmaxf(m, in[j]);
+    }
     pooled[i] = m;
   }
   __syncthreads();
@@ -575,32 +595,54 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_fast_kernel(SnapArgs a)
 
   const int base = tid * kSelPerThread;
   float x[kSelPerThread];
-  for (int w = 1; w <= r; w *= 2) {  // m_w -> m_2w until 2w = r + 1
+  if (a.pool_avg) {
+    // mean over the clipped window: a fixed-point sum slid over the thread's 32 positions
+    long long sum = 0;
+    if (base < n) {
+      const int hi0 = min(n - 1, base + r);
+      for (int j = max(0, base - r); j <= hi0; ++j) sum += to_fixed(sh[sel_slot(j)]);
+    }
 #pragma unroll
     for (int q = 0; q < kSelPerThread; ++q) {
       const int i = base + q;
-      float v = -INFINITY;
+      float v = 0.f;
       if (i < n) {
-        v = sh[sel_slot(i)];
-        if (i + w < n) v = fmaxf(v, sh[sel_slot(i + w)]);
+        if (q > 0) {
+          if (i + r < n) sum += to_fixed(sh[sel_slot(i + r)]);
+          if (i - r - 1 >= 0) sum -= to_fixed(sh[sel_slot(i - r - 1)]);
+        }
+        v = fixed_mean(sum, min(n - 1, i + r) - max(0, i - r) + 1);
       }
       x[q] = v;
     }
-    __syncthreads();
+  } else {
+    for (int w = 1; w <= r; w *= 2) {  // m_w -> m_2w until 2w = r + 1
 #pragma unroll
-    for (int q = 0; q < kSelPerThread; ++q)
-      if (base + q < n) sh[sel_slot(base + q)] = x[q];
-    __syncthreads();
-  }
-  uint32_t hi = 0u, lo = 0xffffffffu;
+      for (int q = 0; q < kSelPerThread; ++q) {
+        const int i = base + q;
+        float v = -INFINITY;
+        if (i < n) {
+          v = sh[sel_slot(i)];
+          if (i + w < n) v = fmaxf(v, sh[sel_slot(i + w)]);
+        }
+        x[q] = v;
+      }
+      __syncthreads();
 #pragma unroll
-  for (int q = 0; q < kSelPerThread; ++q) {
-    const int i = base + q;
-    float v = 0.f;
-    if (i < n) v = fmaxf(sh[sel_slot(max(0, i - r))], sh[sel_slot(i)]);
-    x[q] = v;
+      for (int q = 0; q < kSelPerThread; ++q)
+        if (base + q < n) sh[sel_slot(base + q)] = x[q];
+      __syncthreads();
+    }
+#pragma unroll
+    for (int q = 0; q < kSelPerThread; ++q) {
+      const int i = base + q;
+      float v = 0.f;
+      if (i < n) v = fmaxf(sh[sel_slot(max(0, i - r))], sh[sel_slot(i)]);
+      x[q] = v;
+    }
   }
   __syncthreads();
+  uint32_t hi = 0u, lo = 0xffffffffu;
   uint32_t* key = reinterpret_cast<uint32_t*>(sh);
 #pragma unroll
   for (int q = 0; q < kSelPerThread; ++q) {
@@ -999,7 +1041,8 @@ cudaError_t launch_snapkv(const SnapArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   // the whole-unit shared-memory select applies when every unit fits and the pooling kernel is
   // 2^k - 1 (the adaptive sizes 7 / 15 / 31 all are)
-  const bool pow2_kernel = a.kernel_size <= 0 || ((a.kernel_size + 1) & a.kernel_size) == 0;
+  const bool pow2_kernel =
+      a.pool_avg || a.kernel_size <= 0 || ((a.kernel_size + 1) & a.kernel_size) == 0;
   if (a.max_len - a.window <= kSelMaxN && pow2_kernel) {
     const size_t smem = select_fast_smem_bytes();
     e = ensure_dyn_smem((const void*)select_fast_kernel, smem);

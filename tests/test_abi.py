@@ -132,6 +132,21 @@ def test_per_head_compress_validation(lib):
     assert lib.rkv_snapkv_per_head_workspace_bytes(2, 8, 4, 32768, 32) == \
         lib.rkv_snapkv_workspace_bytes(2, 32, 1, 32768, 32)
 
+def test_avg_pool_compress_validation(lib):
+    vp = FAKE
+    args = (vp, vp, vp, vp, 1, 2, 4, 128, 4096, 32)
+    big = 1 << 30
+    # even kernel, kernel past the fixed-point limit, keep <= window, small workspace
+    assert lib.rkv_snapkv_compress_avg_pool(*args, 6, 256, 0.1, vp, vp, 256, vp, vp, None, vp,
+                                            big, None) == 1
+    assert lib.rkv_snapkv_compress_avg_pool(*args, (1 << 20) + 1, 256, 0.1, vp, vp, 256, vp, vp,
+                                            None, vp, big, None) == 1
+    assert lib.rkv_snapkv_compress_avg_pool(*args, 7, 32, 0.1, vp, vp, 256, vp, vp, None, vp,
+                                            big, None) == 1
+    assert lib.rkv_snapkv_compress_avg_pool(*args, 7, 256, 0.1, vp, vp, 256, vp, vp, None, vp, 64,
+                                            None) == 3
+
+
 def test_mt_validation_rejects_before_launch(lib):
     vp = FAKE
     # (q, new_k, new_v, k_full, v_full, full_len, kept_idx, kept_len, kmin, kmax)

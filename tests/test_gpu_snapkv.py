@@ -33,7 +33,7 @@ def _inputs(n_seq, n_kv, gqa, lens, window, seed, needles=0, outliers=0, layers=
     return wl, x
 
 
-def _run(rkv, x, window, kernel, keep, cap=None):
+def _run(rkv, x, window, kernel, keep, cap=None, avg=False):
     k, v, q, lens = x["k"], x["v"], x["q_win"], x["seq_lens"]
     n, n_kv, max_len, _ = k.shape
     cap = cap or keep
@@ -42,14 +42,15 @@ def _run(rkv, x, window, kernel, keep, cap=None):
     kept = torch.full((n, n_kv, keep), -9, dtype=torch.int32, device="cuda")
     out_len = torch.full((n,), -9, dtype=torch.int32, device="cuda")
     scores = torch.full((n, n_kv, max_len - window), -1.0, dtype=torch.float32, device="cuda")
-    ws = rkv.rkv_snapkv_compress(k, v, lens, q, kernel, keep, 1.0 / math.sqrt(D), k_out, v_out,
-                                 kept, out_len, scores_out=scores)
+    fn = rkv.rkv_snapkv_compress_avg_pool if avg else rkv.rkv_snapkv_compress
+    ws = fn(k, v, lens, q, kernel, keep, 1.0 / math.sqrt(D), k_out, v_out, kept, out_len,
+            scores_out=scores)
     rkv.rkv_check_status(ws)
     return k_out, v_out, kept, out_len, scores
 
 
 def _check_unit(x, u, g, gqa, window, kernel, keep, k_out, v_out, kept, out_len, scores,
-                tag=""):
+                tag="", pool=O.pool_max):
     L = int(x["seq_lens"][u])
     W = window
     k = _f64(x["k"][u, g, :L])
@@ -62,7 +63,7 @@ def _check_unit(x, u, g, gqa, window, kernel, keep, k_out, v_out, kept, out_len,
     assert (err <= tol).all(), (f"{tag} scores: {(err > tol).sum()} bad, worst rel "
                                 f"{(err / np.maximum(ref_scores, 1e-30)).max():.2e}")
     kk = kernel if kernel > 0 else O.adaptive_kernel_size(L)
-    pooled = O.pool_max(ref_scores, kk)
+    pooled = pool(ref_scores, kk)
     got = kept[u, g].cpu().numpy()
     cnt = min(L, keep)
     assert int(out_len[u]) == cnt, tag
@@ -133,6 +134,45 @@ def test_snapkv_select_paths(kernel):
     res = _run(rkv, x, 32, kernel, 2048)
     for u in range(3):
         _check_unit(x, u, 0, 4, 32, kernel, 2048, *res, tag=f"kernel {kernel} u{u}")
+
+
+def _fixed_point_avg(scores, kernel):
+    """The select's average pooling restated on its own fp32 scores: 32.32 fixed-point window
+    sums (exact), then float(sum) * 2^-32 / count in fp32."""
+    fx = np.rint(scores.astype(np.float64) * 2.0 ** 32).astype(np.int64)
+    c = np.concatenate([[0], np.cumsum(fx)])
+    n, r = fx.shape[0], kernel // 2
+    i = np.arange(n)
+    lo, hi = np.maximum(0, i - r), np.minimum(n - 1, i + r)
+    s = (c[hi + 1] - c[lo]).astype(np.float32) * np.float32(2.0 ** -32)
+    return s / (hi - lo + 1).astype(np.float32)
+
+
+@pytest.mark.parametrize("lens,kernel", [((32800, 12345, 9000), 7), ((32800, 12345, 9000), 15),
+                                         ((32800, 12345, 9000), 5), ((32800, 12345, 9000), 0),
+                                         ((40000, 5000, 2100), 5), ((40000, 5000, 2100), 0)])
+def test_snapkv_avg_pool(lens, kernel):
+    # average pooling over the clipped window: the shared-memory select (every odd kernel when
+    # all units hold at most 32768 scores) and the general select (a 40000-token prompt); ragged
+    # lengths, one prompt barely above keep
+    rkv = _lib()
+    W, keep = 32, 2048
+    wl, x = _inputs(3, 1, 4, list(lens), W, seed=109, needles=8)
+    res = _run(rkv, x, W, kernel, keep, avg=True)
+    kept, scores = res[2].cpu().numpy(), res[4].cpu().numpy()
+    for u in range(3):
+        _check_unit(x, u, 0, 4, W, kernel, keep, *res, tag=f"avg kernel {kernel} u{u}",
+                    pool=O.pool_avg)
+        # exact: the kept set is the top-k (ties -> lower position) of the fixed-point means
+        # of the kernel's own scores
+        L = lens[u]
+        kk = kernel if kernel > 0 else O.adaptive_kernel_size(L)
+        keys = _fixed_point_avg(scores[u, 0, :L - W], kk).astype(np.float64)
+        order = np.lexsort((np.arange(L - W), -keys))
+        assert np.array_equal(kept[u, 0, :keep - W], np.sort(order[:keep - W])), f"u{u} exact"
+    # average and max pooling keep different sets
+    res_max = _run(rkv, x, W, kernel, keep)
+    assert not torch.equal(res[2], res_max[2])
 
 
 def test_snapkv_per_head_without_group_sum():

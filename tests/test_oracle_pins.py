@@ -488,3 +488,21 @@ def test_paged_round_trip_and_decode():
     r1 = O.hybrid_decode(q, kc[1], vc[1], L, k1min, k1max, B, p, 8, 0.2)
     assert np.array_equal(r["tokens"], r1["tokens"])
     np.testing.assert_array_equal(r["out"], r1["out"])
+
+
+# ---------------------------------------------------------------- average pooling (R21)
+def test_pool_avg_hand_example_and_invariants():
+    x = np.array([4.0, 0.0, 2.0, 8.0, 1.0])
+    # kernel 3: clipped windows [4,0], [4,0,2], [0,2,8], [2,8,1], [8,1]
+    np.testing.assert_allclose(O.pool_avg(x, 3), [2.0, 2.0, 10 / 3, 11 / 3, 4.5], rtol=1e-15)
+    np.testing.assert_array_equal(O.pool_avg(x, 1), x)
+    rng = np.random.default_rng(22)
+    y = rng.random(200)
+    for kern in (3, 7, 15, 31):
+        a = O.pool_avg(y, kern)
+        assert np.all(a <= O.pool_max(y, kern) + 1e-15)
+        assert np.allclose(O.pool_avg(np.full(50, 0.25), kern), 0.25)
+        # interior positions are the plain moving average
+        r = kern // 2
+        np.testing.assert_allclose(a[r:-r], np.convolve(y, np.ones(kern) / kern, mode="valid"),
+                                   rtol=1e-12)
