@@ -123,6 +123,26 @@ rkv_status rkv_snapkv_compress(const void* k, const void* v, const int32_t* seq_
                                int32_t* out_len, float* scores_out, void* ws, size_t ws_bytes,
                                void* stream);
 
+/* [MT] The selection half of rkv_snapkv_compress (scores, pooling, top-k) without the gather:
+ * RocketKV-MT evicts nothing, so each turn filters the full, unfiltered history again
+ * ("SCBench Results": the next turn's prefill takes all earlier tokens as its prefix and SnapKV++
+ * filters once more) and the decode reads the kept rows through the index list.
+ *   k         [n][n_kv][max_len][128] bf16: the full cache, rows >= L_u ignored (no V needed)
+ *   seq_lens  [n] int32: history length L_u this turn (earlier turns, generated tokens, the new
+ *             input), window <= L_u <= max_len
+ *   q_win     [n][n_kv*gqa][window][128] bf16: the last `window` queries of this turn's input
+ *   kept_idx  [n][n_kv][kept_stride] int32, kept_stride >= keep: entries 0 .. keep-1 of each
+ *             (unit, KV head) written as in rkv_snapkv_compress (-1 past out_len[u]); entries
+ *             keep .. kept_stride-1 untouched, so the list can be handed to
+ *             rkv_build_page_summaries_mt / rkv_hybrid_decode_mt with kcap = kept_stride
+ *   out_len   [n] int32: min(L_u, keep), the kept_len of the MT calls
+ * Other arguments, workspace (rkv_snapkv_workspace_bytes) and errors as rkv_snapkv_compress. */
+rkv_status rkv_snapkv_select(const void* k, const int32_t* seq_lens, const void* q_win, int n,
+                             int n_kv, int gqa, int head_dim, int max_len, int window,
+                             int kernel_size, int keep, float scale, int32_t* kept_idx,
+                             int kept_stride, int32_t* out_len, float* scores_out, void* ws,
+                             size_t ws_bytes, void* stream);
+
 /* rkv_snapkv_compress with average pooling in place of max pooling (a SnapKV pooling variant;
  * the pages describe max pooling only): each prefix score is replaced by the mean of the scores
  * over the in-range positions of its clipped window [max(0, i - r), min(n - 1, i + r)],

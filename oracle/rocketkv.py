@@ -55,6 +55,11 @@ Readings taken where the pages leave a step open (each restated at its function)
       generated since), whose rows stay in the full cache. The pages do not say where generated
       tokens go; they are appended to the full cache and to the kept sequence, and are selectable
       (as in R12).
+  R22 RocketKV-MT across turns ([P3] "SCBench Results": the next turn's prefill takes every
+      earlier token as its prefix and SnapKV++ filters the unfiltered history again): a later
+      turn's history is the full cache in row order (earlier prompts, generated tokens, the new
+      input), its window is the last W queries of the new input, and the new kept list replaces
+      the old one; the turn's generated tokens are appended to it as in R17.
 """
 from __future__ import annotations
 
@@ -66,7 +71,7 @@ __all__ = [
     "plan", "adaptive_kernel_size", "window_scores", "pool_max", "pool_avg", "topk_desc",
     "snapkv_compress", "page_summaries", "channel_pick", "approx_scores", "page_select",
     "attention", "dense_decode", "hybrid_decode", "group_topk_attention", "append_token",
-    "kept_view", "mt_page_summaries", "mt_hybrid_decode", "mt_append_token",
+    "kept_view", "mt_page_summaries", "mt_hybrid_decode", "mt_append_token", "mt_refilter",
     "plan_even_split", "snapkv_compress_per_head", "paged_view", "paged_scatter",
 ]
 
@@ -405,6 +410,17 @@ def mt_append_token(k_full: np.ndarray, v_full: np.ndarray, full_len: int, kept:
         kmin[:, pg] = np.minimum(kmin[:, pg], new_k)
         kmax[:, pg] = np.maximum(kmax[:, pg], new_k)
     return full_len + 1, n_kept + 1
+
+
+def mt_refilter(k_full: np.ndarray, full_len: int, q_win: np.ndarray, keep: int, kernel: int,
+                scale: float) -> np.ndarray:
+    """The kept list of a later RocketKV-MT turn (R22): SnapKV++ over the whole history
+    k_full[:full_len] with this turn's window queries. Returns the kept positions (ascending
+    prefix, then the window), which index the full cache directly.
+    [P3] "SCBench Results".
+    """
+    hist = k_full[:full_len]
+    return snapkv_compress(hist, hist, q_win, keep, kernel, scale)[0]
 
 
 # --------------------------------------------------------------------------------------------

@@ -134,12 +134,21 @@ static rkv_status snapkv_impl(const void* k, const void* v, const int32_t* seq_l
                               int32_t* out_len, float* scores_out, void* ws, size_t ws_bytes,
                               void* stream, bool per_head, const PagedMap& out_pm,
                               int page = 0, int page_cap = 0, void* kmin = nullptr,
-                              void* kmax = nullptr, bool pool_avg = false) {
+                              void* kmax = nullptr, bool pool_avg = false,
+                              int kept_stride = 0) {
   if (head_dim != kHeadDim) return RKV_ERR_UNSUPPORTED;
-  if (!k || !v || !seq_lens || !q_win || !k_out || !v_out || !kept_idx || !out_len)
+  // kept_stride > 0: index-only selection (no v, no compact cache, no gather)
+  const bool index_only = kept_stride > 0;
+  if (index_only) {
+    if (k_out || v_out || kmin || kmax || kept_stride < keep) return RKV_ERR_INVALID_ARG;
+    cap = keep;
+  }
+  if (!k || (!v && !index_only) || !seq_lens || !q_win ||
+      (!index_only && (!k_out || !v_out)) || !kept_idx || !out_len)
     return RKV_ERR_INVALID_ARG;
-  if (!aligned16(k) || !aligned16(v) || !aligned16(q_win) || !aligned16(k_out) ||
-      !aligned16(v_out) || (scores_out && !aligned16(scores_out)))
+  if (!aligned16(k) || (v && !aligned16(v)) || !aligned16(q_win) ||
+      (k_out && !aligned16(k_out)) || (v_out && !aligned16(v_out)) ||
+      (scores_out && !aligned16(scores_out)))
     return RKV_ERR_INVALID_ARG;
   if (n <= 0 || n_kv <= 0 || gqa <= 0 || window <= 0 || max_len <= window || keep <= window ||
       keep > cap || cap <= 0 || !(scale > 0.f) || !std::isfinite(scale))
@@ -178,6 +187,7 @@ static rkv_status snapkv_impl(const void* k, const void* v, const int32_t* seq_l
   a.window = window;
   a.kernel_size = kernel_size;
   a.pool_avg = pool_avg ? 1 : 0;
+  a.kept_stride = index_only ? kept_stride : keep;
   a.keep = keep;
   a.cap = cap;
   a.scale_log2 = scale * kLog2e;
@@ -224,6 +234,18 @@ rkv_status rkv_snapkv_compress_avg_pool(const void* k, const void* v, const int3
   return snapkv_impl(k, v, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window,
                      kernel_size, keep, scale, k_out, v_out, cap, kept_idx, out_len, scores_out,
                      ws, ws_bytes, stream, false, PagedMap{}, 0, 0, nullptr, nullptr, true);
+}
+
+rkv_status rkv_snapkv_select(const void* k, const int32_t* seq_lens, const void* q_win, int n,
+                             int n_kv, int gqa, int head_dim, int max_len, int window,
+                             int kernel_size, int keep, float scale, int32_t* kept_idx,
+                             int kept_stride, int32_t* out_len, float* scores_out, void* ws,
+                             size_t ws_bytes, void* stream) {
+  if (kept_stride <= 0) return RKV_ERR_INVALID_ARG;
+  return snapkv_impl(k, nullptr, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window,
+                     kernel_size, keep, scale, nullptr, nullptr, keep, kept_idx, out_len,
+                     scores_out, ws, ws_bytes, stream, false, PagedMap{}, 0, 0, nullptr, nullptr,
+                     false, kept_stride);
 }
 
 rkv_status rkv_snapkv_compress_summarized(const void* k, const void* v,

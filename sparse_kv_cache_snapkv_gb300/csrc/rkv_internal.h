@@ -145,6 +145,7 @@ struct SnapArgs {
   bf16* kmax;
   int page, page_cap;
   int pool_avg;     // 1: average pooling over the clipped window instead of max pooling
+  int kept_stride;  // entries between units' kept lists (>= keep)
   uint32_t* status;
 };
 

@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(1024) select_kernel(SnapArgs a) {
   const int u = ukv / a.n_kv, g = ukv - u * a.n_kv;
   const int W = a.window;
   const int L = a.seq_lens[u];
-  int32_t* kept = a.kept_idx + (size_t)ukv * a.keep;
+  int32_t* kept = a.kept_idx + (size_t)ukv * a.kept_stride;
   if (L <= W || L > a.max_len) {
     for (int i = threadIdx.x; i < a.keep; i += blockDim.x) kept[i] = -1;
     if (g == 0 && threadIdx.x == 0) a.out_len[u] = 0;
@@ -574,7 +574,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_fast_kernel(SnapArgs a)
   const int u = ukv / a.n_kv, g = ukv - u * a.n_kv;
   const int W = a.window;
   const int L = a.seq_lens[u];
-  int32_t* kept = a.kept_idx + (size_t)ukv * a.keep;
+  int32_t* kept = a.kept_idx + (size_t)ukv * a.kept_stride;
   if (L <= W || L > a.max_len) {
     for (int i = tid; i < a.keep; i += kSelThreads) kept[i] = -1;
     if (g == 0 && tid == 0) a.out_len[u] = 0;
@@ -876,7 +876,7 @@ __global__ void __launch_bounds__(256) gather_kernel(SnapArgs a) {
   const int cnt = min(L, a.keep);
   const int row0 = blockIdx.x * 64;
   if (row0 >= cnt) return;
-  const int32_t* kept = a.kept_idx + (size_t)ukv * a.keep;
+  const int32_t* kept = a.kept_idx + (size_t)ukv * a.kept_stride;
   const size_t src_unit = (size_t)(ukv / a.kv_div);
   const uint4* ksrc = reinterpret_cast<const uint4*>(a.k + src_unit * a.max_len * kHeadDim);
   const uint4* vsrc = reinterpret_cast<const uint4*>(a.v + src_unit * a.max_len * kHeadDim);
@@ -1053,6 +1053,7 @@ cudaError_t launch_snapkv(const SnapArgs& a, cudaStream_t s) {
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (!a.k_out) return cudaSuccess;  // index-only selection (RocketKV-MT keeps every row)
   const size_t gsmem = a.kmin ? gather_smem_bytes(a.page) : 0;
   if (gsmem) {
     e = ensure_dyn_smem((const void*)gather_kernel, gsmem);

@@ -32,7 +32,7 @@ SYMBOLS = [
     "rkv_build_page_summaries_mt", "rkv_hybrid_decode_mt", "rkv_plan_even_split",
     "rkv_snapkv_per_head_workspace_bytes", "rkv_snapkv_compress_per_head",
     "rkv_snapkv_compress_paged", "rkv_build_page_summaries_paged", "rkv_hybrid_decode_paged",
-    "rkv_snapkv_compress_summarized", "rkv_snapkv_compress_avg_pool",
+    "rkv_snapkv_compress_summarized", "rkv_snapkv_compress_avg_pool", "rkv_snapkv_select",
 ]
 
 
@@ -72,6 +72,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
                                  vp, vp, i32, vp, vp, vp, vp, sz, vp], i32),
         "rkv_snapkv_compress_avg_pool": ([vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                           i32, f32, vp, vp, i32, vp, vp, vp, vp, sz, vp], i32),
+        "rkv_snapkv_select": ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, vp, i32,
+                               vp, vp, vp, sz, vp], i32),
         "rkv_summaries_workspace_bytes": ([], sz),
         "rkv_build_page_summaries": ([vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp,
                                       sz, vp], i32),
@@ -219,6 +221,25 @@ def rkv_snapkv_compress_avg_pool(k, v, seq_lens, q_win, kernel_size: int, keep: 
         kernel_size, keep, float(scale), _ptr(k_out), _ptr(v_out), cap, _ptr(kept_idx),
         _ptr(out_len), _ptr(scores_out), _ptr(ws), ws.numel(), _stream(stream))
     _check("rkv_snapkv_compress_avg_pool", code)
+    return ws
+
+
+def rkv_snapkv_select(k, seq_lens, q_win, kernel_size: int, keep: int, scale: float, kept_idx,
+                      out_len, scores_out=None, ws=None, stream=None):
+    """RocketKV-MT stage 1: scores, pooling and top-k over the full history, kept indices only
+    (kept_idx [n][n_kv][kept_stride], kept_stride >= keep); see include/rkv.h."""
+    _bf16(k, "k"), _bf16(q_win, "q_win"), _i32(seq_lens, "seq_lens")
+    _i32(kept_idx, "kept_idx"), _i32(out_len, "out_len")
+    n, n_kv, max_len, d = k.shape
+    hq, window = q_win.shape[1], q_win.shape[2]
+    gqa = hq // n_kv
+    if ws is None:
+        ws = workspace(rkv_snapkv_workspace_bytes(n, n_kv, gqa, max_len, window), k.device)
+    code = load().rkv_snapkv_select(
+        _ptr(k), _ptr(seq_lens), _ptr(q_win), n, n_kv, gqa, d, max_len, window, kernel_size,
+        keep, float(scale), _ptr(kept_idx), kept_idx.shape[2], _ptr(out_len), _ptr(scores_out),
+        _ptr(ws), ws.numel(), _stream(stream))
+    _check("rkv_snapkv_select", code)
     return ws
 
 

@@ -13,6 +13,8 @@ Recipe (Llama-3.1-8B attention shapes: 32 query heads, 8 KV heads, head_dim 128,
     u_g, a key aligned with the mean window-query direction.
   * Decode queries: plain N(0, 1). Appended decode tokens: K as above (same sigma), V ~ N(0, 1).
   * Positions past a sequence's length are zero.
+  * A second conversation turn (`second_turn_inputs`): a new direction u2, window queries
+    z'' + 4 u2, keys ||sigma||_2 u2 planted in the first prompt, and the turn's new input tokens.
 A "unit" is one (sequence, layer) pair; units are sequence-major: u = s * layers + layer.
 """
 from __future__ import annotations
@@ -127,6 +129,45 @@ def prefill_inputs(wl: Workload, seed: int, device="cpu"):
     seq_lens = torch.tensor(lens, dtype=torch.int32, device=dev)
     return {"k": k, "v": v, "q_win": q_win, "seq_lens": seq_lens, "sigma": sigma,
             "needles": needle_pos}
+
+
+def second_turn_inputs(wl: Workload, x: dict, new_tokens: int, needles: int, seed: int,
+                       device="cpu"):
+    """Inputs of a second conversation turn, drawn after `prefill_inputs` (x):
+
+    * u2: a new seeded unit vector per (unit, KV head); the turn's window queries are
+      Q_win2[h, j] = z'' + 4 u2.
+    * `needles` seeded positions of the first prompt's prefix (not its own needles) get
+      K = ||sigma||_2 u2: keys of ordinary norm that only the second turn's queries single out.
+      They are written into x["k"] in place, so draw the second turn before the first one runs.
+    * new_k / new_v [n, Hkv, new_tokens, d] bf16: the turn's new input tokens, K = sigma * z,
+      V = z' (the window queries belong to its last W tokens, so new_tokens >= W).
+    """
+    dev = torch.device(device)
+    g = torch.Generator(device=dev).manual_seed(seed)
+    n, hkv, d, W = wl.n, wl.n_kv, wl.head_dim, wl.window
+    assert new_tokens >= W
+    lens = unit_lens(wl)
+    f32 = dict(device=dev, dtype=torch.float32)
+    sigma = x["sigma"].to(dev)
+    direction = torch.randn(n, hkv, d, generator=g, **f32)
+    direction /= direction.norm(dim=-1, keepdim=True)
+    needle_pos = torch.zeros(n, hkv, needles, dtype=torch.int64)
+    for u in range(n):
+        L = lens[u]
+        for h in range(hkv):
+            taken = set(x["needles"][u, h].tolist())
+            perm = torch.randperm(L - W, generator=g, device=dev).cpu().tolist()
+            pos = sorted([p for p in perm if p not in taken][:needles])
+            key = (sigma[u, h].norm() * direction[u, h]).to(torch.bfloat16)
+            x["k"][u, h, pos] = key.to(x["k"].device)[None, :]
+            needle_pos[u, h] = torch.tensor(pos, dtype=torch.int64)
+    z = torch.randn(n, hkv, new_tokens, d, generator=g, **f32) * sigma[:, :, None, :]
+    zv = torch.randn(n, hkv, new_tokens, d, generator=g, **f32)
+    qz = torch.randn(n, hkv, wl.gqa, W, d, generator=g, **f32)
+    qz += 4.0 * direction[:, :, None, None, :]
+    return {"new_k": z.to(torch.bfloat16), "new_v": zv.to(torch.bfloat16),
+            "q_win": qz.reshape(n, hkv * wl.gqa, W, d).to(torch.bfloat16), "needles": needle_pos}
 
 
 def decode_queries(wl: Workload, steps: int, seed: int, device="cpu"):

@@ -147,6 +147,19 @@ def test_avg_pool_compress_validation(lib):
                                             None) == 3
 
 
+def test_select_only_validation(lib):
+    vp = FAKE
+    big = 1 << 30
+    # (k, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window, kernel, keep, scale)
+    head = (vp, vp, vp, 1, 2, 4, 128, 4096, 32, 7)
+    assert lib.rkv_snapkv_select(*head, 256, 0.1, vp, 255, vp, None, vp, big, None) == 1  # stride
+    assert lib.rkv_snapkv_select(*head, 256, 0.1, vp, 0, vp, None, vp, big, None) == 1
+    assert lib.rkv_snapkv_select(*head, 32, 0.1, vp, 512, vp, None, vp, big, None) == 1   # keep
+    assert lib.rkv_snapkv_select(vp, vp, vp, 1, 2, 4, 64, 4096, 32, 7, 256, 0.1, vp, 256, vp,
+                                 None, vp, big, None) == 2                              # head_dim
+    assert lib.rkv_snapkv_select(*head, 256, 0.1, vp, 256, vp, None, vp, 64, None) == 3  # ws
+
+
 def test_mt_validation_rejects_before_launch(lib):
     vp = FAKE
     # (q, new_k, new_v, k_full, v_full, full_len, kept_idx, kept_len, kmin, kmax)

@@ -183,3 +183,102 @@ def test_mt_bad_kept_index_sets_status():
         rkv.rkv_check_status(ws)
     assert e.value.bits & 0x10
     assert torch.isfinite(out.float()).all()
+
+
+def test_mt_second_turn_refilter():
+    # two turns of RocketKV-MT: turn 1 filters the prompt (index only: nothing is evicted),
+    # decodes with appends; turn 2 appends its new input to the full cache, filters the whole
+    # history again with its own window queries, rebuilds the summaries and decodes on
+    from sparse_kv_cache_snapkv_gb300 import rkv, synthetic as S
+    rkv.load()
+    T1, T2, M = 8, 4, 256
+    wl = S.Workload("mt2", 2, 1, 2, 4, D, (9000, 7000), W, BUDGET, needles=8)
+    x = S.prefill_inputs(wl, seed=6500, device="cuda")
+    t2 = S.second_turn_inputs(wl, x, M, 8, seed=6510, device="cuda")
+    nk, nv = S.append_tokens(wl, T1 + T2, x["sigma"], seed=6520, device="cuda")
+    dq = S.decode_queries(wl, T1 + T2, seed=6530, device="cuda")
+    n, n_kv, gqa, max_len = wl.n, wl.n_kv, wl.gqa, wl.max_len
+    keep = rkv.rkv_plan(max_len, BUDGET)[0]
+    kcap = keep + T1 + T2
+    full_cap = max_len + T1 + M + T2
+    page_cap = ((kcap + PAGE - 1) // PAGE + 7) // 8 * 8
+    scale = 1.0 / math.sqrt(D)
+    k_f = torch.zeros(n, n_kv, full_cap, D, dtype=torch.bfloat16, device="cuda")
+    v_f = torch.zeros_like(k_f)
+    k_f[:, :, :max_len] = x["k"]
+    v_f[:, :, :max_len] = x["v"]
+    full_len = x["seq_lens"].clone()
+    kept = torch.full((n, n_kv, kcap), -7, dtype=torch.int32, device="cuda")
+    kept_len = torch.empty(n, dtype=torch.int32, device="cuda")
+    kmin = torch.zeros(n, n_kv, D, page_cap, dtype=torch.bfloat16, device="cuda")
+    kmax = torch.zeros_like(kmin)
+
+    def decode(t):
+        out = torch.empty_like(dq[t])
+        selp = torch.empty(n, n_kv, (BUDGET // 2) // PAGE, dtype=torch.int32, device="cuda")
+        ws = rkv.rkv_hybrid_decode_mt(dq[t], k_f, v_f, full_len, kept, kept_len, kmin, kmax,
+                                      BUDGET, PAGE, CHANNELS, scale, out, new_k=nk[t],
+                                      new_v=nv[t], sel_pages=selp)
+        rkv.rkv_check_status(ws)
+        return out, selp
+
+    # ---- turn 1
+    rkv.rkv_check_status(rkv.rkv_snapkv_select(k_f, full_len, x["q_win"], 0, keep, scale, kept,
+                                               kept_len))
+    assert (kept[:, :, keep:] == -7).all(), "entries past keep must stay untouched"
+    kept1 = kept[:, :, :keep].cpu().numpy().copy()
+    rkv.rkv_check_status(rkv.rkv_build_page_summaries_mt(k_f, kept, kept_len, PAGE, kmin, kmax))
+    for t in range(T1):
+        decode(t)
+    # ---- turn 2: the new input goes to the end of the full cache, then the history is filtered
+    for u in range(n):
+        L = int(full_len[u])
+        k_f[u, :, L:L + M] = t2["new_k"][u]
+        v_f[u, :, L:L + M] = t2["new_v"][u]
+    full_len += M
+    rkv.rkv_check_status(rkv.rkv_snapkv_select(k_f, full_len, t2["q_win"], 0, keep, scale, kept,
+                                               kept_len))
+    kept2 = kept[:, :, :keep].cpu().numpy().copy()
+    assert np.array_equal(kept_len.cpu().numpy(), [keep, keep])
+    kmin.zero_()
+    kmax.zero_()
+    rkv.rkv_check_status(rkv.rkv_build_page_summaries_mt(k_f, kept, kept_len, PAGE, kmin, kmax))
+    hist_len = full_len.cpu().numpy().copy()
+    for u in range(n):
+        for g in range(n_kv):
+            tag = f"unit {u} kv {g}"
+            L2 = int(hist_len[u])
+            hist = _f64(k_f[u, g, :L2])
+            q2 = _f64(t2["q_win"][u, g * gqa:(g + 1) * gqa])
+            kk = O.adaptive_kernel_size(L2)
+            pooled = O.pool_max(O.window_scores(hist, q2, scale), kk)
+            assert np.array_equal(kept2[u, g, keep - W:], np.arange(L2 - W, L2)), tag
+            parity.check_selection(kept2[u, g, :keep - W], pooled, keep - W, tag)
+            n2 = t2["needles"][u, g].numpy()
+            assert np.isin(n2, kept2[u, g]).all(), f"{tag}: turn 2 misses its keys"
+            assert not np.isin(n2, kept1[u, g]).all(), f"{tag}: turn 1 kept every turn-2 key"
+    # ---- turn 2 decodes on the new kept list (with appends) and matches the oracle
+    for t in range(T1, T1 + T2 - 1):
+        decode(t)
+    t = T1 + T2 - 1
+    kept_before = kept_len.cpu().numpy().copy()
+    len_before = full_len.cpu().numpy().copy()
+    out, selp = decode(t)
+    for u in range(n):
+        for g in range(n_kv):
+            tag = f"turn 2 decode unit {u} kv {g}"
+            L, n1 = int(len_before[u]), int(kept_before[u])
+            kf = _f64(k_f[u, g, :L + 1])
+            vf = _f64(v_f[u, g, :L + 1])
+            kl = kept[u, g, :n1 + 1].cpu().numpy()
+            assert kl[n1] == L, tag
+            assert np.array_equal(kl[keep:n1], np.arange(len_before[u] - (n1 - keep), L)), tag
+            mn, mx = O.mt_page_summaries(kf, kl, n1 + 1, PAGE)
+            qh = _f64(dq[t, u, g * gqa:(g + 1) * gqa])
+            ref = O.mt_hybrid_decode(qh, kf, vf, kl, n1 + 1, mn, mx, BUDGET, PAGE, CHANNELS,
+                                     scale)
+            gp = selp[u, g].cpu().numpy()
+            parity.check_selection(gp, ref["scores"], len(ref["pages"]), tag)
+            rows = np.concatenate([kl[p * PAGE:min(n1 + 1, (p + 1) * PAGE)] for p in gp])
+            parity.check_output(_f64(out[u, g * gqa:(g + 1) * gqa]),
+                                O.attention(qh, kf[rows], vf[rows], scale), tag)

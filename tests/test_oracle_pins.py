@@ -506,3 +506,36 @@ def test_pool_avg_hand_example_and_invariants():
         r = kern // 2
         np.testing.assert_allclose(a[r:-r], np.convolve(y, np.ones(kern) / kern, mode="valid"),
                                    rtol=1e-12)
+
+
+# ---------------------------------------------------------------- RocketKV-MT across turns (R22)
+def test_mt_second_turn_recovers_tokens_the_first_evicted():
+    # "SCBench Results": tokens that the first turn's filtering drops can matter to a later turn,
+    # and RocketKV-MT, which evicts nothing, finds them again when it filters the full history.
+    # Keys that only the second turn's queries single out are planted in the first prompt.
+    from sparse_kv_cache_snapkv_gb300 import synthetic as S
+    wl = S.Workload("mt2", 1, 1, 2, 4, 128, (6000,), 32, 256, needles=8)
+    x = S.prefill_inputs(wl, seed=1)
+    t2 = S.second_turn_inputs(wl, x, 256, 8, seed=101)
+    nk, nv = S.append_tokens(wl, 16, x["sigma"], seed=201)
+    keep, scale = 1024, 1 / math.sqrt(128)
+    for h in range(2):
+        k = x["k"][0, h].double().numpy()
+        kept1 = O.snapkv_compress(k, k, x["q_win"][0, 4 * h:4 * h + 4].double().numpy(), keep,
+                                  7, scale)[0]
+        hist = np.concatenate([k, nk[:, 0, h].double().numpy(),
+                               t2["new_k"][0, h].double().numpy()])
+        L2 = hist.shape[0]
+        q2 = t2["q_win"][0, 4 * h:4 * h + 4].double().numpy()
+        kept2 = O.mt_refilter(hist, L2, q2, keep, 7, scale)
+        n2 = t2["needles"][0, h].numpy()
+        assert np.isin(n2, kept1).sum() <= 2            # the first turn drops them
+        assert np.isin(n2, kept2).all()                 # the second finds them again
+        assert np.array_equal(kept2[-32:], np.arange(L2 - 32, L2))
+        # the re-filter is SnapKV++ on the history: with the history equal to the first prompt
+        # and the first turn's queries it returns the first turn's list
+        assert np.array_equal(O.mt_refilter(k, 6000, x["q_win"][0, 4 * h:4 * h + 4].double()
+                                            .numpy(), keep, 7, scale), kept1)
+        # rows past full_len are not part of the history
+        padded = np.concatenate([hist, np.full((50, 128), 1e3)])
+        assert np.array_equal(O.mt_refilter(padded, L2, q2, keep, 7, scale), kept2)
