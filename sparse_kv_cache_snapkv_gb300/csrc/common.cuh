@@ -5,8 +5,8 @@
 //    forever; 16-byte cp.async copies; programmatic-dependent-launch controls
 //  * warp / block scans
 //  * top-k selects (largest keys first, ties -> lower index, indices emitted in ascending order):
-//    a general block radix select, a low-latency block select for <= NK * 256 keys, and a
-//    one-warp select for 128 keys
+//    a general block radix select and low-latency block selects for <= NK * 256 keys (a
+//    variant for <= 1024 keys with contiguous keys per thread)
 #pragma once
 
 #include <cstdint>
@@ -571,120 +571,212 @@ __device__ __forceinline__ int block_topk_fast(const float* keys, int n, int k, 
   return gt_acc + min(eq_acc, need_eq);
 }
 
-// Top-k of 128 keys within one warp (no block barrier): keys already mapped by ordered_key
-// in shared memory (ukeys[0..127]); lane l holds keys l, l + 32, l + 64, l + 96. Same contract as
-// block_topk_fast (k largest, ties -> lower index, indices written ascending to out[0..k),
-// returns the count; 1 <= k <= 128). MSB-first radix select on the bits below those all keys
-// share, 8-bit digits counted in `hist` (256 words of warp-private scratch); once the k-th key's
-// bin holds at most 32 keys they are gathered in index order into `cand` (32 words of
-// warp-private scratch) and ranked directly by (key desc, index asc). Only the calling warp may
-// touch hist / cand meanwhile.
-__device__ __forceinline__ int warp_topk128(const uint32_t* ukeys, int k, int* out,
-                                            uint32_t* hist, uint32_t* cand) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t lt = (1u << lane) - 1u;
-  uint32_t u[4];
+// block_topk_fast for n <= 1024 with thread t holding the contiguous keys 4t .. 4t + 3 (one
+// 16-byte load; `keys` 16-byte aligned): the radix steps are the same, and the compaction needs
+// one ballot per bit of a thread's 0..4 taken keys, because (warp, lane, j) is already index
+// order. A ranked k-th key whose equal keys are all needed turns the rule into "take >= it",
+// which skips the count of equal keys. Ends without a barrier.
+__device__ __forceinline__ int block_topk_1024(const float* keys, int n, int k, int* out,
+                                             FastSelectSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NK = 4;
+  uint32_t u[NK];
+  bool v[NK];
+  {
+    const int i0 = 4 * tid;
+    if (i0 + 3 < n) {
+      const float4 f = reinterpret_cast<const float4*>(keys)[tid];
+      u[0] = ordered_key(f.x);
+      u[1] = ordered_key(f.y);
+      u[2] = ordered_key(f.z);
+      u[3] = ordered_key(f.w);
+      v[0] = v[1] = v[2] = v[3] = true;
+    } else {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) u[j] = ukeys[32 * j + lane];
-  const uint32_t hi =
-      __reduce_max_sync(0xffffffffu, max(max(u[0], u[1]), max(u[2], u[3])));
-  const uint32_t lo =
-      __reduce_min_sync(0xffffffffu, min(min(u[0], u[1]), min(u[2], u[3])));
+      for (int j = 0; j < NK; ++j) {
+        v[j] = i0 + j < n;
+        u[j] = v[j] ? ordered_key(keys[i0 + j]) : 0u;
+      }
+    }
+  }
+  uint32_t hi, lo;
+  {
+    const uint4 a0 = reinterpret_cast<const uint4*>(sm.wmax)[0];
+    const uint4 a1 = reinterpret_cast<const uint4*>(sm.wmax)[1];
+    const uint4 b0 = reinterpret_cast<const uint4*>(sm.wmin)[0];
+    const uint4 b1 = reinterpret_cast<const uint4*>(sm.wmin)[1];
+    hi = max(max(max(a0.x, a0.y), max(a0.z, a0.w)), max(max(a1.x, a1.y), max(a1.z, a1.w)));
+    lo = min(min(min(b0.x, b0.y), min(b0.z, b0.w)), min(min(b1.x, b1.y), min(b1.z, b1.w)));
+  }
   const uint32_t diff = hi ^ lo;
   int start = diff ? 32 - __clz(diff) : 0;
   uint32_t mask = start >= 32 ? 0u : ~((1u << start) - 1u);
   uint32_t prefix = hi & mask;
   int remaining = k;
   bool inclusive = false;
-  while (start > 0 && !inclusive) {
-    const int nb = start < 8 ? start : 8;
+  if (start > 0) {
+    const int nb = start < 11 ? start : 11;
     const int shift = start - nb;
     const uint32_t dmask = (1u << nb) - 1u;
-    uint4* h4 = reinterpret_cast<uint4*>(hist);
-    __syncwarp();  // the previous pass's reads of hist are done
-    h4[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
-    h4[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
-    __syncwarp();
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if ((u[j] & mask) == prefix) atomicAdd(&hist[(u[j] >> shift) & dmask], 1u);
-    __syncwarp();
-    // lane l holds bins 255 - 8l .. 248 - 8l (descending)
-    const uint4 g0 = h4[62 - 2 * lane], g1 = h4[63 - 2 * lane];
-    const int c8[8] = {(int)g1.w, (int)g1.z, (int)g1.y, (int)g1.x,
-                       (int)g0.w, (int)g0.z, (int)g0.y, (int)g0.x};
-    int own = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) own += c8[j];
-    const int incl = warp_incl_scan(own);
-    const int excl = incl - own;
-    int dl = 0, al = 0, nl = 0;
-    {
-      int acc = excl;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (acc < remaining && acc + c8[j] >= remaining) {
-          dl = 255 - 8 * lane - j;
-          al = acc;
-          nl = c8[j];
-        }
-        acc += c8[j];
+    for (int j = 0; j < NK; ++j) {
+      if (v[j]) {
+        const uint32_t d = (u[j] >> shift) & dmask;
+        atomicAdd(&sm.h11[d], 1u);
+        atomicAdd(&sm.coarse[d >> 5], 1u);
       }
     }
-    const uint32_t b = __ballot_sync(0xffffffffu, excl < remaining && incl >= remaining);
-    const int src = __ffs(b) - 1;
-    const int digit = __shfl_sync(0xffffffffu, dl, src);
-    const int above = __shfl_sync(0xffffffffu, al, src);
-    const int in_bin = __shfl_sync(0xffffffffu, nl, src);
+    __syncthreads();
+    const uint2 cc = *reinterpret_cast<const uint2*>(&sm.coarse[62 - 2 * lane]);
+    const int c_hi = (int)cc.y, c_lo = (int)cc.x;
+    int incl = warp_incl_scan(c_hi + c_lo);
+    int excl = incl - c_hi - c_lo;
+    uint32_t b = __ballot_sync(0xffffffffu, excl < remaining && incl >= remaining);
+    int src = __ffs(b) - 1;
+    const int cbin_l = (excl + c_hi >= remaining) ? 63 - 2 * lane : 62 - 2 * lane;
+    const int above_l = (excl + c_hi >= remaining) ? excl : excl + c_hi;
+    const int cbin = __shfl_sync(0xffffffffu, cbin_l, src);
+    const int above_c = __shfl_sync(0xffffffffu, above_l, src);
+    const int f = (int)sm.h11[cbin * 32 + 31 - lane];
+    incl = warp_incl_scan(f) + above_c;
+    excl = incl - f;
+    b = __ballot_sync(0xffffffffu, excl < remaining && incl >= remaining);
+    src = __ffs(b) - 1;
+    const int digit = cbin * 32 + 31 - src;
+    const int above = __shfl_sync(0xffffffffu, excl, src);
+    const int in_bin = __shfl_sync(0xffffffffu, f, src);
     prefix |= (uint32_t)digit << shift;
     mask |= dmask << shift;
     remaining -= above;
     start = shift;
     if (in_bin == remaining) {
       inclusive = true;
-    } else if (start > 0 && in_bin <= 32) {
-      // gather the bin's keys (index order) and rank them
-      int base = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const bool m = (u[j] & mask) == prefix;
-        const uint32_t bm = __ballot_sync(0xffffffffu, m);
-        if (m) cand[base + __popc(bm & lt)] = u[j];
-        base += __popc(bm);
-      }
-      __syncwarp();
-      const bool mine = lane < in_bin;
-      const uint32_t cu = mine ? cand[lane] : 0u;
-      int rank = 0, gt = 0;
-      for (int m = 0; m < in_bin; ++m) {
-        const uint32_t ou = cand[m];  // candidates are in index order: m < lane is lower
-        gt += ou > cu ? 1 : 0;
-        rank += (ou > cu || (ou == cu && m < lane)) ? 1 : 0;
-      }
-      const uint32_t bt = __ballot_sync(0xffffffffu, mine && rank == remaining - 1);
-      const int st = __ffs(bt) - 1;
-      prefix = __shfl_sync(0xffffffffu, cu, st);
-      remaining -= __shfl_sync(0xffffffffu, gt, st);
       start = 0;
-      __syncwarp();
+    } else if (start > 0 && in_bin <= 32) {
+#pragma unroll
+      for (int j = 0; j < NK; ++j) {
+        if (v[j] && (u[j] & mask) == prefix) {
+          const int slot = atomicAdd(&sm.ncand, 1);
+          sm.cand_u[slot] = u[j];
+          sm.cand_i[slot] = 4 * tid + j;
+        }
+      }
+      __syncthreads();
+      const bool mine = lane < in_bin;
+      const uint32_t cu = mine ? sm.cand_u[lane] : 0u;
+      const int ci = mine ? sm.cand_i[lane] : 0x7fffffff;
+      int rank = 0, gt = 0, eq = 0;
+      for (int m = 0; m < in_bin; ++m) {
+        const uint32_t ou = __shfl_sync(0xffffffffu, cu, m);
+        const int oi = __shfl_sync(0xffffffffu, ci, m);
+        gt += ou > cu ? 1 : 0;
+        eq += ou == cu ? 1 : 0;
+        rank += (ou > cu || (ou == cu && oi < ci)) ? 1 : 0;
+      }
+      b = __ballot_sync(0xffffffffu, mine && rank == remaining - 1);
+      src = __ffs(b) - 1;
+      prefix = __shfl_sync(0xffffffffu, cu, src);
+      const int gt_k = __shfl_sync(0xffffffffu, gt, src);
+      const int eq_k = __shfl_sync(0xffffffffu, eq, src);
+      // when every key equal to the k-th one is needed, the rule is simply "take >= prefix"
+      if (eq_k == remaining - gt_k) {
+        inclusive = true;
+      } else {
+        remaining -= gt_k;
+      }
+      start = 0;
     }
   }
-  // compaction in index order (round j, then lane)
-  const int need_eq = inclusive ? 0 : remaining;
-  int gt_acc = 0, eq_acc = 0;
+  const uint32_t inc = (warp & 1) ? 0x10000u : 1u;
+  for (int pass = 0; start > 0 && !inclusive; ++pass) {
+    const int nb = start < 8 ? start : 8;
+    const int shift = start - nb;
+    const uint32_t dmask = (1u << nb) - 1u;
+    uint32_t* H = &sm.hist[pass & 1][0][0];
+    uint32_t* row = H + (warp >> 1) * 256;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const bool g = inclusive ? u[j] >= prefix : u[j] > prefix;
-    const bool e = !inclusive && u[j] == prefix;
-    const uint32_t bg = __ballot_sync(0xffffffffu, g);
-    const uint32_t be = __ballot_sync(0xffffffffu, e);
-    const int eq_before = eq_acc + __popc(be & lt);
-    const int pos = gt_acc + __popc(bg & lt) + min(eq_before, need_eq);
-    if ((g || (e && eq_before < need_eq)) && pos < k) out[pos] = 32 * j + lane;
-    gt_acc += __popc(bg);
-    eq_acc += __popc(be);
+    for (int j = 0; j < NK; ++j)
+      if (v[j] && (u[j] & mask) == prefix) atomicAdd(&row[(u[j] >> shift) & dmask], inc);
+    __syncthreads();
+    const int bin = 255 - tid;
+    int own = 0;
+#pragma unroll
+    for (int pr = 0; pr < 4; ++pr) {
+      const uint32_t w = H[pr * 256 + bin];
+      own += (int)((w & 0xffffu) + (w >> 16));
+    }
+    const int incl_w = warp_incl_scan(own);
+    if (lane == 31) sm.wsum[warp] = incl_w;
+    reinterpret_cast<uint4*>(&sm.hist[(pass + 1) & 1][0][0])[tid] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    int before = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) before += (w < warp) ? sm.wsum[w] : 0;
+    const int incl = before + incl_w, excl = incl - own;
+    if (own > 0 && excl < remaining && incl >= remaining) {
+      sm.found[0] = bin;
+      sm.found[1] = excl;
+      sm.found[2] = own;
+    }
+    __syncthreads();
+    const int digit = sm.found[0], above = sm.found[1], in_bin = sm.found[2];
+    prefix |= (uint32_t)digit << shift;
+    mask |= dmask << shift;
+    remaining -= above;
+    start = shift;
+    if (in_bin == remaining) {
+      inclusive = true;
+      break;
+    }
   }
-  return gt_acc + min(eq_acc, need_eq);
+  // compaction in index order: thread t's keys are contiguous, so (warp, lane, j) is ascending
+  const uint32_t lt = (1u << lane) - 1u;
+  const int need_eq = inclusive ? 0 : remaining;
+  int cg = 0, ce = 0;
+  bool g[NK], e[NK];
+#pragma unroll
+  for (int j = 0; j < NK; ++j) {
+    g[j] = v[j] && (inclusive ? u[j] >= prefix : u[j] > prefix);
+    e[j] = v[j] && !inclusive && u[j] == prefix;
+    cg += g[j] ? 1 : 0;
+    ce += e[j] ? 1 : 0;
+  }
+  // warp-exclusive prefix of cg and ce (each 0..4) from the ballots of their bits
+  const uint32_t g0 = __ballot_sync(0xffffffffu, cg & 1);
+  const uint32_t g1 = __ballot_sync(0xffffffffu, cg & 2);
+  const uint32_t g2 = __ballot_sync(0xffffffffu, cg & 4);
+  int gb = __popc(g0 & lt) + 2 * __popc(g1 & lt) + 4 * __popc(g2 & lt);
+  const int gw = __popc(g0) + 2 * __popc(g1) + 4 * __popc(g2);
+  int eb = 0, ew = 0;
+  if (!inclusive) {
+    const uint32_t e0 = __ballot_sync(0xffffffffu, ce & 1);
+    const uint32_t e1 = __ballot_sync(0xffffffffu, ce & 2);
+    const uint32_t e2 = __ballot_sync(0xffffffffu, ce & 4);
+    eb = __popc(e0 & lt) + 2 * __popc(e1 & lt) + 4 * __popc(e2 & lt);
+    ew = __popc(e0) + 2 * __popc(e1) + 4 * __popc(e2);
+  }
+  if (lane == 0) sm.cnt[0][warp] = ((uint32_t)gw << 16) | (uint32_t)ew;
+  __syncthreads();
+  const uint4 c0 = reinterpret_cast<const uint4*>(sm.cnt[0])[0];
+  const uint4 c1 = reinterpret_cast<const uint4*>(sm.cnt[0])[1];
+  const uint32_t c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  uint32_t below = 0u, all = 0u;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    below += (w < warp) ? c[w] : 0u;
+    all += c[w];
+  }
+  gb += (int)(below >> 16);
+  eb += (int)(below & 0xffffu);
+#pragma unroll
+  for (int j = 0; j < NK; ++j) {
+    const bool take = g[j] || (e[j] && eb < need_eq);
+    const int pos = gb + min(eb, need_eq);
+    if (take && pos < k) out[pos] = 4 * tid + j;
+    gb += g[j] ? 1 : 0;
+    eb += e[j] ? 1 : 0;
+  }
+  return (int)(all >> 16) + min((int)(all & 0xffffu), need_eq);
 }
 
 }  // namespace rkv

@@ -324,12 +324,30 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(A a) {
   if (!dense) {
     // ---- channel pick: top-c of sum_h |q_h| (ties -> lower channel), ascending -----------
     const int cn = a.channels;
-    if (warp == 0) {
-      // warp-private scratch: the first 256 words of the page select's fine histogram (cleared
-      // again before that select) and 32 words of its second fallback buffer
-      const int got = warp_topk128(umag, cn, chosen, sel_smem.fast.h11,
-                                   &sel_smem.fast.hist[1][0][0]);
-      if (got != cn && lane == 0) set_status(a.status, RKV_DEV_SELECT_FAILED);
+    if (warp < 4) {
+      // thread i ranks channel i among all 128 by the unique key (value, 127 - i), so ties go
+      // to the lower channel; ranks are a permutation, so exactly the channels of rank < cn are
+      // taken, and per-warp ballots place them in ascending channel order
+      const uint64_t mine = ((uint64_t)umag[tid] << 32) | (uint32_t)(kHeadDim - 1 - tid);
+      const uint4* u4 = reinterpret_cast<const uint4*>(umag);
+      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+#pragma unroll 8
+      for (int j4 = 0; j4 < kHeadDim / 4; ++j4) {
+        const uint4 x = u4[j4];
+        const uint32_t j = kHeadDim - 1 - 4 * j4;
+        r0 += ((((uint64_t)x.x << 32) | j) > mine) ? 1 : 0;
+        r1 += ((((uint64_t)x.y << 32) | (j - 1)) > mine) ? 1 : 0;
+        r2 += ((((uint64_t)x.z << 32) | (j - 2)) > mine) ? 1 : 0;
+        r3 += ((((uint64_t)x.w << 32) | (j - 3)) > mine) ? 1 : 0;
+      }
+      const bool take = r0 + r1 + r2 + r3 < cn;
+      const uint32_t b = __ballot_sync(0xffffffffu, take);
+      if (lane == 0) sel_smem.fast.wsum[warp] = __popc(b);
+      group_sync(0);  // warps 0..3
+      int before = 0;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) before += (w < warp) ? sel_smem.fast.wsum[w] : 0;
+      if (take) chosen[before + __popc(b & ((1u << lane) - 1u))] = tid;
     }
     __syncthreads();
     if (a.sel_channels && tid < cn) a.sel_channels[(size_t)ukv * cn + tid] = chosen[tid];
@@ -398,7 +416,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(A a) {
     } else {
       int got;
       if (P <= 1024)
-        got = block_topk_fast<4>(scores, P, S, sel, sel_smem.fast);
+        got = block_topk_1024(scores, P, S, sel, sel_smem.fast);
       else if (P <= 2048)
         got = block_topk_fast<8>(scores, P, S, sel, sel_smem.fast);
       else if (P <= 4096)
