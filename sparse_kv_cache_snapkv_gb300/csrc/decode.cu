@@ -139,11 +139,11 @@ struct MmaAttn {
     mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
     mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
     const float mn = fmaxf(m, mt);
-    const float alpha = exp2f(m - mn);
+    const float alpha = fast_exp2(m - mn);
     m = mn;
     // P in bf16 (the A operand of P V); l sums the same rounded values
-    const __nv_bfloat162 p01 = __floats2bfloat162_rn(exp2f(s[0] - mn), exp2f(s[1] - mn));
-    const __nv_bfloat162 p23 = __floats2bfloat162_rn(exp2f(s[2] - mn), exp2f(s[3] - mn));
+    const __nv_bfloat162 p01 = __floats2bfloat162_rn(fast_exp2(s[0] - mn), fast_exp2(s[1] - mn));
+    const __nv_bfloat162 p23 = __floats2bfloat162_rn(fast_exp2(s[2] - mn), fast_exp2(s[3] - mn));
     const float2 f01 = __bfloat1622float2(p01), f23 = __bfloat1622float2(p23);
     l = l * alpha + ((f01.x + f01.y) + (f23.x + f23.y));
     const uint32_t pa0 = *reinterpret_cast<const uint32_t*>(&p01);
@@ -208,7 +208,7 @@ __device__ __forceinline__ void warp_merge(const CombineSmem<G>* cs, int h, int 
   float ll = 0.f, oo = 0.f;
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
-    const float f = exp2f(cs->m[w][h] - mm);
+    const float f = fast_exp2(cs->m[w][h] - mm);
     ll = fmaf(cs->l[w][h], f, ll);
     oo = fmaf(cs->o[w][h][c], f, oo);
   }
@@ -516,7 +516,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(A a) {
     float ll = 0.f, o0 = 0.f, o1 = 0.f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-      const float f = exp2f(cs->m[w][h] - mm);
+      const float f = fast_exp2(cs->m[w][h] - mm);
       const float2 x = *reinterpret_cast<const float2*>(&cs->o[w][h][c]);
       ll = fmaf(cs->l[w][h], f, ll);
       o0 = fmaf(f, x.x, o0);
@@ -893,7 +893,7 @@ __global__ void dense_combine_kernel(DenseArgs a) {
   for (int s = 0; s < a.nsplit; ++s) M = fmaxf(M, pm[s]);
   float L = 0.f, O = 0.f;
   for (int s = 0; s < a.nsplit; ++s) {
-    const float f = exp2f(pm[s] - M);
+    const float f = fast_exp2(pm[s] - M);
     L = fmaf(pl[s], f, L);
     O = fmaf(po[(size_t)s * kHeadDim + c], f, O);
   }

@@ -375,8 +375,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             float a4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              a4[j & 3] += exp2f(fmaf(__uint_as_float(r[j]), p.scale_log2, nmn));
-            l = l * exp2f(m - mn) + ((a4[0] + a4[1]) + (a4[2] + a4[3]));
+              a4[j & 3] += fast_exp2(fmaf(__uint_as_float(r[j]), p.scale_log2, nmn));
+            l = l * fast_exp2(m - mn) + ((a4[0] + a4[1]) + (a4[2] + a4[3]));
             m = mn;
           }
           tc_fence_before();
@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           if (hf == 0) {
             const float m2 = xch_m[lrow], l2 = xch_l[lrow];
             const float mn = fmaxf(m, m2);
-            l = l * exp2f(m - mn) + l2 * exp2f(m2 - mn);
+            l = l * fast_exp2(m - mn) + l2 * fast_exp2(m2 - mn);
             m = mn;
           }
           named_bar_sync(1, kEpiThreads);  // xch is rewritten by the next item
@@ -428,10 +428,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 #pragma unroll
               for (int i4 = 0; i4 < 8; ++i4) {
                 const float4 v = nl[i4];  // negated log-sum-exp of four window rows
-                a4[0] += exp2f(fmaf(__uint_as_float(r[4 * i4 + 0]), p.scale_log2, v.x));
-                a4[1] += exp2f(fmaf(__uint_as_float(r[4 * i4 + 1]), p.scale_log2, v.y));
-                a4[2] += exp2f(fmaf(__uint_as_float(r[4 * i4 + 2]), p.scale_log2, v.z));
-                a4[3] += exp2f(fmaf(__uint_as_float(r[4 * i4 + 3]), p.scale_log2, v.w));
+                a4[0] += fast_exp2(fmaf(__uint_as_float(r[4 * i4 + 0]), p.scale_log2, v.x));
+                a4[1] += fast_exp2(fmaf(__uint_as_float(r[4 * i4 + 1]), p.scale_log2, v.y));
+                a4[2] += fast_exp2(fmaf(__uint_as_float(r[4 * i4 + 2]), p.scale_log2, v.z));
+                a4[3] += fast_exp2(fmaf(__uint_as_float(r[4 * i4 + 3]), p.scale_log2, v.w));
               }
             }
             acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
@@ -479,7 +479,7 @@ __global__ void lse_merge_kernel(ScoreParams p, int rp) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const float mn = fmaxf(m, x[j].x);
-        l = l * exp2f(m - mn) + x[j].y * exp2f(x[j].x - mn);
+        l = l * fast_exp2(m - mn) + x[j].y * fast_exp2(x[j].x - mn);
         m = mn;
       }
     }
