@@ -141,6 +141,11 @@ __device__ __forceinline__ void cp_async16(void* dst_smem, const void* src_gmem)
                "l"(src_gmem)
                : "memory");
 }
+__device__ __forceinline__ void cp_async4(void* dst_smem, const void* src_gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst_smem)),
+               "l"(src_gmem)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }

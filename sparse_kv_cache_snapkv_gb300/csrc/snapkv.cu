@@ -559,6 +559,80 @@ __device__ __forceinline__ int sel_slot(int i) { return i + (i >> 5); }
 
 size_t select_fast_smem_bytes() { return (size_t)(kSelMaxN + kSelMaxN / 32) * 4; }
 
+// Max pooling in registers for r = 2^k - 1 <= 15 known at compile time. Thread t holds positions
+// base .. base + 31 in x[] (-inf past n). A doubling step m_2w[q] = max(m_w[q], m_w[q + w]) takes
+// the next thread's first w values by a shuffle, and lane 31 takes them from lane 0 of the next
+// warp through xch (one buffer per step, so one barrier per step). Ascending q reads x[q + w]
+// before it is updated.
+template <int W>
+__device__ __forceinline__ void reg_double_step(float (&x)[kSelPerThread], float* xch, int lane,
+                                                int warp) {
+  if (lane == 0) {
+#pragma unroll
+    for (int j = 0; j < W; ++j) xch[warp * 8 + j] = x[j];
+  }
+  float halo[W];
+#pragma unroll
+  for (int j = 0; j < W; ++j) halo[j] = __shfl_down_sync(0xffffffffu, x[j], 1);
+  __syncthreads();
+  if (lane == 31) {
+#pragma unroll
+    for (int j = 0; j < W; ++j)
+      halo[j] = (warp + 1 < kSelThreads / 32) ? xch[(warp + 1) * 8 + j] : -INFINITY;
+  }
+#pragma unroll
+  for (int q = 0; q < kSelPerThread; ++q)
+    x[q] = fmaxf(x[q], (q + W < kSelPerThread) ? x[q + W] : halo[q + W - kSelPerThread]);
+}
+
+// After the doubling steps (w = R + 1): pooled[i] = max(m_w[max(0, i - R)], m_w[i]), with the
+// previous thread's last R values by a shuffle (lane 0: from lane 31 of the previous warp through
+// xch; thread 0 clips to position 0), written straight out as ordered keys with their range.
+template <int R>
+__device__ __forceinline__ void reg_pool_keys(const float (&x)[kSelPerThread], float* xch,
+                                              uint32_t* key, int base, int n, int lane, int warp,
+                                              uint32_t& hi, uint32_t& lo) {
+  if constexpr (R > 0) {
+    if (lane == 31) {
+#pragma unroll
+      for (int j = 0; j < R; ++j) xch[warp * 16 + j] = x[kSelPerThread - R + j];
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int q = 0; q < kSelPerThread; ++q) {
+    float m = x[q];
+    if constexpr (R > 0) {
+      float prev;
+      if (q >= R) {
+        prev = x[q - R];
+      } else {
+        prev = __shfl_up_sync(0xffffffffu, x[kSelPerThread - R + q], 1);
+        if (lane == 0) prev = warp > 0 ? xch[(warp - 1) * 16 + q] : x[0];
+      }
+      m = fmaxf(m, prev);
+    }
+    const int i = base + q;
+    if (i < n) {
+      const uint32_t kk = ordered_key(m);
+      key[sel_slot(i)] = kk;
+      hi = max(hi, kk);
+      lo = min(lo, kk);
+    }
+  }
+}
+
+template <int R>
+__device__ __forceinline__ void reg_max_pool(float (&x)[kSelPerThread], float* xch, uint32_t* key,
+                                             int base, int n, int lane, int warp, uint32_t& hi,
+                                             uint32_t& lo) {
+  if constexpr (R >= 1) reg_double_step<1>(x, xch + 0 * 256, lane, warp);
+  if constexpr (R >= 3) reg_double_step<2>(x, xch + 1 * 256, lane, warp);
+  if constexpr (R >= 7) reg_double_step<4>(x, xch + 2 * 256, lane, warp);
+  if constexpr (R >= 15) reg_double_step<8>(x, xch + 3 * 256, lane, warp);
+  reg_pool_keys<R>(x, xch + 4 * 256, key, base, n, lane, warp, hi, lo);
+}
+
 // Max pooling over [max(0, i - r), min(n - 1, i + r)] for 2r + 1 = 2^k - 1 by doubling: with
 // m_w[i] = max over [i, min(i + w - 1, n - 1)], m_{2w}[i] = max(m_w[i], m_w[i + w]); once
 // w = r + 1, the pooled value is max(m_w[max(0, i - r)], m_w[i]) (the two runs meet or overlap
@@ -569,6 +643,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_fast_kernel(SnapArgs a)
   __shared__ int wsum[32], wsum2[32];
   __shared__ uint32_t wmax[32], wmin[32];
   __shared__ int found[4];
+  __shared__ float xch[4 * 256 + 32 * 16];  // pooling exchange: 4 doubling steps, final step
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ukv = blockIdx.x;
   const int u = ukv / a.n_kv, g = ukv - u * a.n_kv;
@@ -589,12 +664,34 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_fast_kernel(SnapArgs a)
   const int ks = a.kernel_size > 0 ? a.kernel_size : adaptive_kernel(L);
   const int r = ks / 2;
   const float* in = a.scores + (size_t)ukv * (a.max_len - W);
-  for (int i = tid; i < n; i += kSelThreads) sh[sel_slot(i)] = in[i];
+  // coalesced 4-byte asynchronous copies (position tid + 1024 q), all in flight at once
+#pragma unroll
+  for (int q = 0; q < kSelPerThread; ++q) {
+    const int i = tid + q * kSelThreads;
+    if (i < n) cp_async4(sh + sel_slot(i), in + i);
+  }
+  cp_async_commit();
   for (int i = tid; i < 2048; i += kSelThreads) hist[i] = 0u;
+  cp_async_wait_all();
   __syncthreads();
 
   const int base = tid * kSelPerThread;
   float x[kSelPerThread];
+  uint32_t hi = 0u, lo = 0xffffffffu;
+  uint32_t* key = reinterpret_cast<uint32_t*>(sh);
+  if (!a.pool_avg && (r == 0 || r == 1 || r == 3 || r == 7 || r == 15)) {
+    // the thread's run, then pooling in registers; keys written by the last step
+#pragma unroll
+    for (int q = 0; q < kSelPerThread; ++q)
+      x[q] = (base + q < n) ? sh[sel_slot(base + q)] : -INFINITY;
+    switch (r) {
+      case 0: reg_max_pool<0>(x, xch, key, base, n, lane, warp, hi, lo); break;
+      case 1: reg_max_pool<1>(x, xch, key, base, n, lane, warp, hi, lo); break;
+      case 3: reg_max_pool<3>(x, xch, key, base, n, lane, warp, hi, lo); break;
+      case 7: reg_max_pool<7>(x, xch, key, base, n, lane, warp, hi, lo); break;
+      default: reg_max_pool<15>(x, xch, key, base, n, lane, warp, hi, lo); break;
+    }
+  } else {
   if (a.pool_avg) {
     // mean over the clipped window: a fixed-point sum slid over the thread's 32 positions
     long long sum = 0;
@@ -642,8 +739,6 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_fast_kernel(SnapArgs a)
     }
   }
   __syncthreads();
-  uint32_t hi = 0u, lo = 0xffffffffu;
-  uint32_t* key = reinterpret_cast<uint32_t*>(sh);
 #pragma unroll
   for (int q = 0; q < kSelPerThread; ++q) {
     const int i = base + q;
@@ -653,6 +748,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_fast_kernel(SnapArgs a)
       hi = max(hi, kk);
       lo = min(lo, kk);
     }
+  }
   }
   hi = __reduce_max_sync(0xffffffffu, hi);
   lo = __reduce_min_sync(0xffffffffu, lo);
