@@ -146,6 +146,11 @@ __device__ __forceinline__ void cp_async4(void* dst_smem, const void* src_gmem) 
                "l"(src_gmem)
                : "memory");
 }
+// Hint: bring `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src_gmem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }

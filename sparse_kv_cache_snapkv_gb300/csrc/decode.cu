@@ -318,12 +318,36 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(A a) {
     qg[tid] = t;
   }
   __syncthreads();
-  if (warp == 7) MmaAttn<G>::build_fragments(qs, qfrag);  // overlaps the channel pick
 
   int nsel;
   if (!dense) {
     // ---- channel pick: top-c of sum_h |q_h| (ties -> lower channel), ascending -----------
     const int cn = a.channels;
+    if (warp >= 4) {
+      // Meanwhile warps 4..7 bring the summary rows of every channel that can still be picked
+      // into L2: warp 4 + v finds the ceil(cn / 4)-th largest key of channels 32v .. 32v + 31;
+      // those four top sets hold at least cn channels, all at or above the smallest of the
+      // four bounds, so the picked channels are among the channels that reach it.
+      const int c = tid - 128;
+      const uint32_t mine = umag[c];
+      const int kw = (cn + 3) >> 2;
+      uint32_t v = mine, m = 0u;
+      for (int i = 0; i < kw; ++i) {
+        m = __reduce_max_sync(0xffffffffu, v);
+        const uint32_t who = __ballot_sync(0xffffffffu, v == m);
+        if (lane == __ffs(who) - 1) v = 0u;  // one instance leaves
+      }
+      if (lane == 0) sel_smem.fast.wmin[warp - 4] = m;
+      group_sync(1);  // warps 4..7
+      const uint32_t bound = min(min(sel_smem.fast.wmin[0], sel_smem.fast.wmin[1]),
+                                 min(sel_smem.fast.wmin[2], sel_smem.fast.wmin[3]));
+      if (mine >= bound) {
+        const bf16* row = ((qg[c] >= 0.f) ? a.kmax : a.kmin) +
+                          ((size_t)ukv * kHeadDim + c) * a.page_cap;
+        prefetch_l2_bulk(row, (uint32_t)((P * 2 + 15) & ~15));
+      }
+      if (warp == 7) MmaAttn<G>::build_fragments(qs, qfrag);
+    }
     if (warp < 4) {
       // thread i ranks channel i among all 128 by the unique key (value, 127 - i), so ties go
       // to the lower channel; ranks are a permutation, so exactly the channels of rank < cn are
@@ -427,6 +451,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(A a) {
       nsel = S;
     }
   } else {
+    if (warp == 7) MmaAttn<G>::build_fragments(qs, qfrag);
     if (a.sel_channels && tid < a.channels) a.sel_channels[(size_t)ukv * a.channels + tid] = -1;
     for (int i = tid; i < P; i += kDecodeThreads) sel[i] = i;
     nsel = P;
