@@ -404,12 +404,15 @@ def _profiled_traffic(kernel_name):
     for line in lines:
         cells = [c.strip() for c in line.strip().strip("|").split("|")]
         if len(cells) == 5 and cells[0] == kernel_name:
-            src = os.path.join(ROOT, "sparse_kv_cache_snapkv_gb300", "csrc", cells[3])
+            # the hash covers every file named ("a.cu+common.cuh"), read in that order
+            h = hashlib.sha256()
             try:
-                digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+                for name in cells[3].split("+"):
+                    src = os.path.join(ROOT, "sparse_kv_cache_snapkv_gb300", "csrc", name.strip())
+                    h.update(open(src, "rb").read())
             except OSError:
                 return None
-            return int(cells[1]) if digest == cells[4] else None
+            return int(cells[1]) if h.hexdigest()[:16] == cells[4] else None
     return None
 
 
