@@ -175,6 +175,19 @@ def test_snapkv_avg_pool(lens, kernel):
     assert not torch.equal(res[2], res_max[2])
 
 
+@pytest.mark.parametrize("kernel", [1, 3, 7, 15, 31])
+def test_snapkv_select_tiny_prefixes(kernel):
+    # prefixes of 8, 33 and 68 scores: one, two and three threads of the shared-memory select
+    # hold positions, so the register pooling's neighbour exchange meets the end of the scores
+    # inside a warp; pooling windows wider than the prefix clip at both ends
+    rkv = _lib()
+    W, keep = 32, 36
+    wl, x = _inputs(3, 1, 4, [40, 65, 100], W, seed=110, needles=0)
+    res = _run(rkv, x, W, kernel, keep)
+    for u in range(3):
+        _check_unit(x, u, 0, 4, W, kernel, keep, *res, tag=f"kernel {kernel} u{u}")
+
+
 def test_snapkv_per_head_without_group_sum():
     # SnapKV without the GQA enhancement: each query head is scored with its own window rows and
     # keeps its own rows of its K/V head; ragged lengths, one prompt shorter than keep
