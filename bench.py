@@ -334,7 +334,10 @@ def run_ours(args):
                 "frac": round(comp_gbs / hbm_peak, 4), "traffic": None,
                 "peak_source": peak_src, "bytes_per_launch": comp_bytes,
                 "launch_us": round(comp_ms * 1e3, 1)}
-    traffic = _profiled_traffic(roof["kernel"])
+    # the committed capture is of the default workload at 32 layers: other shapes get null
+    traffic = None
+    if args.workload == "llama8b_32k" and wl.n_layers == 32:
+        traffic = _profiled_traffic(roof["kernel"])
     if traffic is not None:
         roof["traffic"] = traffic
 
