@@ -10,10 +10,11 @@
 // attention), "Are Different KV Tokens Retrieved at Each Decoding Step?" (selection per step).
 //
 // Memory movement: the approximate scores read the kept channels' summary rows straight from
-// global memory into registers (a vector-matrix product: fp32 FMAs, no staging); the K/V rows of
-// the selected pages are staged in shared memory by 16-byte cp.async copies, each warp group
-// the 64-token chunk it attends over, rows padded by 16 bytes so that ldmatrix reads them
-// without bank conflicts.
+// global memory into registers (a vector-matrix product: fp32 FMAs, no staging), after the
+// channel pick has brought every channel that can still be picked into L2; the K/V rows of the
+// selected pages are staged in shared memory by 16-byte cp.async copies, each warp the 16-token
+// unit it attends over (the dense decode: each warp group a 64-token chunk), rows padded by
+// 16 bytes so that ldmatrix reads them without bank conflicts.
 //
 // Attention arithmetic: warp-level mma.sync m16n8k16 (bf16 in, fp32 accumulate). The G query
 // heads of a KV group are the rows of the A operand (padded to 16 with zeros); each warp takes 16
