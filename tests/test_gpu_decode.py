@@ -83,9 +83,11 @@ def test_summaries_incremental_first_token():
         assert torch.equal(kmax[u, :, :, :P], full_max[u, :, :, :P])
 
 
-def _hybrid_case(n, n_kv, gqa, lens, cap, budget, page, channels, seed, steps=2):
+def _hybrid_case(n, n_kv, gqa, lens, cap, budget, page, channels, seed, steps=2, tweak=None):
     rkv = _lib()
     k, v = _make_cache(n, n_kv, cap, lens, seed)
+    if tweak is not None:
+        tweak(k, v)
     page_cap = _page_cap(cap, page)
     lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
     kmin, kmax = _summaries(rkv, k, lens_t, page, page_cap)
@@ -282,6 +284,60 @@ def test_device_status_len_over_cap():
     assert ei.value.bits & 1
     # the word is cleared by the check
     assert rkv.rkv_check_status(ws) == 0
+
+
+def test_hybrid_page_select_heavy_tail():
+    # a few pages whose keys are 300x larger: the linear first pass puts the other pages into a
+    # handful of bins, so the page select needs its second pass over the crowded bin
+    def tweak(k, v):
+        k[:, :, 40:52] *= 300
+        k[:, :, 2000:2004] *= -300
+    _hybrid_case(2, 2, 4, [4096, 3001], 4096, 256, 4, 32, seed=61, steps=3, tweak=tweak)
+
+
+def test_hybrid_page_select_crowded_equal_scores():
+    # 1004 identical pages (equal approximate scores) and 20 pages with 4x larger keys: the
+    # k-th page lies among a thousand equal scores, which only the radix form resolves; the
+    # equal pages are then taken lowest index first, checked exactly on the kernel's own scores
+    rkv = _lib()
+    n, n_kv, gqa, L, B, page, C = 1, 2, 4, 4096, 256, 4, 32
+    k, v = _make_cache(n, n_kv, L, [L], seed=63)
+    row = k[:, :, 0:1].clone()
+    k[:, :, :] = row.expand(-1, -1, L, -1)
+    k[:, :, 4000:4080] = row.expand(-1, -1, 80, -1) * 4
+    lens_t = torch.tensor([L], dtype=torch.int32, device="cuda")
+    page_cap = _page_cap(L, page)
+    kmin, kmax = _summaries(rkv, k, lens_t, page, page_cap)
+    S = B // 2 // page
+    q = row[:, :, 0].repeat_interleave(gqa, dim=1).float()
+    q = (q + 0.01 * torch.randn(q.shape, generator=torch.Generator().manual_seed(64)).cuda())
+    q = q.to(torch.bfloat16)
+    out = torch.empty_like(q)
+    sel_c = torch.empty(n, n_kv, C, dtype=torch.int32, device="cuda")
+    sel_p = torch.empty(n, n_kv, S, dtype=torch.int32, device="cuda")
+    approx = torch.zeros(n, n_kv, page_cap, dtype=torch.float32, device="cuda")
+    scale = 1.0 / math.sqrt(D)
+    ws = rkv.rkv_hybrid_decode(q, k, v, lens_t, kmin, kmax, B, page, C, scale, out,
+                               sel_channels=sel_c, sel_pages=sel_p, approx_scores=approx)
+    rkv.rkv_check_status(ws)
+    kk, vv, qq = _f64(k), _f64(v), _f64(q)
+    P = L // page
+    for g in range(n_kv):
+        a = approx[0, g, :P].cpu().numpy().astype(np.float64)
+        order = np.lexsort((np.arange(P), -a))
+        gp = sel_p[0, g].cpu().numpy()
+        assert np.array_equal(gp, np.sort(order[:S])), f"kv {g}: exact rule on own scores"
+        # the k-th score is shared by hundreds of pages
+        assert (a == a[order[S - 1]]).sum() > 1000, f"kv {g}: case not crowded"
+        # and the selection is the oracle's within the tie band
+        qh = qq[0, g * gqa:(g + 1) * gqa]
+        rmin, rmax = O.page_summaries(kk[0, g], L, page)
+        gch = np.sort(sel_c[0, g].cpu().numpy())
+        ref_a = O.approx_scores(qh.sum(axis=0), gch, rmin, rmax)
+        parity.check_selection(gp, ref_a, S, f"kv {g} pages")
+        toks = np.concatenate([np.arange(pg * page, (pg + 1) * page) for pg in gp])
+        parity.check_output(_f64(out[0, g * gqa:(g + 1) * gqa]),
+                            O.attention(qh, kk[0, g][toks], vv[0, g][toks], scale), f"kv {g}")
 
 
 def test_hybrid_exact_ties_take_lowest_pages_and_channels():
