@@ -376,8 +376,6 @@ struct __align__(16) FastSelectSmem {
   uint32_t h11[2048];        // fine histogram of the first pass (up to 11 bits)
   uint32_t coarse[64];       // the same counts summed over 32 fine bins
   uint32_t hist[2][4][256];  // 8-bit fallback passes, double-buffered; warps 2p, 2p+1 share row p
-  uint32_t h10[1024];        // block_topk_1024: second pass over the first pass's bin
-  uint32_t coarse10[32];
   uint32_t wmax[8], wmin[8];
   int wsum[8];               // per-warp sums of a fallback pass's descending bin scan
   int found[4];              // fallback pass: digit, keys above, keys in the digit's bin
@@ -390,8 +388,6 @@ struct __align__(16) FastSelectSmem {
 static_assert(offsetof(FastSelectSmem, h11) % 16 == 0, "h11 alignment");
 static_assert(offsetof(FastSelectSmem, coarse) % 16 == 0, "coarse alignment");
 static_assert(offsetof(FastSelectSmem, hist) % 16 == 0, "hist alignment");
-static_assert(offsetof(FastSelectSmem, h10) % 16 == 0, "h10 alignment");
-static_assert(offsetof(FastSelectSmem, coarse10) % 16 == 0, "coarse10 alignment");
 static_assert(offsetof(FastSelectSmem, wmax) % 16 == 0, "wmax alignment");
 static_assert(offsetof(FastSelectSmem, wmin) % 16 == 0, "wmin alignment");
 static_assert(offsetof(FastSelectSmem, cnt) % 16 == 0, "cnt alignment");
@@ -413,8 +409,6 @@ __device__ __forceinline__ void fast_select_prepare(uint32_t hi, uint32_t lo, Fa
   h[2 * tid + 1] = make_uint4(0u, 0u, 0u, 0u);
   if (tid < 16) reinterpret_cast<uint4*>(sm.coarse)[tid] = make_uint4(0u, 0u, 0u, 0u);
   reinterpret_cast<uint4*>(&sm.hist[0][0][0])[tid] = make_uint4(0u, 0u, 0u, 0u);
-  reinterpret_cast<uint4*>(sm.h10)[tid] = make_uint4(0u, 0u, 0u, 0u);
-  if (tid < 8) reinterpret_cast<uint4*>(sm.coarse10)[tid] = make_uint4(0u, 0u, 0u, 0u);
   if (tid == 0) sm.ncand = 0;
 }
 
@@ -609,9 +603,8 @@ __device__ __forceinline__ int block_topk_fast(const float* keys, int n, int k, 
 // 16-byte load; `keys` 16-byte aligned): the radix steps are the same, and the compaction needs
 // one ballot per bit of a thread's 0..4 taken keys, because (warp, lane, j) is already index
 // order. A ranked k-th key whose equal keys are all needed turns the rule into "take >= it",
-// which skips the count of equal keys. Ends without a barrier. (The fallback of
-// block_topk_1024.)
-__device__ __forceinline__ int block_topk_1024_radix(const float* keys, int n, int k, int* out,
+// which skips the count of equal keys. Ends without a barrier.
+__device__ __forceinline__ int block_topk_1024(const float* keys, int n, int k, int* out,
                                              FastSelectSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NK = 4;
@@ -808,226 +801,6 @@ __device__ __forceinline__ int block_topk_1024_radix(const float* keys, int n, i
     const bool take = g[j] || (e[j] && eb < need_eq);
     const int pos = gb + min(eb, need_eq);
     if (take && pos < k) out[pos] = 4 * tid + j;
-    gb += g[j] ? 1 : 0;
-    eb += e[j] ? 1 : 0;
-  }
-  return (int)(all >> 16) + min((int)(all & 0xffffu), need_eq);
-}
-
-
-__device__ __forceinline__ float ordered_key_value(uint32_t u) {
-  return (u & 0x80000000u) ? __uint_as_float(u & 0x7fffffffu) : __uint_as_float(~u);
-}
-
-// Top-k for n <= 1024 keys (thread t: keys 4t .. 4t + 3 in shared memory, `keys` 16-byte
-// aligned; after fast_select_prepare), k >= 1. Same contract as block_topk_fast (k largest, ties
-// -> lower index, indices written ascending; returns the count). The first pass bins the keys
-// linearly over the value range [min, max] into 2048 bins (64 coarse x 32 fine), which resolves
-// far more keys than bins of the float's top bits; a bin is monotone in the value, so every key
-// of a higher bin is larger. The k-th key's bin is taken whole when it holds exactly the keys
-// still needed; a bin of at most 32 keys is ranked directly; a larger one gets a second linear
-// pass over its own interval (1024 bins), then the same two cases. What remains (more than 32
-// keys in one second-pass bin, i.e. equal or nearly equal keys, or no finite range) runs
-// block_topk_1024_radix. Ends without a barrier.
-__device__ __forceinline__ int block_topk_1024(const float* keys, int n, int k, int* out,
-                                               FastSelectSmem& sm) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int NK = 4;
-  float x[NK];
-  uint32_t u[NK];
-  bool v[NK];
-  {
-    const int i0 = 4 * tid;
-    if (i0 + 3 < n) {
-      const float4 f = reinterpret_cast<const float4*>(keys)[tid];
-      x[0] = f.x;
-      x[1] = f.y;
-      x[2] = f.z;
-      x[3] = f.w;
-      v[0] = v[1] = v[2] = v[3] = true;
-    } else {
-#pragma unroll
-      for (int j = 0; j < NK; ++j) {
-        v[j] = i0 + j < n;
-        x[j] = v[j] ? keys[i0 + j] : 0.f;
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < NK; ++j) u[j] = ordered_key(x[j]);
-  }
-  uint32_t hi, lo;
-  {
-    const uint4 a0 = reinterpret_cast<const uint4*>(sm.wmax)[0];
-    const uint4 a1 = reinterpret_cast<const uint4*>(sm.wmax)[1];
-    const uint4 b0 = reinterpret_cast<const uint4*>(sm.wmin)[0];
-    const uint4 b1 = reinterpret_cast<const uint4*>(sm.wmin)[1];
-    hi = max(max(max(a0.x, a0.y), max(a0.z, a0.w)), max(max(a1.x, a1.y), max(a1.z, a1.w)));
-    lo = min(min(min(b0.x, b0.y), min(b0.z, b0.w)), min(min(b1.x, b1.y), min(b1.z, b1.w)));
-  }
-  const float flo = ordered_key_value(lo);
-  const float span = ordered_key_value(hi) - flo;
-  if (!(span > 0.f) || !(span < INFINITY)) return block_topk_1024_radix(keys, n, k, out, sm);
-  const float scale = 2048.f / span;
-  // ---- first pass: 2048 linear bins ----------------------------------------------------
-  float pos[NK];  // the key's position in bin units, monotone in its value
-  int b[NK];
-#pragma unroll
-  for (int j = 0; j < NK; ++j) {
-    pos[j] = (x[j] - flo) * scale;
-    b[j] = v[j] ? min(2047, max(0, (int)pos[j])) : -1;
-    if (v[j]) {
-      atomicAdd(&sm.h11[b[j]], 1u);
-      atomicAdd(&sm.coarse[b[j] >> 5], 1u);
-    }
-  }
-  __syncthreads();
-  int remaining = k;
-  int D, in_bin;
-  {
-    const uint2 cc = *reinterpret_cast<const uint2*>(&sm.coarse[62 - 2 * lane]);
-    const int c_hi = (int)cc.y, c_lo = (int)cc.x;
-    int incl = warp_incl_scan(c_hi + c_lo);
-    int excl = incl - c_hi - c_lo;
-    uint32_t bal = __ballot_sync(0xffffffffu, excl < remaining && incl >= remaining);
-    int src = __ffs(bal) - 1;
-    const int cbin_l = (excl + c_hi >= remaining) ? 63 - 2 * lane : 62 - 2 * lane;
-    const int above_l = (excl + c_hi >= remaining) ? excl : excl + c_hi;
-    const int cbin = __shfl_sync(0xffffffffu, cbin_l, src);
-    const int above_c = __shfl_sync(0xffffffffu, above_l, src);
-    const int f = (int)sm.h11[cbin * 32 + 31 - lane];
-    incl = warp_incl_scan(f) + above_c;
-    excl = incl - f;
-    bal = __ballot_sync(0xffffffffu, excl < remaining && incl >= remaining);
-    src = __ffs(bal) - 1;
-    D = cbin * 32 + 31 - src;
-    remaining -= __shfl_sync(0xffffffffu, excl, src);
-    in_bin = __shfl_sync(0xffffffffu, f, src);
-  }
-  // sub[j]: the key's bin in the second pass (-1 outside bin D); D2 = -1 while unused
-  int sub[NK];
-  int D2 = -1;
-#pragma unroll
-  for (int j = 0; j < NK; ++j) sub[j] = -1;
-  if (in_bin != remaining && in_bin > 32) {
-    // ---- second pass: 1024 linear bins over bin D --------------------------------------
-#pragma unroll
-    for (int j = 0; j < NK; ++j) {
-      if (b[j] == D) {
-        sub[j] = min(1023, max(0, (int)((pos[j] - (float)D) * 1024.f)));
-        atomicAdd(&sm.h10[sub[j]], 1u);
-        atomicAdd(&sm.coarse10[sub[j] >> 5], 1u);
-      }
-    }
-    __syncthreads();
-    const int cnt = (int)sm.coarse10[31 - lane];  // lane l: coarse bin 31 - l (descending)
-    int incl = warp_incl_scan(cnt);
-    int excl = incl - cnt;
-    uint32_t bal = __ballot_sync(0xffffffffu, excl < remaining && incl >= remaining);
-    int src = __ffs(bal) - 1;
-    const int cbin = 31 - src;
-    const int above_c = __shfl_sync(0xffffffffu, excl, src);
-    const int f = (int)sm.h10[cbin * 32 + 31 - lane];
-    incl = warp_incl_scan(f) + above_c;
-    excl = incl - f;
-    bal = __ballot_sync(0xffffffffu, excl < remaining && incl >= remaining);
-    src = __ffs(bal) - 1;
-    D2 = cbin * 32 + 31 - src;
-    remaining -= __shfl_sync(0xffffffffu, excl, src);
-    in_bin = __shfl_sync(0xffffffffu, f, src);
-    if (in_bin != remaining && in_bin > 32) {
-      // equal or nearly equal keys: the radix select from the start. Every warp has read h11 /
-      // coarse (before the barrier above), so they can be cleared for it; its other scratch
-      // (hist, ncand) is untouched.
-      uint4* h = reinterpret_cast<uint4*>(sm.h11);
-      h[2 * tid] = make_uint4(0u, 0u, 0u, 0u);
-      h[2 * tid + 1] = make_uint4(0u, 0u, 0u, 0u);
-      if (tid < 16) reinterpret_cast<uint4*>(sm.coarse)[tid] = make_uint4(0u, 0u, 0u, 0u);
-      __syncthreads();
-      return block_topk_1024_radix(keys, n, k, out, sm);
-    }
-  }
-  // the bin that holds the k-th key: (b == D) and, after a second pass, (sub == D2)
-  auto in_kbin = [&](int j) { return b[j] == D && (D2 < 0 || sub[j] == D2); };
-  auto above_kbin = [&](int j) { return b[j] > D || (b[j] == D && D2 >= 0 && sub[j] > D2); };
-  bool bin_all = in_bin == remaining;  // every key of that bin is taken
-  bool key_incl = false;               // else: keys > T of the bin, then keys == T below
-  uint32_t T = 0u;
-  int need_eq = 0;
-  if (!bin_all) {
-#pragma unroll
-    for (int j = 0; j < NK; ++j) {
-      if (v[j] && in_kbin(j)) {
-        const int slot = atomicAdd(&sm.ncand, 1);
-        sm.cand_u[slot] = u[j];
-        sm.cand_i[slot] = 4 * tid + j;
-      }
-    }
-    __syncthreads();
-    const bool mine = lane < in_bin;
-    const uint32_t cu = mine ? sm.cand_u[lane] : 0u;
-    const int ci = mine ? sm.cand_i[lane] : 0x7fffffff;
-    int rank = 0, gt = 0, eq = 0;
-    for (int m = 0; m < in_bin; ++m) {
-      const uint32_t ou = __shfl_sync(0xffffffffu, cu, m);
-      const int oi = __shfl_sync(0xffffffffu, ci, m);
-      gt += ou > cu ? 1 : 0;
-      eq += ou == cu ? 1 : 0;
-      rank += (ou > cu || (ou == cu && oi < ci)) ? 1 : 0;
-    }
-    const uint32_t bal = __ballot_sync(0xffffffffu, mine && rank == remaining - 1);
-    const int src = __ffs(bal) - 1;
-    T = __shfl_sync(0xffffffffu, cu, src);
-    const int gt_k = __shfl_sync(0xffffffffu, gt, src);
-    const int eq_k = __shfl_sync(0xffffffffu, eq, src);
-    if (eq_k == remaining - gt_k) {
-      key_incl = true;
-    } else {
-      need_eq = remaining - gt_k;
-    }
-  }
-  // ---- compaction in index order ((warp, lane, j) is ascending) -------------------------
-  const uint32_t lt = (1u << lane) - 1u;
-  int cg = 0, ce = 0;
-  bool g[NK], e[NK];
-#pragma unroll
-  for (int j = 0; j < NK; ++j) {
-    const bool kb = v[j] && in_kbin(j);
-    g[j] = v[j] && (above_kbin(j) || (kb && (bin_all || (key_incl ? u[j] >= T : u[j] > T))));
-    e[j] = kb && need_eq > 0 && u[j] == T;
-    cg += g[j] ? 1 : 0;
-    ce += e[j] ? 1 : 0;
-  }
-  const uint32_t g0 = __ballot_sync(0xffffffffu, cg & 1);
-  const uint32_t g1 = __ballot_sync(0xffffffffu, cg & 2);
-  const uint32_t g2 = __ballot_sync(0xffffffffu, cg & 4);
-  int gb = __popc(g0 & lt) + 2 * __popc(g1 & lt) + 4 * __popc(g2 & lt);
-  const int gw = __popc(g0) + 2 * __popc(g1) + 4 * __popc(g2);
-  int eb = 0, ew = 0;
-  if (need_eq > 0) {
-    const uint32_t e0 = __ballot_sync(0xffffffffu, ce & 1);
-    const uint32_t e1 = __ballot_sync(0xffffffffu, ce & 2);
-    const uint32_t e2 = __ballot_sync(0xffffffffu, ce & 4);
-    eb = __popc(e0 & lt) + 2 * __popc(e1 & lt) + 4 * __popc(e2 & lt);
-    ew = __popc(e0) + 2 * __popc(e1) + 4 * __popc(e2);
-  }
-  if (lane == 0) sm.cnt[0][warp] = ((uint32_t)gw << 16) | (uint32_t)ew;
-  __syncthreads();
-  const uint4 c0 = reinterpret_cast<const uint4*>(sm.cnt[0])[0];
-  const uint4 c1 = reinterpret_cast<const uint4*>(sm.cnt[0])[1];
-  const uint32_t c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-  uint32_t below = 0u, all = 0u;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    below += (w < warp) ? c[w] : 0u;
-    all += c[w];
-  }
-  gb += (int)(below >> 16);
-  eb += (int)(below & 0xffffu);
-#pragma unroll
-  for (int j = 0; j < NK; ++j) {
-    const bool take = g[j] || (e[j] && eb < need_eq);
-    const int p = gb + min(eb, need_eq);
-    if (take && p < k) out[p] = 4 * tid + j;
     gb += g[j] ? 1 : 0;
     eb += e[j] ? 1 : 0;
   }

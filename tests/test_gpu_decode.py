@@ -287,8 +287,8 @@ def test_device_status_len_over_cap():
 
 
 def test_hybrid_page_select_heavy_tail():
-    # a few pages whose keys are 300x larger: the linear first pass puts the other pages into a
-    # handful of bins, so the page select needs its second pass over the crowded bin
+    # a few pages whose keys are 300x larger (both signs): a score range dominated by outliers,
+    # with the k-th page among the crowded ordinary ones
     def tweak(k, v):
         k[:, :, 40:52] *= 300
         k[:, :, 2000:2004] *= -300
@@ -297,8 +297,9 @@ def test_hybrid_page_select_heavy_tail():
 
 def test_hybrid_page_select_crowded_equal_scores():
     # 1004 identical pages (equal approximate scores) and 20 pages with 4x larger keys: the
-    # k-th page lies among a thousand equal scores, which only the radix form resolves; the
-    # equal pages are then taken lowest index first, checked exactly on the kernel's own scores
+    # k-th page lies among a thousand equal scores, which the select resolves down to the last
+    # bit; the equal pages are then taken lowest index first, checked exactly on the kernel's
+    # own scores
     rkv = _lib()
     n, n_kv, gqa, L, B, page, C = 1, 2, 4, 4096, 256, 4, 32
     k, v = _make_cache(n, n_kv, L, [L], seed=63)
