@@ -1,6 +1,7 @@
 // C ABI of the RocketKV library: argument validation, workspace carving, kernel launches.
 // Declarations and the contract of every entry point are in include/rkv.h.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -50,6 +51,15 @@ inline rkv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RKV_OK : 
 inline bool gqa_ok(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxAvgKernel = (1 << 20) - 1;  // keeps a fixed-point window sum below 2^60
+
+// An NVTX range named after the entry point around each call that launches kernels, so that a
+// profiler's timeline (or ncu --nvtx filters) shows the library's calls; without a tool attached
+// NVTX returns at once.
+struct TraceRange {
+  explicit TraceRange(const char* name) { nvtxRangePushA(name); }
+  ~TraceRange() { nvtxRangePop(); }
+};
+#define RKV_TRACE() TraceRange rkv_trace_range_(__func__)
 
 }  // namespace
 
@@ -220,6 +230,7 @@ rkv_status rkv_snapkv_compress(const void* k, const void* v, const int32_t* seq_
                                void* k_out, void* v_out, int cap, int32_t* kept_idx,
                                int32_t* out_len, float* scores_out, void* ws, size_t ws_bytes,
                                void* stream) {
+  RKV_TRACE();
   return snapkv_impl(k, v, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window,
                      kernel_size, keep, scale, k_out, v_out, cap, kept_idx, out_len, scores_out,
                      ws, ws_bytes, stream, false, PagedMap{});
@@ -231,6 +242,7 @@ rkv_status rkv_snapkv_compress_avg_pool(const void* k, const void* v, const int3
                                         int keep, float scale, void* k_out, void* v_out, int cap,
                                         int32_t* kept_idx, int32_t* out_len, float* scores_out,
                                         void* ws, size_t ws_bytes, void* stream) {
+  RKV_TRACE();
   return snapkv_impl(k, v, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window,
                      kernel_size, keep, scale, k_out, v_out, cap, kept_idx, out_len, scores_out,
                      ws, ws_bytes, stream, false, PagedMap{}, 0, 0, nullptr, nullptr, true);
@@ -241,6 +253,7 @@ rkv_status rkv_snapkv_select(const void* k, const int32_t* seq_lens, const void*
                              int kernel_size, int keep, float scale, int32_t* kept_idx,
                              int kept_stride, int32_t* out_len, float* scores_out, void* ws,
                              size_t ws_bytes, void* stream) {
+  RKV_TRACE();
   if (kept_stride <= 0) return RKV_ERR_INVALID_ARG;
   return snapkv_impl(k, nullptr, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window,
                      kernel_size, keep, scale, nullptr, nullptr, keep, kept_idx, out_len,
@@ -256,6 +269,7 @@ rkv_status rkv_snapkv_compress_summarized(const void* k, const void* v,
                                           int32_t* out_len, float* scores_out, int page,
                                           int page_cap, void* kmin, void* kmax, void* ws,
                                           size_t ws_bytes, void* stream) {
+  RKV_TRACE();
   if (!kmin || !kmax) return RKV_ERR_INVALID_ARG;
   return snapkv_impl(k, v, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window,
                      kernel_size, keep, scale, k_out, v_out, cap, kept_idx, out_len, scores_out,
@@ -273,6 +287,7 @@ rkv_status rkv_snapkv_compress_per_head(const void* k, const void* v, const int3
                                         int keep, float scale, void* k_out, void* v_out, int cap,
                                         int32_t* kept_idx, int32_t* out_len, float* scores_out,
                                         void* ws, size_t ws_bytes, void* stream) {
+  RKV_TRACE();
   if (gqa <= 0) return RKV_ERR_INVALID_ARG;
   return snapkv_impl(k, v, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window,
                      kernel_size, keep, scale, k_out, v_out, cap, kept_idx, out_len, scores_out,
@@ -316,6 +331,7 @@ rkv_status rkv_build_page_summaries(const void* k_cache, const int32_t* len, int
                                     int head_dim, int cap, int page, int page_cap,
                                     int first_token, void* kmin, void* kmax, void* ws,
                                     size_t ws_bytes, void* stream) {
+  RKV_TRACE();
   return summaries_impl(k_cache, len, nullptr, PagedMap{}, n, n_kv, head_dim, cap, cap, page,
                         page_cap, first_token, kmin, kmax, ws, ws_bytes, stream);
 }
@@ -325,6 +341,7 @@ rkv_status rkv_build_page_summaries_mt(const void* k_full, const int32_t* kept_i
                                        int full_cap, int kcap, int page, int page_cap,
                                        int first_token, void* kmin, void* kmax, void* ws,
                                        size_t ws_bytes, void* stream) {
+  RKV_TRACE();
   if (!kept_idx) return RKV_ERR_INVALID_ARG;
   return summaries_impl(k_full, kept_len, kept_idx, PagedMap{}, n, n_kv, head_dim, full_cap, kcap,
                         page, page_cap, first_token, kmin, kmax, ws, ws_bytes, stream);
@@ -424,6 +441,7 @@ rkv_status rkv_hybrid_decode(const void* q, const void* new_k, const void* new_v
                              int budget, int page, int channels, float scale, void* out,
                              int32_t* sel_channels, int32_t* sel_pages, float* approx_scores,
                              void* ws, size_t ws_bytes, void* stream) {
+  RKV_TRACE();
   return hybrid_impl(q, new_k, new_v, k_cache, v_cache, len, nullptr, nullptr, PagedMap{}, kmin,
                      kmax, n, n_kv, gqa, head_dim, cap, cap, page_cap, budget, page, channels,
                      scale, out, sel_channels, sel_pages, approx_scores, ws, ws_bytes, stream);
@@ -436,6 +454,7 @@ rkv_status rkv_hybrid_decode_mt(const void* q, const void* new_k, const void* ne
                                 int budget, int page, int channels, float scale, void* out,
                                 int32_t* sel_channels, int32_t* sel_pages, float* approx_scores,
                                 void* ws, size_t ws_bytes, void* stream) {
+  RKV_TRACE();
   if (!kept_idx || !full_len) return RKV_ERR_INVALID_ARG;
   return hybrid_impl(q, new_k, new_v, k_full, v_full, kept_len, kept_idx, full_len, PagedMap{},
                      kmin, kmax, n, n_kv, gqa, head_dim, full_cap, kcap, page_cap, budget, page,
@@ -456,6 +475,7 @@ rkv_status rkv_snapkv_compress_paged(const void* k, const void* v, const int32_t
                                      int block, const int32_t* block_table, int max_blocks,
                                      int32_t* kept_idx, int32_t* out_len, float* scores_out,
                                      void* ws, size_t ws_bytes, void* stream) {
+  RKV_TRACE();
   if (!paged_ok(block_table, num_blocks, block, max_blocks)) return RKV_ERR_INVALID_ARG;
   const PagedMap pm{block_table, max_blocks, block, num_blocks};
   return snapkv_impl(k, v, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window,
@@ -468,6 +488,7 @@ rkv_status rkv_build_page_summaries_paged(const void* k_pool, const int32_t* blo
                                           int num_blocks, int block, int max_blocks, int page,
                                           int page_cap, int first_token, void* kmin, void* kmax,
                                           void* ws, size_t ws_bytes, void* stream) {
+  RKV_TRACE();
   if (!paged_ok(block_table, num_blocks, block, max_blocks)) return RKV_ERR_INVALID_ARG;
   const PagedMap pm{block_table, max_blocks, block, num_blocks};
   const int capacity = max_blocks * block;
@@ -483,6 +504,7 @@ rkv_status rkv_hybrid_decode_paged(const void* q, const void* new_k, const void*
                                    void* out, int32_t* sel_channels, int32_t* sel_pages,
                                    float* approx_scores, void* ws, size_t ws_bytes,
                                    void* stream) {
+  RKV_TRACE();
   if (!paged_ok(block_table, num_blocks, block, max_blocks)) return RKV_ERR_INVALID_ARG;
   const PagedMap pm{block_table, max_blocks, block, num_blocks};
   const int capacity = max_blocks * block;
@@ -500,6 +522,7 @@ size_t rkv_dense_decode_workspace_bytes(int n, int n_kv, int gqa, int max_len) {
 rkv_status rkv_dense_decode(const void* q, const void* k, const void* v, const int32_t* len,
                             int n, int n_kv, int gqa, int head_dim, int max_len, float scale,
                             void* out, void* ws, size_t ws_bytes, void* stream) {
+  RKV_TRACE();
   if (head_dim != kHeadDim) return RKV_ERR_UNSUPPORTED;
   if (!gqa_ok(gqa)) return RKV_ERR_UNSUPPORTED;
   if (!q || !k || !v || !len || !out) return RKV_ERR_INVALID_ARG;
