@@ -805,8 +805,11 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_fast_kernel(SnapArgs a)
     const int incl_w = warp_incl_scan(own);
     if (lane == 31) wsum[warp] = incl_w;
     __syncthreads();
-    int before = 0;
-    for (int w = 0; w < warp; ++w) before += wsum[w];
+    int before;
+    {  // the totals of the warps before this one, by a scan of all 32 in every warp
+      const int xw = wsum[lane];
+      before = __shfl_sync(0xffffffffu, warp_incl_scan(xw) - xw, warp);
+    }
     const int incl = before + incl_w, excl = incl - own;
     if (excl < remaining && incl >= remaining) {
       if (excl + c_hi >= remaining) {
@@ -846,15 +849,16 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_fast_kernel(SnapArgs a)
     wsum2[warp] = ie;
   }
   __syncthreads();
-  int gb = ig - cg, eb = ie - ce, gtot = 0, etot = 0;
-  for (int w = 0; w < 32; ++w) {
-    const int x1 = wsum[w], x2 = wsum2[w];
-    if (w < warp) {
-      gb += x1;
-      eb += x2;
-    }
-    gtot += x1;
-    etot += x2;
+  // each warp scans the 32 per-warp totals itself (lane l holds warp l's) instead of a serial
+  // loop over them in every thread
+  int gb, eb, gtot, etot;
+  {
+    const int x1 = wsum[lane], x2 = wsum2[lane];
+    const int s1 = warp_incl_scan(x1), s2 = warp_incl_scan(x2);
+    gb = ig - cg + __shfl_sync(0xffffffffu, s1 - x1, warp);
+    eb = ie - ce + __shfl_sync(0xffffffffu, s2 - x2, warp);
+    gtot = __shfl_sync(0xffffffffu, s1, 31);
+    etot = __shfl_sync(0xffffffffu, s2, 31);
   }
 #pragma unroll
   for (int q = 0; q < kSelPerThread; ++q) {
