@@ -145,6 +145,13 @@ def _i32(t: torch.Tensor, name: str):
         raise TypeError(f"{name} must be int32")
 
 
+def _group(hq: int, n_kv: int) -> int:
+    """Query heads per KV head; the query heads must split evenly over the KV heads."""
+    if n_kv <= 0 or hq % n_kv != 0:
+        raise ValueError(f"{hq} query heads do not split over {n_kv} KV heads")
+    return hq // n_kv
+
+
 def workspace(nbytes: int, device) -> torch.Tensor:
     """A zeroed workspace (the device status word must start at zero)."""
     return torch.zeros(max(int(nbytes), STATUS_BYTES), dtype=torch.uint8, device=device)
@@ -192,7 +199,7 @@ def rkv_snapkv_compress(k, v, seq_lens, q_win, kernel_size: int, keep: int, scal
     _i32(kept_idx, "kept_idx"), _i32(out_len, "out_len")
     n, n_kv, max_len, d = k.shape
     hq, window = q_win.shape[1], q_win.shape[2]
-    gqa = hq // n_kv
+    gqa = _group(hq, n_kv)
     cap = k_out.shape[2]
     if ws is None:
         ws = workspace(rkv_snapkv_workspace_bytes(n, n_kv, gqa, max_len, window), k.device)
@@ -212,7 +219,7 @@ def rkv_snapkv_compress_avg_pool(k, v, seq_lens, q_win, kernel_size: int, keep: 
     _i32(kept_idx, "kept_idx"), _i32(out_len, "out_len")
     n, n_kv, max_len, d = k.shape
     hq, window = q_win.shape[1], q_win.shape[2]
-    gqa = hq // n_kv
+    gqa = _group(hq, n_kv)
     cap = k_out.shape[2]
     if ws is None:
         ws = workspace(rkv_snapkv_workspace_bytes(n, n_kv, gqa, max_len, window), k.device)
@@ -232,7 +239,7 @@ def rkv_snapkv_select(k, seq_lens, q_win, kernel_size: int, keep: int, scale: fl
     _i32(kept_idx, "kept_idx"), _i32(out_len, "out_len")
     n, n_kv, max_len, d = k.shape
     hq, window = q_win.shape[1], q_win.shape[2]
-    gqa = hq // n_kv
+    gqa = _group(hq, n_kv)
     if ws is None:
         ws = workspace(rkv_snapkv_workspace_bytes(n, n_kv, gqa, max_len, window), k.device)
     code = load().rkv_snapkv_select(
@@ -257,7 +264,7 @@ def rkv_snapkv_compress_per_head(k, v, seq_lens, q_win, kernel_size: int, keep: 
     _i32(kept_idx, "kept_idx"), _i32(out_len, "out_len")
     n, n_kv, max_len, d = k.shape
     hq, window = q_win.shape[1], q_win.shape[2]
-    gqa = hq // n_kv
+    gqa = _group(hq, n_kv)
     cap = k_out.shape[2]
     if ws is None:
         ws = workspace(rkv_snapkv_per_head_workspace_bytes(n, n_kv, gqa, max_len, window),
@@ -278,7 +285,7 @@ def rkv_snapkv_compress_summarized(k, v, seq_lens, q_win, kernel_size: int, keep
     _i32(kept_idx, "kept_idx"), _i32(out_len, "out_len"), _bf16(kmin, "kmin")
     n, n_kv, max_len, d = k.shape
     hq, window = q_win.shape[1], q_win.shape[2]
-    gqa = hq // n_kv
+    gqa = _group(hq, n_kv)
     cap = k_out.shape[2]
     page_cap = kmin.shape[-1]
     if ws is None:
@@ -318,7 +325,7 @@ def rkv_hybrid_decode(q, k_cache, v_cache, length, kmin, kmax, budget: int, page
     """One hybrid sparse decode step (optionally appending new_k / new_v first)."""
     _bf16(q, "q"), _bf16(k_cache, "k_cache"), _i32(length, "len")
     n, n_kv, cap, d = k_cache.shape
-    gqa = q.shape[1] // n_kv
+    gqa = _group(q.shape[1], n_kv)
     page_cap = kmin.shape[-1]
     if ws is None:
         ws = workspace(rkv_hybrid_decode_workspace_bytes(n, n_kv, gqa, page_cap, budget, page),
@@ -357,7 +364,7 @@ def rkv_hybrid_decode_mt(q, k_full, v_full, full_len, kept_idx, kept_len, kmin, 
     _bf16(q, "q"), _bf16(k_full, "k_full"), _i32(full_len, "full_len")
     _i32(kept_idx, "kept_idx"), _i32(kept_len, "kept_len")
     n, n_kv, full_cap, d = k_full.shape
-    gqa = q.shape[1] // n_kv
+    gqa = _group(q.shape[1], n_kv)
     kcap = kept_idx.shape[-1]
     page_cap = kmin.shape[-1]
     if ws is None:
@@ -381,7 +388,7 @@ def rkv_snapkv_compress_paged(k, v, seq_lens, q_win, kernel_size: int, keep: int
     _i32(kept_idx, "kept_idx"), _i32(out_len, "out_len"), _i32(seq_lens, "seq_lens")
     n, n_kv, max_len, d = k.shape
     hq, window = q_win.shape[1], q_win.shape[2]
-    gqa = hq // n_kv
+    gqa = _group(hq, n_kv)
     num_blocks, _, block, _ = k_pool.shape
     max_blocks = block_table.shape[-1]
     if ws is None:
@@ -419,7 +426,7 @@ def rkv_hybrid_decode_paged(q, k_pool, v_pool, block_table, length, kmin, kmax, 
     _bf16(q, "q"), _bf16(k_pool, "k_pool"), _i32(block_table, "block_table"), _i32(length, "len")
     num_blocks, n_kv, block, d = k_pool.shape
     n, max_blocks = block_table.shape
-    gqa = q.shape[1] // n_kv
+    gqa = _group(q.shape[1], n_kv)
     page_cap = kmin.shape[-1]
     if ws is None:
         ws = workspace(rkv_hybrid_decode_workspace_bytes(n, n_kv, gqa, page_cap, budget, page),
@@ -441,7 +448,7 @@ def rkv_dense_decode(q, k, v, length, scale: float, out, ws=None, stream=None):
     """Full-KV decode attention over len[u] tokens."""
     _bf16(q, "q"), _bf16(k, "k"), _i32(length, "len")
     n, n_kv, max_len, d = k.shape
-    gqa = q.shape[1] // n_kv
+    gqa = _group(q.shape[1], n_kv)
     if ws is None:
         ws = workspace(rkv_dense_decode_workspace_bytes(n, n_kv, gqa, max_len), q.device)
     code = load().rkv_dense_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(length), n, n_kv, gqa, d,
@@ -456,7 +463,7 @@ def rkv_dense_decode_noalloc(q, k, v, length, scale: float, out, stream=None):
     For callers that cannot allocate; calls sharing the scratch must not overlap on the GPU."""
     _bf16(q, "q"), _bf16(k, "k"), _i32(length, "len")
     n, n_kv, max_len, d = k.shape
-    gqa = q.shape[1] // n_kv
+    gqa = _group(q.shape[1], n_kv)
     code = load().rkv_dense_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(length), n, n_kv, gqa,
                                            d, max_len, float(scale), _ptr(out), _stream(stream))
     _check("rkv_dense_decode_noalloc", code)

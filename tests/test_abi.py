@@ -197,3 +197,10 @@ def test_workspace_sizes_monotone(lib):
     assert lib.rkv_snapkv_workspace_bytes(1, 8, 4, 131072, 64) > \
         lib.rkv_snapkv_workspace_bytes(1, 8, 4, 4096, 32)
     assert lib.rkv_hybrid_decode_workspace_bytes(32, 8, 4, 1024, 256, 4) >= 256
+
+
+def test_binding_rejects_uneven_groups():
+    from sparse_kv_cache_snapkv_gb300 import rkv
+    with pytest.raises(ValueError):
+        rkv._group(30, 8)
+    assert rkv._group(32, 8) == 4
