@@ -171,7 +171,7 @@ rkv_status rkv_snapkv_compress_summarized(const void* k, const void* v,
                                           int page_cap, void* kmin, void* kmax, void* ws,
                                           size_t ws_bytes, void* stream);
 
-/* The ablation without the GQA enhancement ([SNAP++], [KEYPTS] "original SnapKV"): every query
+/* The ablation without the GQA enhancement ([SNAP++], [KEYPTS]: plain SnapKV): every query
  * head is scored and filtered on its own -- its W window rows only, no sum over the group -- and
  * keeps its own copy of the selected rows of its K/V head h / gqa. Same arguments as
  * rkv_snapkv_compress, with the per-unit outputs per query head:

@@ -27,7 +27,8 @@ Readings taken where the pages leave a step open (each restated at its function)
       visible to that window query: the prefix plus the causal part of the window), summed over the
       window rows and over the query heads of the KV head's group. Only prefix columns are ranked;
       the window tokens are always kept.
-  R3  adaptive pooling kernel: L <= 8192 -> 7, L <= 32768 -> 15, else 31 ("longer -> larger").
+  R3  adaptive pooling kernel: L <= 8192 -> 7, L <= 32768 -> 15, else 31 (the pages only say
+      that longer contexts get larger kernels).
   R4  max pooling, stride 1, same length, window clipped at both ends.
   R5  top-k order: larger key first, equal keys -> lower index. Kept indices stored ascending, then
       the window positions.
@@ -48,8 +49,8 @@ Readings taken where the pages leave a step open (each restated at its function)
       the in-range positions of the clipped window.
   R20 a paged (block-table) compact cache is a storage layout only: every step computes on the
       rows the table names, in token order, exactly as on the contiguous cache.
-  R19 SnapKV without the GQA enhancement ([P1] "Key points": the ablation against "original
-      SnapKV"): each query head scores with its own W window rows only, and keeps its own top-k.
+  R19 SnapKV without the GQA enhancement ([P1] "Key points": the ablation against plain SnapKV):
+      each query head scores with its own W window rows only, and keeps its own top-k.
   R17 RocketKV-MT ([P3] "SCBench Results"): nothing is evicted; the decode runs the stage-2 steps
       on the sequence of kept tokens (stage 1's kept positions in its order, then the tokens
       generated since), whose rows stay in the full cache. The pages do not say where generated

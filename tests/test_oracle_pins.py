@@ -363,8 +363,8 @@ def test_mt_identity_kept_list_is_plain_decode():
 
 
 def test_mt_evicted_rows_never_matter():
-    # "all KV tokens are kept in memory but [decode] only selects among the important tokens":
-    # rows outside the kept list may hold anything without changing the step
+    # "SCBench Results": RocketKV-MT keeps every token in memory, yet the decode picks only from
+    # the filtered ones, so rows outside the kept list may hold anything without changing a step
     rng = np.random.default_rng(18)
     L, d, B, p, n_kept = 2000, 32, 128, 4, 500
     kf = _bf16_values((L, d), rng)
