@@ -621,6 +621,8 @@ cudaError_t launch_hybrid(const HybridArgsAll& a, cudaStream_t s) {
 // ==========================================================================================
 __global__ void append_kernel(AppendArgs a) {
   const int u = blockIdx.x, c = threadIdx.x;  // 128 threads: one channel each
+  pdl_wait();     // the previous decode step may still be reading the cache and the length
+  pdl_trigger();  // the decode after this append may be scheduled now; it waits for our writes
   const int len = a.len[u];
   const int row = a.kept ? a.full_len[u] : len;  // cache row receiving the token
   const int pg = len / a.page;
@@ -657,8 +659,7 @@ __global__ void append_kernel(AppendArgs a) {
 }
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
-  append_kernel<<<a.n, kHeadDim, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(append_kernel, dim3(a.n), dim3(kHeadDim), 0, s, a);
 }
 
 // ==========================================================================================
