@@ -1,7 +1,7 @@
 // C ABI of the RocketKV library: argument validation, workspace carving, kernel launches.
 // Declarations and the contract of every entry point are in include/rkv.h.
 #include <cuda_runtime.h>
-#include <nvtx3/nvToolsExt.h>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -39,6 +39,27 @@ cudaError_t ensure_dyn_smem(const void* func, size_t bytes) {
   return cudaSuccess;
 }
 
+int device_sm_count() {
+  static std::mutex mu;
+  static int cached[128] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) {
+    cudaGetLastError();
+    return kFallbackSMs;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0) {
+      cudaGetLastError();
+      return kFallbackSMs;
+    }
+    cached[dev] = sms;
+  }
+  return cached[dev];
+}
+
 }  // namespace rkv
 
 namespace {
@@ -51,15 +72,6 @@ inline rkv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RKV_OK : 
 inline bool gqa_ok(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxAvgKernel = (1 << 20) - 1;  // keeps a fixed-point window sum below 2^60
-
-// An NVTX range named after the entry point around each call that launches kernels, so that a
-// profiler's timeline (or ncu --nvtx filters) shows the library's calls; without a tool attached
-// NVTX returns at once.
-struct TraceRange {
-  explicit TraceRange(const char* name) { nvtxRangePushA(name); }
-  ~TraceRange() { nvtxRangePop(); }
-};
-#define RKV_TRACE() TraceRange rkv_trace_range_(__func__)
 
 }  // namespace
 
@@ -516,6 +528,7 @@ rkv_status rkv_hybrid_decode_paged(const void* q, const void* new_k, const void*
 // ------------------------------------------------------------------------------- dense
 size_t rkv_dense_decode_workspace_bytes(int n, int n_kv, int gqa, int max_len) {
   if (n <= 0 || n_kv <= 0 || gqa <= 0 || max_len <= 0) return 0;
+  if ((long long)n * n_kv * gqa > INT_MAX) return 0;
   return kStatusBytes + dense_partials_bytes(n, n_kv, gqa, max_len);
 }
 
@@ -523,15 +536,39 @@ rkv_status rkv_dense_decode(const void* q, const void* k, const void* v, const i
                             int n, int n_kv, int gqa, int head_dim, int max_len, float scale,
                             void* out, void* ws, size_t ws_bytes, void* stream) {
   RKV_TRACE();
+  int bad = dense_check_sizes(n, n_kv, gqa, head_dim, max_len, scale);
+  if (!bad) bad = dense_check_pointers(q, k, v, len, out);
+  if (bad) return static_cast<rkv_status>(bad);
+  const size_t need = rkv_dense_decode_workspace_bytes(n, n_kv, gqa, max_len);
+  if (!ws || !aligned16(ws) || ws_bytes < need) return RKV_ERR_WORKSPACE;
+  const DenseArgs a = dense_args(q, k, v, len, n, n_kv, gqa, max_len, scale, out, ws);
+  return from_cuda(launch_dense(a, as_stream(stream)));
+}
+
+}  // extern "C"
+
+namespace rkv {
+
+int dense_check_sizes(int n, int n_kv, int gqa, int head_dim, int max_len, float scale) {
   if (head_dim != kHeadDim) return RKV_ERR_UNSUPPORTED;
   if (!gqa_ok(gqa)) return RKV_ERR_UNSUPPORTED;
+  if (n <= 0 || n_kv <= 0 || max_len <= 0 || !(scale > 0.f) || !std::isfinite(scale))
+    return RKV_ERR_INVALID_ARG;
+  // one CTA per (unit, KV head) and split, one combine CTA per query head: grid limits
+  if ((long long)n * n_kv * gqa > INT_MAX) return RKV_ERR_INVALID_ARG;
+  return RKV_OK;
+}
+
+int dense_check_pointers(const void* q, const void* k, const void* v, const int32_t* len,
+                         const void* out) {
   if (!q || !k || !v || !len || !out) return RKV_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return RKV_ERR_INVALID_ARG;
-  if (n <= 0 || n_kv <= 0 || max_len <= 0 || !(scale > 0.f) || !std::isfinite(scale))
-    return RKV_ERR_INVALID_ARG;
-  const size_t need = rkv_dense_decode_workspace_bytes(n, n_kv, gqa, max_len);
-  if (!ws || !aligned16(ws) || ws_bytes < need) return RKV_ERR_WORKSPACE;
+  return RKV_OK;
+}
+
+DenseArgs dense_args(const void* q, const void* k, const void* v, const int32_t* len, int n,
+                     int n_kv, int gqa, int max_len, float scale, void* out, void* scratch) {
   DenseArgs a{};
   a.q = static_cast<const bf16*>(q);
   a.k = static_cast<const bf16*>(k);
@@ -544,15 +581,15 @@ rkv_status rkv_dense_decode(const void* q, const void* k, const void* v, const i
   dense_plan(n, n_kv, max_len, &a.nsplit, &a.tokens_per_split);
   a.scale_log2 = scale * kLog2e;
   const size_t rows = (size_t)n * n_kv * gqa * a.nsplit;
-  unsigned char* p = static_cast<unsigned char*>(ws) + kStatusBytes;
+  unsigned char* p = static_cast<unsigned char*>(scratch) + kStatusBytes;
   a.part_m = reinterpret_cast<float*>(p);
   p += align_up(rows * 4, 256);
   a.part_l = reinterpret_cast<float*>(p);
   p += align_up(rows * 4, 256);
   a.part_o = reinterpret_cast<float*>(p);
   a.out = static_cast<bf16*>(out);
-  a.status = status_ptr(ws);
-  return from_cuda(launch_dense(a, as_stream(stream)));
+  a.status = static_cast<uint32_t*>(scratch);
+  return a;
 }
 
-}  // extern "C"
+}  // namespace rkv

@@ -816,9 +816,9 @@ cudaError_t launch_summaries(const SummaryArgs& a, cudaStream_t s) {
 // per-split partials are merged by a second kernel.
 // ==========================================================================================
 void dense_plan(int n, int n_kv, int max_len, int* nsplit, int* tokens_per_split) {
-  const int units = n * n_kv;
-  const int target_ctas = 152 * 4;  // two waves of two resident CTAs per SM
-  int ns = (target_ctas + units - 1) / units;
+  const long long units = (long long)n * n_kv;
+  const long long target_ctas = 4LL * device_sm_count();  // two waves of two CTAs per SM
+  int ns = (int)((target_ctas + units - 1) / units);
   const int max_ns = (max_len + 255) / 256;  // at least 256 tokens per split
   ns = ns < 1 ? 1 : (ns > max_ns ? max_ns : ns);
   int tps = (max_len + ns - 1) / ns;

@@ -9,7 +9,6 @@
 // Cost: every GPU that loads the library keeps kNoAllocScratchBytes of device memory for this
 // array until the process exits.
 #include <cuda_runtime.h>
-#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -51,42 +50,20 @@ extern "C" rkv_status rkv_dense_decode_noalloc(const void* q, const void* k, con
                                                const int32_t* len, int n, int n_kv, int gqa,
                                                int head_dim, int max_len, float scale,
                                                void* out, void* stream) {
-  if (head_dim != kHeadDim) return RKV_ERR_UNSUPPORTED;
-  if (!(gqa == 1 || gqa == 2 || gqa == 4 || gqa == 8)) return RKV_ERR_UNSUPPORTED;
-  if (!q || !k || !v || !len || !out) return RKV_ERR_INVALID_ARG;
-  const uintptr_t mis = (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) & 15u;
-  if (mis) return RKV_ERR_INVALID_ARG;
-  if (n <= 0 || n_kv <= 0 || max_len <= 0 || !(scale > 0.f) || !std::isfinite(scale))
-    return RKV_ERR_INVALID_ARG;
+  RKV_TRACE();
+  // sizes first: a problem beyond the fixed array is rejected before any pointer is looked at
+  int bad = dense_check_sizes(n, n_kv, gqa, head_dim, max_len, scale);
+  if (bad) return static_cast<rkv_status>(bad);
   const size_t need = kStatusBytes + dense_partials_bytes(n, n_kv, gqa, max_len);
   if (need > kNoAllocScratchBytes) return RKV_ERR_TOO_LARGE;
+  bad = dense_check_pointers(q, k, v, len, out);
+  if (bad) return static_cast<rkv_status>(bad);
 
   void* base = nullptr;
   if (noalloc_scratch(&base) != cudaSuccess) return RKV_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the status word must start at zero; the partials are fully rewritten by every call
   if (cudaMemsetAsync(base, 0, kStatusBytes, s) != cudaSuccess) return RKV_ERR_CUDA;
-
-  DenseArgs a{};
-  a.q = static_cast<const bf16*>(q);
-  a.k = static_cast<const bf16*>(k);
-  a.v = static_cast<const bf16*>(v);
-  a.len = len;
-  a.n = n;
-  a.n_kv = n_kv;
-  a.gqa = gqa;
-  a.max_len = max_len;
-  dense_plan(n, n_kv, max_len, &a.nsplit, &a.tokens_per_split);
-  a.scale_log2 = scale * 1.4426950408889634f;
-  const size_t rows = (size_t)n * n_kv * gqa * a.nsplit;
-  unsigned char* p = static_cast<unsigned char*>(base) + kStatusBytes;
-  a.part_m = reinterpret_cast<float*>(p);
-  p += align_up(rows * 4, 256);
-  a.part_l = reinterpret_cast<float*>(p);
-  p += align_up(rows * 4, 256);
-  a.part_o = reinterpret_cast<float*>(p);
-  a.out = static_cast<bf16*>(out);
-  a.status = static_cast<uint32_t*>(base);
+  const DenseArgs a = dense_args(q, k, v, len, n, n_kv, gqa, max_len, scale, out, base);
   return launch_dense(a, s) == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
 }

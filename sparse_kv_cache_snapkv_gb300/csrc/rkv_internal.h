@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <nvtx3/nvToolsExt.h>
 
 namespace rkv {
 
@@ -112,9 +113,35 @@ struct DenseArgs {
 // no-ops, so launches stay legal inside stream capture.
 cudaError_t ensure_dyn_smem(const void* func, size_t bytes);
 
+// Streaming multiprocessors of the current device, looked up once per device: persistent grids
+// and split plans are sized in multiples of it. When no device answers (a host-only workspace
+// query), the GB300's 152.
+constexpr int kFallbackSMs = 152;
+int device_sm_count();
+
+// An NVTX range named after the entry point around each call that launches kernels, so that a
+// profiler's timeline (or ncu --nvtx filters) shows the library's calls; without a tool attached
+// NVTX returns at once.
+struct TraceRange {
+  explicit TraceRange(const char* name) { nvtxRangePushA(name); }
+  ~TraceRange() { nvtxRangePop(); }
+};
+#define RKV_TRACE() ::rkv::TraceRange rkv_trace_range_(__func__)
+
 // split plan for dense decode, shared by the workspace query and the launch
 void dense_plan(int n, int n_kv, int max_len, int* nsplit, int* tokens_per_split);
 size_t dense_partials_bytes(int n, int n_kv, int gqa, int max_len);
+
+// Argument checks of the dense decode, shared by the workspace and the allocation-free entry
+// points: 0 when the call may proceed, else an rkv_status code. Sizes come first, so that a
+// problem too large for a fixed scratch is reported before any pointer is looked at.
+int dense_check_sizes(int n, int n_kv, int gqa, int head_dim, int max_len, float scale);
+int dense_check_pointers(const void* q, const void* k, const void* v, const int32_t* len,
+                         const void* out);
+// The launch arguments over a scratch area whose first kStatusBytes hold the status word and the
+// rest the split partials (dense_partials_bytes of them).
+DenseArgs dense_args(const void* q, const void* k, const void* v, const int32_t* len, int n,
+                     int n_kv, int gqa, int max_len, float scale, void* out, void* scratch);
 
 size_t hybrid_smem_bytes(int gqa, int page_cap, int budget, int page);
 cudaError_t launch_hybrid(const HybridArgsAll& a, cudaStream_t s);

@@ -17,8 +17,9 @@
 //           reduction. The partial (m, l) of all splits are merged into lse_r first.
 // Both passes stream 128-token K tiles by TMA (SWIZZLE_128B, 2 x 64-column boxes) through a
 // 4-stage mbarrier ring; one thread issues MMAs, eight warps run the epilogue; TMEM holds two
-// accumulator buffers so the epilogue of tile i overlaps the MMA of tile i+1. Units are
-// processed in waves small enough that pass 2 re-reads K from L2.
+// accumulator buffers so the epilogue of tile i overlaps the MMA of tile i+1. Each pass is one
+// persistent launch over every (unit, split) work item; pass 2 walks the units in reverse, so
+// its first items find the K tiles pass 1 read last still in L2.
 //   select  max-pool (odd kernel, clipped ends; or the average over the clipped window) + block
 //           radix top-k, ascending kept positions
 //   gather  kept K / V rows -> compact cache (16-byte vector copies)
@@ -36,7 +37,6 @@ constexpr int kKStages = 4;
 constexpr int kScoreThreads = 320;  // warp 0: TMA, warp 1: MMA, warps 2..9: epilogue
 constexpr int kEpiThreads = 256;
 constexpr int kTileBytes = kTileTok * kHeadDim * 2;  // 32 KB per K tile
-constexpr int kSMs = 152;
 
 // ------------------------------------------------------------------------------------------
 // tcgen05 / TMA wrappers
@@ -1026,7 +1026,7 @@ void snapkv_plan(int n, int n_kv, int gqa, int max_len, int window, int* nsplit,
   (void)window;
   const int units = n * n_kv;
   const int tiles = (max_len + kTileTok - 1) / kTileTok;
-  int ns = (16 * kSMs + units - 1) / units;
+  int ns = (16 * device_sm_count() + units - 1) / units;
   const int max_ns = tiles / 4 > 1 ? tiles / 4 : 1;
   ns = ns < 1 ? 1 : (ns > max_ns ? max_ns : ns);
   const int tps = (tiles + ns - 1) / ns;
@@ -1100,7 +1100,8 @@ static cudaError_t launch_pass(const CUtensorMap& km, const CUtensorMap& qm,
   cudaError_t e = ensure_dyn_smem((const void*)score_kernel<PASS, RB>, smem);
   if (e != cudaSuccess) return e;
   const int items = sp.units * sp.nsplit;
-  const int grid = items < kSMs ? items : kSMs;
+  const int sms = device_sm_count();
+  const int grid = items < sms ? items : sms;
   e = launch_pdl_kernel(score_kernel<PASS, RB>, dim3(grid), dim3(kScoreThreads), smem, s, km, qm,
                         sp);
   if (e != cudaSuccess) return e;

@@ -47,6 +47,17 @@ def check_output(gpu_out, ref_out, what="output"):
                            f"{err.max():.3e} at ref {ref_out.flat[np.argmax(err - tol)]:.4f}")
 
 
+def approx_magnitude(q_g, channels, kmin, kmax):
+    """Per page: sum over the kept channels i of |q_g[i] * K_sel[i][page]|, where K_sel is the
+    Kmax row when q_g[i] >= 0 and the Kmin row otherwise (the summary the score itself reads)."""
+    q_g = np.asarray(q_g, dtype=np.float64)
+    mag = np.zeros(kmin.shape[1], dtype=np.float64)
+    for i in np.asarray(channels, dtype=np.int64):
+        row = kmax[i] if q_g[i] >= 0 else kmin[i]
+        mag += np.abs(q_g[i] * row)
+    return mag
+
+
 def check_approx(gpu_scores, ref_scores, magnitude, what="approx scores"):
     err = np.abs(np.asarray(gpu_scores, dtype=np.float64) - ref_scores)
     tol = APPROX_REL * np.maximum(np.abs(ref_scores), magnitude)

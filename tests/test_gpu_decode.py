@@ -126,8 +126,7 @@ def _hybrid_case(n, n_kv, gqa, lens, cap, budget, page, channels, seed, steps=2,
                 # approximate scores: recompute on the GPU's channels (equal unless tie band)
                 ref_a = O.approx_scores(q_g, gch, rmin, rmax)
                 P = rmin.shape[1]
-                magn = sum(np.abs(q_g[i]) * np.maximum(np.abs(rmin[i]), np.abs(rmax[i]))
-                           for i in gch)
+                magn = parity.approx_magnitude(q_g, gch, rmin, rmax)
                 parity.check_approx(approx[u, g, :P].cpu().numpy(), ref_a, magn,
                                     f"{tag} approx")
                 nsel = min(S, P)
