@@ -52,7 +52,21 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=2000)
     ap.add_argument("--layers", type=int, default=0,
                     help="run the workload with this many layers (smaller profiling cases)")
+    ap.add_argument("--ctx", type=int, default=0,
+                    help="prompt length of every sequence (e.g. 131072: the 128K end of the "
+                         "metric at the default workload's budget)")
     return ap.parse_args()
+
+
+def select_workload(args):
+    from dataclasses import replace
+    from sparse_kv_cache_snapkv_gb300 import synthetic as S
+    wl = S.WORKLOADS[args.workload]
+    if args.layers:
+        wl = wl.with_layers(args.layers)
+    if args.ctx:
+        wl = replace(wl, name=f"{wl.name}@ctx{args.ctx}", lens=(args.ctx,) * wl.n_seq)
+    return wl
 
 
 def peaks():
@@ -131,15 +145,14 @@ def _oracle_worker_init():
 _UNIT_CACHE = {}
 
 
-def _unit_data(wl_name, unit, seed):
+def _unit_data(wl, unit, seed):
     """One (layer, KV head) unit of the workload, drawn on the CPU in the worker (float64)."""
-    key = (wl_name, unit, seed)
+    key = (wl.name, unit, seed)
     if key not in _UNIT_CACHE:
         from dataclasses import replace
         from sparse_kv_cache_snapkv_gb300 import synthetic as S
-        wl = replace(S.WORKLOADS[wl_name], n_seq=1, n_layers=1, n_kv=1,
-                     lens=(S.WORKLOADS[wl_name].lens[0],))
-        x = S.prefill_inputs(wl, seed=seed + 7919 * unit, device="cpu")
+        one = replace(wl, n_seq=1, n_layers=1, n_kv=1, lens=(wl.lens[0],))
+        x = S.prefill_inputs(one, seed=seed + 7919 * unit, device="cpu")
         if len(_UNIT_CACHE) >= 2:
             _UNIT_CACHE.clear()
         _UNIT_CACHE[key] = (x["k"][0, 0].double().numpy(), x["v"][0, 0].double().numpy(),
@@ -152,8 +165,8 @@ def _oracle_unit(args):
     Returns (compress seconds, seconds per decode step); input drawing is not timed."""
     import numpy as np
     from oracle import rocketkv as O
-    wl_name, unit, seed, keep, kernel, budget, page, channels, steps = args
-    k, v, q_win, L = _unit_data(wl_name, unit, seed)
+    wl, unit, seed, keep, kernel, budget, page, channels, steps = args
+    k, v, q_win, L = _unit_data(wl, unit, seed)
     scale = 1.0 / math.sqrt(128)
     t0 = time.perf_counter()
     kept, kc, vc, _, _ = O.snapkv_compress(k[:L], v[:L], q_win, keep, kernel, scale)
@@ -176,7 +189,7 @@ def oracle_sample(wl, keep, kernel, units, cores, seed, pool, first_unit=0):
     leg and the reference arm time the oracle through this one rule."""
     kernel = kernel or (7 if wl.max_len <= 8192 else 15 if wl.max_len <= 32768 else 31)
     n_units = min(units, cores)
-    args = [(wl.name, (first_unit + i) % units, seed, keep, kernel, wl.budget, wl.page,
+    args = [(wl, (first_unit + i) % units, seed, keep, kernel, wl.budget, wl.page,
              wl.channels, wl.decode_steps) for i in range(n_units)]
     res = pool.map(_oracle_unit, args, chunksize=1)
     measured = max(r[0] + wl.decode_steps * r[1] for r in res)
@@ -248,9 +261,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     rkv.load()
     dev = torch.device("cuda", local)
-    wl = S.WORKLOADS[args.workload]
-    if args.layers:
-        wl = wl.with_layers(args.layers)
+    wl = select_workload(args)
     hbm_peak, bf16_peak, bf16_sus, peak_src = peaks()
 
     # cpu-baseline pool first (spawn, before heavy GPU work)
@@ -348,7 +359,7 @@ def run_ours(args):
                 "launch_us": round(comp_ms * 1e3, 1)}
     # the committed capture is of the default workload at 32 layers: other shapes get null
     traffic = None
-    if args.workload == "llama8b_32k" and wl.n_layers == 32:
+    if args.workload == "llama8b_32k" and wl.n_layers == 32 and not args.ctx:
         traffic = _profiled_traffic(roof["kernel"])
     if traffic is not None:
         roof["traffic"] = traffic
@@ -505,6 +516,119 @@ def _e2e(hp, host_in, wl, stream, world, steps):
             "ms_per_step": round(ms / steps, 3)}
 
 
+# --------------------------------------------------------------------------------- prefill sweep
+SWEEP_KERNELS = (1, 3, 7, 15, 31)
+SWEEP_BUDGETS = (256, 1024, 4096)
+
+
+def _time_ms(fn, stream, reps, warmup=3):
+    """Mean milliseconds of fn() over `reps` back-to-back calls (CUDA events on `stream`), after
+    `warmup` untimed calls."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def run_prefill_sweep(args):
+    """SnapKV++ prefill sweep on one 128K prompt (32 query / 8 KV heads, window 64, so the score
+    GEMM has G*W = 256 rows): the two tensor-core score passes, then the pooling + top-k select
+    for every pooling kernel in {1, 3, 7, 15, 31} and budget in {256, 1024, 4096} (keep = 16 x
+    budget), and the gather of each budget's kept rows. Phases are timed by difference of
+    C-ABI calls that stop after them: rkv_snapkv_scores (score passes), rkv_snapkv_select
+    (+ pooling and top-k), rkv_snapkv_compress (+ gather)."""
+    import torch
+    from sparse_kv_cache_snapkv_gb300 import rkv
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    rkv.load()
+    dev = torch.device("cuda", local)
+    wl = select_workload(args)
+    hbm_peak, bf16_peak, _, peak_src = peaks()
+    from sparse_kv_cache_snapkv_gb300 import synthetic as S
+    x = S.prefill_inputs(wl, seed=args.seed + rank, device=dev)
+    n, n_kv, L = wl.n, wl.n_kv, wl.max_len
+    W, G = wl.window, wl.gqa
+    scale = 1.0 / math.sqrt(128)
+    ws = rkv.workspace(rkv.rkv_snapkv_workspace_bytes(n, n_kv, G, L, W), dev)
+    scores = torch.empty(n, n_kv, L - W, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream()
+    reps = max(3, args.steps)
+    warm = max(3, args.warmup)
+    units = n * n_kv
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    t_scores = _time_ms(lambda: rkv.rkv_snapkv_scores(x["k"], x["seq_lens"], x["q_win"], scale,
+                                                      scores, ws=ws, stream=stream),
+                        stream, reps, warm)
+    flops = 2 * 2 * units * G * W * L * 128
+    score_tflops = flops / (t_scores * 1e-3) / 1e12
+    cells = []
+    for budget in SWEEP_BUDGETS:
+        keep = rkv.rkv_plan(L, budget)[0]
+        kept = torch.empty(n, n_kv, keep, dtype=torch.int32, device=dev)
+        out_len = torch.empty(n, dtype=torch.int32, device=dev)
+        k_out = torch.empty(n, n_kv, keep, 128, dtype=torch.bfloat16, device=dev)
+        v_out = torch.empty_like(k_out)
+        for kernel in SWEEP_KERNELS:
+            t_sel = _time_ms(lambda: rkv.rkv_snapkv_select(
+                x["k"], x["seq_lens"], x["q_win"], kernel, keep, scale, kept, out_len, ws=ws,
+                stream=stream), stream, reps, warm)
+            t_all = _time_ms(lambda: rkv.rkv_snapkv_compress(
+                x["k"], x["v"], x["seq_lens"], x["q_win"], kernel, keep, scale, k_out, v_out,
+                kept, out_len, ws=ws, stream=stream), stream, reps, warm)
+            rkv.rkv_check_status(ws)
+            select_ms = max(t_sel - t_scores, 1e-6)
+            gather_ms = max(t_all - t_sel, 1e-6)
+            sel_bytes = units * ((L - W) * 4 + keep * 4)       # scores read, kept list written
+            gat_bytes = units * keep * 128 * 2 * 4              # K, V rows read and written
+            cells.append({
+                "kernel": kernel, "budget": budget, "keep": keep,
+                "compress_ms": round(t_all, 4), "select_ms": round(select_ms, 4),
+                "select_gbs": round(sel_bytes / (select_ms * 1e-3) / 1e9, 1),
+                "gather_ms": round(gather_ms, 4),
+                "gather_gbs": round(gat_bytes / (gather_ms * 1e-3) / 1e9, 1),
+                "gather_frac_of_peak_hbm": round(gat_bytes / (gather_ms * 1e-3) / 1e9 / hbm_peak, 4)})
+        del k_out, v_out
+    clocks = sampler.stop()
+    if rank == 0:
+        line = {"metric": "SnapKV++ prefill sweep: score-GEMM TFLOP/s (tensor pipe) and "
+                          "select / gather GB/s, 128K prompt, window 64",
+                "value": round(score_tflops, 2), "unit": "TFLOP/s", "n_gpus": world,
+                "steps": reps, "warmup": warm, "ms_per_step": round(t_scores, 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic (seeded; K/V with lognormal channel scales "
+                "and planted needles)",
+                "config": {"workload": wl.name, "layers": wl.n_layers, "batch": wl.n_seq,
+                           "q_heads": wl.n_q, "kv_heads": n_kv, "head_dim": 128, "ctx": L,
+                           "window": W, "score_rows": G * W, "kernels": list(SWEEP_KERNELS),
+                           "budgets": list(SWEEP_BUDGETS),
+                           "l2": "prompt K %.2f GB per score pass (larger than L2)"
+                                 % (units * L * 256 / 1e9),
+                           "parallelism": "replicas"},
+                "roofline": {"kernel": "score_kernel (two passes)", "bound": "tensor",
+                             "achieved": round(score_tflops, 1), "peak": bf16_peak,
+                             "unit": "TFLOP/s", "frac": round(score_tflops / bf16_peak, 4),
+                             "traffic": None, "peak_source": peak_src + " (burst)",
+                             "flops_per_launch": flops // 2,
+                             "launch_us": round(t_scores * 1e3 / 2, 2),
+                             "hbm_gbs_of_k": round(2 * units * L * 256 / (t_scores * 1e-3) / 1e9,
+                                                   1)},
+                "cpu_baseline": None, "e2e": None, "clocks": clocks,
+                "gpu_launches": None, "sweep": cells, "impl": "ours"}
+        print(json.dumps(line), flush=True)
+
+
 # --------------------------------------------------------------------------------- reference
 def run_reference(args):
     """The oracle (plain fp64 CPU implementation) timed on the host cores, same metric/config."""
@@ -512,8 +636,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    from sparse_kv_cache_snapkv_gb300 import synthetic as S
-    wl = S.WORKLOADS[args.workload]
+    wl = select_workload(args)
     keep = wl.keep or min(wl.max_len, wl.budget * wl.page * 128 // wl.channels)
     cores = min(16, len(os.sched_getaffinity(0)))
     _oracle_worker_init_env()
@@ -552,6 +675,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "prefill128k":
+        run_prefill_sweep(args)
     else:
         run_ours(args)
 

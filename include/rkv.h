@@ -123,6 +123,20 @@ rkv_status rkv_snapkv_compress(const void* k, const void* v, const int32_t* seq_
                                int32_t* out_len, float* scores_out, void* ws, size_t ws_bytes,
                                void* stream);
 
+/* [SNAP++] The scoring half of rkv_snapkv_compress alone: for each unit u and KV head g, the
+ * score of every prefix position i < L_u - window (softmax probabilities of the window queries
+ * over the keys each may see, summed over the window and over the gqa query heads of the group),
+ * with no pooling, selection or gather. For a caller that pools or selects by its own rule, and
+ * for timing the two tensor-core score passes on their own.
+ *   k, seq_lens, q_win, window, scale as rkv_snapkv_compress (no V needed)
+ *   scores_out [n][n_kv][max_len - window] fp32 (required): entries i >= L_u - window of a
+ *             unit are left untouched
+ * Workspace rkv_snapkv_workspace_bytes; errors as rkv_snapkv_compress. */
+rkv_status rkv_snapkv_scores(const void* k, const int32_t* seq_lens, const void* q_win, int n,
+                             int n_kv, int gqa, int head_dim, int max_len, int window,
+                             float scale, float* scores_out, void* ws, size_t ws_bytes,
+                             void* stream);
+
 /* [MT] The selection half of rkv_snapkv_compress (scores, pooling, top-k) without the gather:
  * RocketKV-MT evicts nothing, so each turn filters the full, unfiltered history again
  * ("SCBench Results": the next turn's prefill takes all earlier tokens as its prefix and SnapKV++
@@ -209,12 +223,14 @@ rkv_status rkv_build_page_summaries(const void* k_cache, const int32_t* len, int
 /* ------------------------------------------------------------------------------------------ */
 /* Stage 2: hybrid sparse decode ([APPROX], [LAT], [STEP], [PAGE])                              */
 /* ------------------------------------------------------------------------------------------ */
+/* The decode's workspace: the status word and one append counter per unit (both zero at first
+ * use; the counters are back at zero after every call). */
 size_t rkv_hybrid_decode_workspace_bytes(int n, int n_kv, int gqa, int page_cap, int budget,
                                          int page);
 
 /* One decode step. If new_k / new_v are given, token len_u is first appended to every KV head
- * of unit u (cache rows and the page summary it lands in) and len[u] is incremented; the new
- * token can be selected in this step. Then, per (unit, KV head g):
+ * of unit u (cache rows and the page summary it lands in) and len[u] is incremented, inside the
+ * same launch; the new token can be selected in this step. Then, per (unit, KV head g):
  *   len_u <= budget: exact attention over every cached token;
  *   otherwise: the `channels` channels with the largest sum over the group of |q_h| (ties ->
  *   lower channel) are kept; with q_g = sum_h q_h, each page scores

@@ -34,7 +34,8 @@ def _stale() -> bool:
         return True
     t = os.path.getmtime(LIB)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    deps.append(os.path.join(ROOT, "include", "rkv.h"))
+    inc = os.path.join(ROOT, "include")
+    deps += [os.path.join(inc, f) for f in os.listdir(inc)]
     deps.append(os.path.abspath(__file__))
     return any(os.path.getmtime(d) > t for d in deps)
 

@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "../../include/rkv.h"
+#include "../../include/rkv_testing.h"
 #include "rkv_internal.h"
 
 using namespace rkv;
@@ -157,16 +158,25 @@ static rkv_status snapkv_impl(const void* k, const void* v, const int32_t* seq_l
                               void* stream, bool per_head, const PagedMap& out_pm,
                               int page = 0, int page_cap = 0, void* kmin = nullptr,
                               void* kmax = nullptr, bool pool_avg = false,
-                              int kept_stride = 0) {
+                              int kept_stride = 0, bool scores_only = false,
+                              uint64_t wait_limit_ns = 0, int test_skip_tile = 0) {
   if (head_dim != kHeadDim) return RKV_ERR_UNSUPPORTED;
+  if (scores_only) {  // scores only: no V, no selection or gather outputs
+    if (!scores_out || v || k_out || v_out || kept_idx || out_len || kmin || kmax)
+      return RKV_ERR_INVALID_ARG;
+    kept_stride = 0;
+    keep = window + 1;
+    cap = keep;
+  }
   // kept_stride > 0: index-only selection (no v, no compact cache, no gather)
   const bool index_only = kept_stride > 0;
   if (index_only) {
     if (k_out || v_out || kmin || kmax || kept_stride < keep) return RKV_ERR_INVALID_ARG;
     cap = keep;
   }
-  if (!k || (!v && !index_only) || !seq_lens || !q_win ||
-      (!index_only && (!k_out || !v_out)) || !kept_idx || !out_len)
+  if (!k || (!v && !index_only && !scores_only) || !seq_lens || !q_win ||
+      (!index_only && !scores_only && (!k_out || !v_out)) ||
+      (!scores_only && (!kept_idx || !out_len)))
     return RKV_ERR_INVALID_ARG;
   if (!aligned16(k) || (v && !aligned16(v)) || !aligned16(q_win) ||
       (k_out && !aligned16(k_out)) || (v_out && !aligned16(v_out)) ||
@@ -217,6 +227,9 @@ static rkv_status snapkv_impl(const void* k, const void* v, const int32_t* seq_l
   a.v_out = static_cast<bf16*>(v_out);
   a.kept_idx = kept_idx;
   a.out_len = out_len;
+  a.scores_only = scores_only ? 1 : 0;
+  a.wait_limit_ns = wait_limit_ns;
+  a.test_skip_tile = test_skip_tile;
   snapkv_plan(n, n_kv, gqa, max_len, window, &a.nsplit, &a.tokens_per_split, &a.rows_pad);
   // workspace carve: [status][pooled][scores (if not given)][split partials]
   unsigned char* p = static_cast<unsigned char*>(ws) + kStatusBytes;
@@ -271,6 +284,29 @@ rkv_status rkv_snapkv_select(const void* k, const int32_t* seq_lens, const void*
                      kernel_size, keep, scale, nullptr, nullptr, keep, kept_idx, out_len,
                      scores_out, ws, ws_bytes, stream, false, PagedMap{}, 0, 0, nullptr, nullptr,
                      false, kept_stride);
+}
+
+rkv_status rkv_snapkv_scores(const void* k, const int32_t* seq_lens, const void* q_win, int n,
+                             int n_kv, int gqa, int head_dim, int max_len, int window,
+                             float scale, float* scores_out, void* ws, size_t ws_bytes,
+                             void* stream) {
+  RKV_TRACE();
+  return snapkv_impl(k, nullptr, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window, 0, 0,
+                     scale, nullptr, nullptr, 0, nullptr, nullptr, scores_out, ws, ws_bytes,
+                     stream, false, PagedMap{}, 0, 0, nullptr, nullptr, false, 0, true);
+}
+
+rkv_status rkv_testing_scores_wait_timeout(const void* k, const int32_t* seq_lens,
+                                           const void* q_win, int n, int n_kv, int gqa,
+                                           int head_dim, int max_len, int window, float scale,
+                                           float* scores_out, uint64_t wait_limit_ns, void* ws,
+                                           size_t ws_bytes, void* stream) {
+  RKV_TRACE();
+  if (wait_limit_ns < 1000ull || wait_limit_ns > 1000000000ull) return RKV_ERR_INVALID_ARG;
+  return snapkv_impl(k, nullptr, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window, 0, 0,
+                     scale, nullptr, nullptr, 0, nullptr, nullptr, scores_out, ws, ws_bytes,
+                     stream, false, PagedMap{}, 0, 0, nullptr, nullptr, false, 0, true,
+                     wait_limit_ns, 1);
 }
 
 rkv_status rkv_snapkv_compress_summarized(const void* k, const void* v,
@@ -362,13 +398,12 @@ rkv_status rkv_build_page_summaries_mt(const void* k_full, const int32_t* kept_i
 // ------------------------------------------------------------------------------- hybrid
 size_t rkv_hybrid_decode_workspace_bytes(int n, int n_kv, int gqa, int page_cap, int budget,
                                          int page) {
-  (void)n;
   (void)n_kv;
   (void)gqa;
   (void)page_cap;
   (void)budget;
   (void)page;
-  return kStatusBytes;
+  return kStatusBytes + hybrid_counter_bytes(n);
 }
 
 // One decode step over the cache (kept == nullptr) or over the kept sequence of the full cache.
@@ -397,28 +432,6 @@ static rkv_status hybrid_impl(const void* q, const void* new_k, const void* new_
       ws_bytes < rkv_hybrid_decode_workspace_bytes(n, n_kv, gqa, page_cap, budget, page))
     return RKV_ERR_WORKSPACE;
   cudaStream_t s = as_stream(stream);
-  if (new_k) {
-    AppendArgs ap{};
-    ap.new_k = static_cast<const bf16*>(new_k);
-    ap.new_v = static_cast<const bf16*>(new_v);
-    ap.k_cache = static_cast<bf16*>(k_cache);
-    ap.v_cache = static_cast<bf16*>(v_cache);
-    ap.len = len;
-    ap.kmin = static_cast<bf16*>(kmin);
-    ap.kmax = static_cast<bf16*>(kmax);
-    ap.kept = kept;
-    ap.full_len = full_len;
-    ap.pm = pm;
-    ap.n = n;
-    ap.n_kv = n_kv;
-    ap.cap = cap;
-    ap.vcap = vcap;
-    ap.page_cap = page_cap;
-    ap.page = page;
-    ap.status = status_ptr(ws);
-    cudaError_t e = launch_append(ap, s);
-    if (e != cudaSuccess) return RKV_ERR_CUDA;
-  }
   HybridArgsAll a{};
   a.pm = pm;
   a.q = static_cast<const bf16*>(q);
@@ -444,6 +457,9 @@ static rkv_status hybrid_impl(const void* q, const void* new_k, const void* new_
   a.sel_pages = sel_pages;
   a.approx = approx_scores;
   a.status = status_ptr(ws);
+  a.ap.new_k = static_cast<const bf16*>(new_k);
+  a.ap.new_v = static_cast<const bf16*>(new_v);
+  a.ap.acount = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(ws) + kStatusBytes);
   return from_cuda(launch_hybrid(a, s));
 }
 

@@ -125,13 +125,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 // returns false (the caller records RKV_DEV_WAIT_TIMEOUT and abandons its unit).
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_addr(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -396,20 +397,27 @@ static_assert(offsetof(FastSelectSmem, cnt) % 16 == 0, "cnt alignment");
 // passes the max / min of the ordered keys (ordered_key) it produced (0 / ~0 if none); this
 // records the per-warp range and clears the histograms. A barrier must separate it from
 // block_topk_fast (the one that publishes the keys serves).
-__device__ __forceinline__ void fast_select_prepare(uint32_t hi, uint32_t lo, FastSelectSmem& sm) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  hi = __reduce_max_sync(0xffffffffu, hi);
-  lo = __reduce_min_sync(0xffffffffu, lo);
-  if (lane == 0) {
-    sm.wmax[warp] = hi;
-    sm.wmin[warp] = lo;
-  }
+// Clears the histograms and the candidate count (the part of fast_select_prepare that does not
+// depend on the keys).
+__device__ __forceinline__ void fast_select_clear(FastSelectSmem& sm) {
+  const int tid = threadIdx.x;
   uint4* h = reinterpret_cast<uint4*>(sm.h11);
   h[2 * tid] = make_uint4(0u, 0u, 0u, 0u);
   h[2 * tid + 1] = make_uint4(0u, 0u, 0u, 0u);
   if (tid < 16) reinterpret_cast<uint4*>(sm.coarse)[tid] = make_uint4(0u, 0u, 0u, 0u);
   reinterpret_cast<uint4*>(&sm.hist[0][0][0])[tid] = make_uint4(0u, 0u, 0u, 0u);
   if (tid == 0) sm.ncand = 0;
+}
+
+__device__ __forceinline__ void fast_select_prepare(uint32_t hi, uint32_t lo, FastSelectSmem& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  if (lane == 0) {
+    sm.wmax[warp] = hi;
+    sm.wmin[warp] = lo;
+  }
+  fast_select_clear(sm);
 }
 
 // Same contract as block_topk_ascending (k largest, ties -> lower index, indices written
@@ -805,6 +813,194 @@ __device__ __forceinline__ int block_topk_1024(const float* keys, int n, int k, 
     eb += e[j] ? 1 : 0;
   }
   return (int)(all >> 16) + min((int)(all & 0xffffu), need_eq);
+}
+
+// ------------------------------------------------------------------------------------------
+// Top-k of page scores by value bins, for one 256-thread block (the decode's page select)
+// ------------------------------------------------------------------------------------------
+// The scores are binned linearly in value between their minimum and maximum (kBinFine bins,
+// bin 0 at the top, grouped into 32 coarse bins of 32). The map is monotone and deterministic,
+// so every key of a higher bin is larger than every key of a lower bin, and equal keys share a
+// bin. Every warp finds the fine bin F of the k-th largest key from the histograms on its own
+// (a scan of the coarse bins, then of the 32 fine bins of the chosen one). When all of F's keys
+// are needed -- with about one key per fine bin, nearly always -- the rule "bin <= F" selects the
+// k largest. Otherwise F's keys are ranked exactly by (key desc, index asc) and the k-th one
+// (key, index) decides: a page is taken iff its key is larger, or equal with an index not above.
+// The result equals block_topk_ascending's (k largest, ties -> lower index, ascending).
+constexpr int kBinFine = 1024;
+constexpr int kMaxCand = 256;
+
+struct __align__(16) BinSelectSmem {
+  uint32_t fine[kBinFine];     // fine histogram (shared by the warps)
+  uint32_t wh[8][32];          // per-warp coarse histograms (one word per thread)
+  uint2 cand[kMaxCand];        // (ordered key, page) of the k-th key's fine bin
+  uint32_t cnt[4][8];          // per key round and warp: pages taken
+  uint32_t wmax[8], wmin[8];   // per-warp range of the ordered keys
+  uint2 kth;
+  int ncand;
+};
+static_assert(offsetof(BinSelectSmem, fine) % 16 == 0, "fine alignment");
+static_assert(offsetof(BinSelectSmem, cnt) % 16 == 0, "cnt alignment");
+static_assert(offsetof(BinSelectSmem, wmax) % 16 == 0, "wmax alignment");
+static_assert(offsetof(BinSelectSmem, wmin) % 16 == 0, "wmin alignment");
+
+// Inverse of ordered_key.
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// First phase, fused into whatever produces the keys: each thread passes the max / min of the
+// ordered keys it produced (0 / ~0 if none). Records the per-warp range and clears the
+// histograms. A barrier must separate it from bin_topk.
+__device__ __forceinline__ void bin_select_prepare(uint32_t hi, uint32_t lo, BinSelectSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  if (lane == 0) {
+    sm.wmax[warp] = hi;
+    sm.wmin[warp] = lo;
+  }
+  reinterpret_cast<uint4*>(sm.fine)[tid] = make_uint4(0u, 0u, 0u, 0u);
+  (&sm.wh[0][0])[tid] = 0u;
+  if (tid == 0) sm.ncand = 0;
+}
+
+// k largest of scores[0..n) (1 <= k < n <= 1024 NR), page indices written ascending to
+// out[0..k). Thread t reads the pages 1024 r + 4 t + e (r < NR, e < 4) as one float4 per round
+// (`scores` 16-byte aligned, padded to a multiple of 4). Returns false, with nothing written
+// and every thread agreeing, when the scores' range is not a normal finite
+// positive number (NaN, infinities, all equal) or the k-th key's fine bin holds more than
+// kMaxCand keys: the caller then runs a general select. Ends without a barrier on success.
+template <int NR>
+__device__ __forceinline__ bool bin_topk(const float* scores, int n, int k, int* out,
+                                         BinSelectSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t hi, lo;
+  {
+    const uint4 a0 = reinterpret_cast<const uint4*>(sm.wmax)[0];
+    const uint4 a1 = reinterpret_cast<const uint4*>(sm.wmax)[1];
+    const uint4 b0 = reinterpret_cast<const uint4*>(sm.wmin)[0];
+    const uint4 b1 = reinterpret_cast<const uint4*>(sm.wmin)[1];
+    hi = max(max(max(a0.x, a0.y), max(a0.z, a0.w)), max(max(a1.x, a1.y), max(a1.z, a1.w)));
+    lo = min(min(min(b0.x, b0.y), min(b0.z, b0.w)), min(min(b1.x, b1.y), min(b1.z, b1.w)));
+  }
+  const float smax = key_value(hi), smin = key_value(lo);
+  const float range = smax - smin;
+  if (!(range >= 1e-30f) || !(range <= 3.0e38f)) return false;
+  const float inv = (float)kBinFine / range;
+  float f[NR][4];
+  bool v[NR][4];
+  int fb[NR][4];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    const int p0 = 1024 * r + 4 * tid;
+    const float4 x = p0 < n ? reinterpret_cast<const float4*>(scores)[256 * r + tid]
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    f[r][0] = x.x;
+    f[r][1] = x.y;
+    f[r][2] = x.z;
+    f[r][3] = x.w;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[r][e] = p0 + e < n;
+      fb[r][e] = min(kBinFine - 1, (int)((smax - f[r][e]) * inv));
+      if (v[r][e]) {
+        atomicAdd(&sm.fine[fb[r][e]], 1u);
+        atomicAdd(&sm.wh[warp][fb[r][e] >> 5], 1u);
+      }
+    }
+  }
+  __syncthreads();
+  // every warp: the coarse bin C of the k-th key (lane l = coarse bin l, from the top), then
+  // the fine bin F inside it (lane l = fine bin 32 C + l)
+  int c = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) c += (int)sm.wh[w][lane];
+  int incl = warp_incl_scan(c);
+  uint32_t b = __ballot_sync(0xffffffffu, incl >= k);
+  const int C = __ffs(b) - 1;
+  const int above_c = __shfl_sync(0xffffffffu, incl - c, C);
+  const int cf = (int)sm.fine[32 * C + lane];
+  incl = warp_incl_scan(cf) + above_c;
+  b = __ballot_sync(0xffffffffu, incl >= k);
+  const int fl = __ffs(b) - 1;
+  const int F = 32 * C + fl;
+  const int above = __shfl_sync(0xffffffffu, incl - cf, fl);
+  const int nF = __shfl_sync(0xffffffffu, cf, fl);
+  const int remaining = k - above;  // 1 .. nF keys of bin F are taken
+  uint2 kth = make_uint2(0u, 0u);
+  const bool whole = nF == remaining;
+  if (!whole && nF > kMaxCand) return false;
+  if (!whole) {
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (v[r][e] && fb[r][e] == F) {
+          const int slot = atomicAdd(&sm.ncand, 1);
+          sm.cand[slot] = make_uint2(ordered_key(f[r][e]), (uint32_t)(1024 * r + 4 * tid + e));
+        }
+    __syncthreads();
+    if (tid < nF) {
+      const uint2 me = sm.cand[tid];
+      int rank = 0;
+#pragma unroll 4
+      for (int j = 0; j < nF; ++j) {
+        const uint2 o = sm.cand[j];
+        rank += (o.x > me.x || (o.x == me.x && o.y < me.y)) ? 1 : 0;
+      }
+      if (rank == remaining - 1) sm.kth = me;  // ranks are a permutation: exactly one writer
+    }
+    __syncthreads();
+    kth = sm.kth;
+  }
+  // compaction in page order: (round, thread, e) is ascending
+  const uint32_t lt = (1u << lane) - 1u;
+  bool t[NR][4];
+  int pre[NR];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    int cr = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t pg = (uint32_t)(1024 * r + 4 * tid + e);
+      bool take;
+      if (whole) {
+        take = fb[r][e] <= F;
+      } else {
+        const uint32_t key = ordered_key(f[r][e]);
+        take = fb[r][e] < F ||
+               (fb[r][e] == F && (key > kth.x || (key == kth.x && pg <= kth.y)));
+      }
+      t[r][e] = v[r][e] && take;
+      cr += t[r][e] ? 1 : 0;
+    }
+    const uint32_t g0 = __ballot_sync(0xffffffffu, cr & 1);
+    const uint32_t g1 = __ballot_sync(0xffffffffu, cr & 2);
+    const uint32_t g2 = __ballot_sync(0xffffffffu, cr & 4);
+    pre[r] = __popc(g0 & lt) + 2 * __popc(g1 & lt) + 4 * __popc(g2 & lt);
+    if (lane == 0) sm.cnt[r][warp] = __popc(g0) + 2 * __popc(g1) + 4 * __popc(g2);
+  }
+  __syncthreads();
+  int base = 0;
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    const uint4 c0 = reinterpret_cast<const uint4*>(sm.cnt[r])[0];
+    const uint4 c1 = reinterpret_cast<const uint4*>(sm.cnt[r])[1];
+    const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    uint32_t before = 0u, all = 0u;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      before += (w < warp) ? cw[w] : 0u;
+      all += cw[w];
+    }
+    int pos = base + (int)before + pre[r];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (t[r][e]) out[pos++] = 1024 * r + 4 * tid + e;
+    base += (int)all;
+  }
+  return true;
 }
 
 }  // namespace rkv

@@ -34,6 +34,7 @@ constexpr int kStageElems = 2 * kChunkTokens * kRowPad;         // K rows then V
 constexpr int kStageBytes = kStageElems * 2;                    // 34,816 B
 constexpr int kDecStages = 2;                                   // one per warp group
 
+
 // ------------------------------------------------------------------------------------------
 // warp-level MMA helpers
 // ------------------------------------------------------------------------------------------
@@ -114,13 +115,28 @@ struct MmaAttn {
     for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = 0.f;
   }
 
+  // Lane roles of the two ldmatrix operands: the K row (token n_k) and 16-byte half kh this lane
+  // addresses for S = Q K^T, and the V row (token n_v) and column block cb for O += P V.
+  static __device__ __forceinline__ int k_row(int ln) { return (ln & 7) + ((ln >> 4) << 3); }
+  static __device__ __forceinline__ int k_col(int ln) { return ((ln >> 3) & 1) * 8; }
+  static __device__ __forceinline__ int v_row(int ln) { return (ln & 7) + (((ln >> 3) & 1) << 3); }
+  static __device__ __forceinline__ int v_col(int ln) { return (ln >> 4) << 3; }
+
   // tokens tok0 .. tok0 + 15 of a stage with `ntok` valid rows (rows >= ntok of V are zero)
   __device__ __forceinline__ void step16(const bf16* Ks, const bf16* Vs, int tok0, int ntok,
                                          float scale_log2) {
+    step16_at(Ks + (tok0 + k_row(lane)) * kRowPad + k_col(lane),
+              Vs + (tok0 + v_row(lane)) * kRowPad + v_col(lane), tok0, ntok, scale_log2);
+  }
+
+  // The same step with this lane's ldmatrix row addresses given (rows anywhere in shared memory,
+  // each kRowPad-aligned as staged): kaddr = row k_row(lane) + k_col(lane), vaddr = row
+  // v_row(lane) + v_col(lane) of the 16-token unit.
+  __device__ __forceinline__ void step16_at(const bf16* kaddr, const bf16* vaddr, int tok0,
+                                            int ntok, float scale_log2) {
     float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
     {
-      const int n = (lane & 7) + ((lane >> 4) << 3), kh = (lane >> 3) & 1;
-      const uint32_t base = smem_addr(Ks + (tok0 + n) * kRowPad + kh * 8);
+      const uint32_t base = smem_addr(kaddr);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         uint32_t b0, b1, b2, b3;
@@ -155,8 +171,7 @@ struct MmaAttn {
       o[nt][1] *= alpha;
     }
     {
-      const int tr = (lane & 7) + (((lane >> 3) & 1) << 3), cb = (lane >> 4) << 3;
-      const uint32_t base = smem_addr(Vs + (tok0 + tr) * kRowPad + cb);
+      const uint32_t base = smem_addr(vaddr);
 #pragma unroll
       for (int np = 0; np < 8; ++np) {
         uint32_t v0, v1, v2, v3;
@@ -218,6 +233,31 @@ __device__ __forceinline__ void warp_merge(const CombineSmem<G>* cs, int h, int 
   *O = oo;
 }
 
+// Per-warp partial state in the warp's own staging rows (no other warp touches them, so no
+// block barrier is needed before depositing): m[G], l[G], then o[G][kORow] (rows padded to 136
+// floats so that the fragment stores of the G rows fall in distinct banks).
+constexpr int kORow = 136;
+template <int G>
+__device__ __forceinline__ float* warp_state(bf16* stages, int w, size_t wstride) {
+  return reinterpret_cast<float*>(stages + (size_t)w * wstride);
+}
+static_assert((2 * 8 + 8 * kORow) * 4 <= 2 * 16 * kRowPad * 2, "warp state fits its rows");
+
+template <int G>
+__device__ __forceinline__ void warp_deposit_own(const MmaAttn<G>& at, float* st) {
+  const float lt = at.row_l();
+  if (at.r0 < G) {
+    if (at.t == 0) {
+      st[at.r0] = at.m;
+      st[G + at.r0] = lt;
+    }
+    float* o = st + 2 * G + at.r0 * kORow + 2 * at.t;
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+      *reinterpret_cast<float2*>(o + nt * 8) = make_float2(at.o[nt][0], at.o[nt][1]);
+  }
+}
+
 // Zero V rows [ntok, round_up(ntok, 16)) of a partially filled stage so that P = 0 never meets
 // stale bits there (0 * NaN would poison the accumulators). Called by the 128 threads of a group.
 __device__ __forceinline__ void zero_tail_rows(bf16* Vs, int ntok, int gtid) {
@@ -247,26 +287,67 @@ size_t hybrid_smem_bytes(int gqa, int page_cap, int budget, int page) {
   return b;
 }
 
+// Wide layout, for launches of at most one CTA per SM: the staging area holds either every kept
+// channel's summary row at once (the page-score GEMV reads them from shared memory after one
+// round of copies) or every selected token's K and V rows at once (each warp stages all of its
+// 16-token units before it waits). Returns 0 when that does not fit beside the scores and the
+// selection in kWideSmemMax bytes.
+constexpr size_t kWideSmemMax = 190 * 1024;
+constexpr size_t kUnitRowsBytes = (size_t)2 * 16 * kRowPad * 2;  // one 16-token unit, K + V
+
+__host__ __device__ inline int wide_units_per_warp(int budget) {
+  const int units = ((budget / 2) + 15) / 16;
+  return (units + 7) / 8;
+}
+
+__host__ __device__ inline size_t wide_region_bytes(int channels, int page_cap, int budget) {
+  const size_t gemv = (size_t)channels * page_cap * 2;
+  const size_t att = (size_t)8 * wide_units_per_warp(budget) * kUnitRowsBytes;
+  size_t r = gemv > att ? gemv : att;
+  const size_t base = (size_t)kDecStages * kStageBytes;
+  return align_up(r > base ? r : base, 16);
+}
+
+// After the region, the scores and the selection, the wide layout holds the kept rows'
+// addresses (kHeadDim pointers); being larger, its size never equals the ordinary layout's, by
+// which the kernel tells the two apart.
+__host__ __device__ inline size_t wide_smem_bytes(int channels, int page_cap, int budget) {
+  const size_t b = wide_region_bytes(channels, page_cap, budget) +
+                   2 * align_up((size_t)page_cap * 4, 16) + kHeadDim * sizeof(void*);
+  return b <= kWideSmemMax ? b : 0;
+}
+
 // MODE 0: the sequence is the cache itself (A = HybridArgs, whose smaller parameter block keeps
-// the plain launch cheaper); 1: the kept list of the full cache (RocketKV-MT, A = HybridArgsMT);
-// 2: a paged cache (A = HybridArgsPaged).
+// the plain launch cheaper); 3: the same with this step's token appended first
+// (A = HybridArgsApp); 1: the kept list of the full cache (RocketKV-MT, A = HybridArgsMT);
+// 2: a paged cache (A = HybridArgsPaged). Modes 1 and 2 append when a.ap.new_k is set.
 template <int G, int MODE, typename A>
 __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(A a) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  __shared__ float qs[G * kHeadDim];
-  __shared__ __align__(16) uint32_t umag[kHeadDim];
-  __shared__ float qg[kHeadDim];
+  __shared__ __align__(16) uint32_t ukey[kHeadDim];  // ordered key of sum_h |q_h[c]|
+  __shared__ float qg[kHeadDim];                     // sum_h q_h[c]
   __shared__ int chosen[kHeadDim];
+  __shared__ int part_rank[kHeadDim];
+  __shared__ int wcnt[4];
+  __shared__ BinSelectSmem bsel;
   __shared__ union {
     SelectScratch generic;
     FastSelectSmem fast;
   } sel_smem;
   __shared__ uint2 qfrag[8 * 32];
 
+  // The launch picks the layout through the dynamic shared-memory size: the wide one (see
+  // wide_smem_bytes) when it allotted exactly that much.
+  uint32_t dsmem;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dsmem));
+  const size_t wbytes = wide_smem_bytes(a.channels, a.page_cap, a.budget);
+  const bool wide = wbytes != 0 && dsmem == (uint32_t)wbytes;
+  const size_t region = wide ? wide_region_bytes(a.channels, a.page_cap, a.budget)
+                             : (size_t)kDecStages * kStageBytes;
+  const int upw = wide ? wide_units_per_warp(a.budget) : 1;  // 16-token units staged per warp
   bf16* stages = reinterpret_cast<bf16*>(smem);
-  float* scores = reinterpret_cast<float*>(smem + (size_t)kDecStages * kStageBytes);
-  int* sel = reinterpret_cast<int*>(smem + (size_t)kDecStages * kStageBytes +
-                                    align_up((size_t)a.page_cap * 4, 16));
+  float* scores = reinterpret_cast<float*>(smem + region);
+  int* sel = reinterpret_cast<int*>(smem + region + align_up((size_t)a.page_cap * 4, 16));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ukv = blockIdx.x;
@@ -275,11 +356,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(A a) {
   const int hq = a.n_kv * G;
   pdl_wait();     // inputs may come from the kernel before this one in the stream
   pdl_trigger();  // the next decode step may be scheduled while this one runs
-  // q and len are loaded together (q's address does not depend on len)
+  // q and len are loaded together (q's address does not depend on len): thread c < 128 loads
+  // channel c of every query head of the group
   const bf16* qgroup = a.q + ((size_t)u * hq + g * G) * kHeadDim;
-  uint4 qraw = make_uint4(0u, 0u, 0u, 0u);
-  if (tid < G * 16) qraw = *reinterpret_cast<const uint4*>(qgroup + tid * 8);
-  const int len = a.len[u];
+  float qv[G];
+  if (tid < kHeadDim) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) qv[h] = __bfloat162float(qgroup[h * kHeadDim + tid]);
+  }
+  int len = a.len[u];
   int flen = a.cap;  // rows a kept index may name
   int vcap = a.cap;  // bound of len
   if constexpr (MODE == 1) {
@@ -287,35 +372,83 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(A a) {
     vcap = a.vcap;
   }
   if constexpr (MODE == 2) vcap = a.pm.max_blocks * a.pm.block;
+  bool appended = false;  // this launch appended the unit's token (length advanced at the end)
+  const int len0 = len;
+  int arow = 0;
+  if constexpr (MODE != 0) {
+    if (a.ap.new_k != nullptr) {
+      // ---- append this step's token before attending (it is selectable in this step) ----
+      // threads 0..127 write the K row and fold it into its page's Kmin / Kmax, threads
+      // 128..255 the V row. The unit's length advances at the end of the launch: the last of
+      // the unit's KV-head CTAs to finish (all of them read the length at their start) writes it.
+      const int row = (MODE == 1) ? flen : len;  // cache row receiving the token
+      arow = row;
+      const int pg0 = len / a.page;
+      const bool fits = len >= 0 && len < vcap && pg0 < a.page_cap && row >= 0 && row < a.cap;
+      if (fits) {
+        const int c = tid & (kHeadDim - 1);
+        size_t dst;
+        if constexpr (MODE == 2)
+          dst = paged_row(a.pm, paged_block(a.pm, u, len, a.status), a.n_kv, g, len);
+        else
+          dst = (size_t)ukv * a.cap + row;
+        const size_t src = (size_t)ukv * kHeadDim + c;
+        if (tid < kHeadDim) {
+          const size_t si = src * a.page_cap + pg0;
+          const bf16 kval = a.ap.new_k[src];
+          const bool fresh = len % a.page == 0;  // the token opens a new page
+          bf16 omin = kval, omax = kval;
+          if (!fresh) {
+            omin = a.kmin[si];
+            omax = a.kmax[si];
+          }
+          const float kf = __bfloat162float(kval);
+          const_cast<bf16*>(a.k_cache)[dst * kHeadDim + c] = kval;
+          const_cast<bf16*>(a.kmin)[si] = (fresh || kf < __bfloat162float(omin)) ? kval : omin;
+          const_cast<bf16*>(a.kmax)[si] = (fresh || kf > __bfloat162float(omax)) ? kval : omax;
+        } else {
+          const_cast<bf16*>(a.v_cache)[dst * kHeadDim + c] = a.ap.new_v[src];
+          if constexpr (MODE == 1) {
+            if (c == 0) const_cast<int32_t*>(a.kept)[(size_t)ukv * vcap + len] = row;
+          }
+        }
+        appended = true;
+      } else if (tid == 0) {
+        set_status(a.status, RKV_DEV_LEN_OVER_CAP);
+      }
+      __syncthreads();  // the new row and summary are visible to this CTA's reads below
+      if (fits) {
+        ++len;
+        if constexpr (MODE == 1) flen = row + 1;
+      }
+    }
+  }
   const int p = a.page;
   const int P = (len + p - 1) / p;
   const int S = (a.budget / 2) / p;
   const bool dense = len <= a.budget;
-
+  const size_t cache_base = (size_t)ukv * a.cap;
   if (len <= 0 || len > vcap || P > a.page_cap) {
     if (tid == 0 && len != 0) set_status(a.status, RKV_DEV_LEN_OVER_CAP);
+    if constexpr (MODE != 0) {
+      if (appended && tid == 0 && atomicAdd(&a.ap.acount[u], 1) == a.n_kv - 1) {
+        a.ap.acount[u] = 0;
+        const_cast<int32_t*>(a.len)[u] = len0 + 1;
+        if constexpr (MODE == 1) const_cast<int32_t*>(a.full_len)[u] = arow + 1;
+      }
+    }
     return;
   }
-
-  // ---- q: raw values to shared memory -------------------------------------------------
-  if (tid < G * 16) {
-    float f[8];
-    unpack8(qraw, f);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) qs[tid * 8 + i] = f[i];
-  }
-  __syncthreads();
 
   // ---- group sums: |q| for the channel pick, signed q for the score --------------------
   if (tid < kHeadDim) {
     float s = 0.f, t = 0.f;
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const float x = qs[h * kHeadDim + tid];
-      s += fabsf(x);
-      t += x;
+      s += fabsf(qv[h]);
+      t += qv[h];
     }
-    umag[tid] = ordered_key(s);
+    ukey[tid] = ordered_key(s);
     qg[tid] = t;
   }
   __syncthreads();
@@ -323,56 +456,38 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(A a) {
   int nsel;
   if (!dense) {
     // ---- channel pick: top-c of sum_h |q_h| (ties -> lower channel), ascending -----------
+    // Threads c and c + 128 rank channel c against channels 0..63 and 64..127 by the unique
+    // order (key desc, channel asc); the ranks are a permutation, so exactly the channels of
+    // rank < cn are taken, placed in channel order by the ballots of warps 0..3.
     const int cn = a.channels;
-    if (warp >= 4) {
-      // Meanwhile warps 4..7 bring the summary rows of every channel that can still be picked
-      // into L2: warp 4 + v finds the ceil(cn / 4)-th largest key of channels 32v .. 32v + 31;
-      // those four top sets hold at least cn channels, all at or above the smallest of the
-      // four bounds, so the picked channels are among the channels that reach it.
-      const int c = tid - 128;
-      const uint32_t mine = umag[c];
-      const int kw = (cn + 3) >> 2;
-      uint32_t v = mine, m = 0u;
-      for (int i = 0; i < kw; ++i) {
-        m = __reduce_max_sync(0xffffffffu, v);
-        const uint32_t who = __ballot_sync(0xffffffffu, v == m);
-        if (lane == __ffs(who) - 1) v = 0u;  // one instance leaves
+    {
+      const int c = tid & (kHeadDim - 1), half = tid >> 7;
+      const uint32_t mk = ukey[c];
+      const uint4* k4 = reinterpret_cast<const uint4*>(ukey + 64 * half);
+      int r = 0;
+#pragma unroll 4
+      for (int j4 = 0; j4 < 16; ++j4) {
+        const uint4 x = k4[j4];
+        const int j = 64 * half + 4 * j4;
+        r += (x.x > mk || (x.x == mk && j < c)) ? 1 : 0;
+        r += (x.y > mk || (x.y == mk && j + 1 < c)) ? 1 : 0;
+        r += (x.z > mk || (x.z == mk && j + 2 < c)) ? 1 : 0;
+        r += (x.w > mk || (x.w == mk && j + 3 < c)) ? 1 : 0;
       }
-      if (lane == 0) sel_smem.fast.wmin[warp - 4] = m;
-      group_sync(1);  // warps 4..7
-      const uint32_t bound = min(min(sel_smem.fast.wmin[0], sel_smem.fast.wmin[1]),
-                                 min(sel_smem.fast.wmin[2], sel_smem.fast.wmin[3]));
-      if (mine >= bound) {
-        const bf16* row = ((qg[c] >= 0.f) ? a.kmax : a.kmin) +
-                          ((size_t)ukv * kHeadDim + c) * a.page_cap;
-        prefetch_l2_bulk(row, (uint32_t)((P * 2 + 15) & ~15));
-      }
-      if (warp == 7) MmaAttn<G>::build_fragments(qs, qfrag);
-    }
-    if (warp < 4) {
-      // thread i ranks channel i among all 128 by the unique key (value, 127 - i), so ties go
-      // to the lower channel; ranks are a permutation, so exactly the channels of rank < cn are
-      // taken, and per-warp ballots place them in ascending channel order
-      const uint64_t mine = ((uint64_t)umag[tid] << 32) | (uint32_t)(kHeadDim - 1 - tid);
-      const uint4* u4 = reinterpret_cast<const uint4*>(umag);
-      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-#pragma unroll 8
-      for (int j4 = 0; j4 < kHeadDim / 4; ++j4) {
-        const uint4 x = u4[j4];
-        const uint32_t j = kHeadDim - 1 - 4 * j4;
-        r0 += ((((uint64_t)x.x << 32) | j) > mine) ? 1 : 0;
-        r1 += ((((uint64_t)x.y << 32) | (j - 1)) > mine) ? 1 : 0;
-        r2 += ((((uint64_t)x.z << 32) | (j - 2)) > mine) ? 1 : 0;
-        r3 += ((((uint64_t)x.w << 32) | (j - 3)) > mine) ? 1 : 0;
-      }
-      const bool take = r0 + r1 + r2 + r3 < cn;
-      const uint32_t b = __ballot_sync(0xffffffffu, take);
-      if (lane == 0) sel_smem.fast.wsum[warp] = __popc(b);
-      group_sync(0);  // warps 0..3
-      int before = 0;
+      if (half) part_rank[c] = r;
+      __syncthreads();
+      if (!half) {
+        const bool take = r + part_rank[c] < cn;
+        const uint32_t bt = __ballot_sync(0xffffffffu, take);
+        if (lane == 0) wcnt[warp] = __popc(bt);
+        group_sync(0);  // warps 0..3
+        int before = 0;
 #pragma unroll
-      for (int w = 0; w < 4; ++w) before += (w < warp) ? sel_smem.fast.wsum[w] : 0;
-      if (take) chosen[before + __popc(b & ((1u << lane) - 1u))] = tid;
+        for (int w = 0; w < 4; ++w) before += (w < warp) ? wcnt[w] : 0;
+        if (take) chosen[before + __popc(bt & ((1u << lane) - 1u))] = c;
+      } else if (warp == 7) {
+        MmaAttn<G>::build_fragments(qgroup, qfrag);
+      }
     }
     __syncthreads();
     if (a.sel_channels && tid < cn) a.sel_channels[(size_t)ukv * cn + tid] = chosen[tid];
@@ -382,28 +497,64 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(A a) {
     // (Kmax where q_g >= 0, else Kmin): a vector-matrix product over the kept rows, bound by
     // HBM, so plain fp32 FMAs on rows read straight from global memory (nothing staged).
     // Thread pair (2p, 2p + 1) takes the 8-page groups p, p + 128, ... (16 bytes of a row) over
-    // the even / odd kept channels; one shuffle joins the pair's partial sums. The same pass
-    // records the range of the scores' ordered keys and clears the select's histograms.
+    // the even / odd kept channels; one shuffle joins the pair's partial sums, and thread
+    // 2p + h keeps pages 4h .. 4h + 3 of the group, so thread t holds pages 1024 r + 4 t + e.
+    // The same pass records the range of the scores' ordered keys for the select.
     {
       const int h = tid & 1, pr = tid >> 1;
       const int ngroups = (P + 7) >> 3;
       const size_t rowbase = (size_t)ukv * kHeadDim;
       float* approx_row = a.approx ? a.approx + (size_t)ukv * a.page_cap : nullptr;
       uint32_t khi = 0u, klo = 0xffffffffu;
+      if (wide) {
+        // one round of 16-byte copies brings every kept row into shared memory (row i at
+        // stages + i * page_cap); the GEMV below then reads 16 bytes per (row, 8-page group).
+        // The rows' addresses are looked up once into shared memory, so that every thread
+        // issues its copies back to back.
+        const bf16** rowp = reinterpret_cast<const bf16**>(
+            smem + region + 2 * align_up((size_t)a.page_cap * 4, 16));
+        if (tid < cn) {
+          const int c = chosen[tid] & (kHeadDim - 1);
+          rowp[tid] = ((qg[c] >= 0.f) ? a.kmax : a.kmin) + (rowbase + c) * a.page_cap;
+        }
+        __syncthreads();
+        for (int cc = tid; cc < ngroups; cc += kDecodeThreads) {
+#pragma unroll 8
+          for (int i = 0; i < cn; ++i)
+            cp_async16(stages + (size_t)i * a.page_cap + cc * 8, rowp[i] + cc * 8);
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        __syncthreads();
+      }
       for (int gb = 0; gb < ngroups; gb += kDecodeThreads / 2) {
         const int gi = gb + pr;
         const bool valid = gi < ngroups;
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        if (valid) {
+        if (valid && !wide) {
           const size_t col = (size_t)gi * 8;
 #pragma unroll 16
           for (int i = h; i < cn; i += 2) {
             const int c = chosen[i] & (kHeadDim - 1);
             const float w = qg[c];
             const bf16* row = ((w >= 0.f) ? a.kmax : a.kmin) + (rowbase + c) * a.page_cap;
-            const uint4 x = __ldg(reinterpret_cast<const uint4*>(row + col));
+            // (the append variants may have written these rows in this launch: no
+            // non-coherent loads there)
+            const uint4 x = (MODE == 0) ? __ldg(reinterpret_cast<const uint4*>(row + col))
+                                        : __ldcg(reinterpret_cast<const uint4*>(row + col));
+            float f[8];
+            unpack8(x, f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(w, f[e], acc[e]);
+          }
+        } else if (valid) {
+          const bf16* srow = stages + (size_t)gi * 8;
+#pragma unroll 8
+          for (int i = h; i < cn; i += 2) {
+            const float w = qg[chosen[i] & (kHeadDim - 1)];
+            const uint4 x = *reinterpret_cast<const uint4*>(srow + (size_t)i * a.page_cap);
             float f[8];
             unpack8(x, f);
 #pragma unroll
@@ -430,7 +581,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(A a) {
           }
         }
       }
-      fast_select_prepare(khi, klo, sel_smem.fast);
+      bin_select_prepare(khi, klo, bsel);
       __syncthreads();
     }
 
@@ -439,20 +590,41 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(A a) {
       for (int i = tid; i < P; i += kDecodeThreads) sel[i] = i;
       nsel = P;
     } else {
-      int got;
+      bool done;
       if (P <= 1024)
-        got = block_topk_1024(scores, P, S, sel, sel_smem.fast);
+        done = bin_topk<1>(scores, P, S, sel, bsel);
       else if (P <= 2048)
-        got = block_topk_fast<8>(scores, P, S, sel, sel_smem.fast);
+        done = bin_topk<2>(scores, P, S, sel, bsel);
+      else if (P <= 3072)
+        done = bin_topk<3>(scores, P, S, sel, bsel);
       else if (P <= 4096)
-        got = block_topk_fast<16>(scores, P, S, sel, sel_smem.fast);
+        done = bin_topk<4>(scores, P, S, sel, bsel);
       else
-        got = block_topk_ascending(scores, P, S, sel, sel_smem.generic);
-      if (got != S && tid == 0) set_status(a.status, RKV_DEV_SELECT_FAILED);
+        done = false;
+      if (!done) {
+        // general select over the scores in shared memory (a range that is not a finite
+        // positive number, a crowded k-th bin, or more than 4096 pages)
+        if (tid < 8) {
+          sel_smem.fast.wmax[tid] = bsel.wmax[tid];
+          sel_smem.fast.wmin[tid] = bsel.wmin[tid];
+        }
+        fast_select_clear(sel_smem.fast);
+        __syncthreads();
+        int got;
+        if (P <= 1024)
+          got = block_topk_1024(scores, P, S, sel, sel_smem.fast);
+        else if (P <= 2048)
+          got = block_topk_fast<8>(scores, P, S, sel, sel_smem.fast);
+        else if (P <= 4096)
+          got = block_topk_fast<16>(scores, P, S, sel, sel_smem.fast);
+        else
+          got = block_topk_ascending(scores, P, S, sel, sel_smem.generic);
+        if (got != S && tid == 0) set_status(a.status, RKV_DEV_SELECT_FAILED);
+      }
       nsel = S;
     }
   } else {
-    if (warp == 7) MmaAttn<G>::build_fragments(qs, qfrag);
+    if (warp == 7) MmaAttn<G>::build_fragments(qgroup, qfrag);
     if (a.sel_channels && tid < a.channels) a.sel_channels[(size_t)ukv * a.channels + tid] = -1;
     for (int i = tid; i < P; i += kDecodeThreads) sel[i] = i;
     nsel = P;
@@ -465,92 +637,111 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) hybrid_decode_kernel(A a) {
 
   // ---- exact attention over the selected pages -------------------------------------------
   // The selected pages' tokens, in page order, are cut into 16-token units; warp w takes units
-  // w, w + 8, ...: it stages the unit's K and V rows with 16-byte cp.async into its own area
-  // (rows kRowPad apart), waits for its own copies only, and runs one MMA step over them.
-  const size_t cache_base = (size_t)ukv * a.cap;
+  // w, w + 8, ...: it stages up to `upw` of them at a time (one in the ordinary layout, all of
+  // its units in the wide one) with 16-byte cp.async into its own area (rows kRowPad apart),
+  // waits for its own copies only, and runs one MMA step per unit.
   const int lp = __ffs(p) - 1;  // log2(page)
   const int ntok_all = (nsel - 1) * p + min(p, len - sel[nsel - 1] * p);
   const int nunits = (ntok_all + 15) >> 4;
-  bf16* Kw = stages + (size_t)warp * (2 * 16 * kRowPad);
-  bf16* Vw = Kw + 16 * kRowPad;
+  const size_t wstride = (size_t)upw * (2 * 16 * kRowPad);  // one warp's area (bf16)
+  bf16* warea = stages + (size_t)warp * wstride;
   MmaAttn<G> at;
   at.init(qfrag);
-  for (int t = warp; t < nunits; t += kDecodeThreads / 32) {
-    const int v0 = t * 16;
-    const int nt = min(16, ntok_all - v0);
-    // lanes 0..15 copy a K row, lanes 16..31 the V row of the same token, 16 bytes each
-    const int half = (lane >> 4) & 1, c16 = lane & 15;
-    const bf16* cache = half ? a.v_cache : a.k_cache;
-    bf16* dst = (half ? Vw : Kw) + c16 * 8;
-    if constexpr (MODE == 2) {
-      // lane r looks up (and checks) the block of the unit's token r in the page table
-      int kblk = 0;
-      if (lane < nt) {
-        const int v = v0 + lane;
-        kblk = paged_block(a.pm, u, (sel[v >> lp] << lp) + (v & (p - 1)), a.status);
-      }
-      for (int r = 0; r < nt; ++r) {
-        const int v = v0 + r;
-        const int blk = __shfl_sync(0xffffffffu, kblk, r);
-        const size_t row = paged_row(a.pm, blk, a.n_kv, g, (sel[v >> lp] << lp) + (v & (p - 1)));
-        cp_async16(dst + r * kRowPad, cache + row * kHeadDim + c16 * 8);
-      }
-    } else if constexpr (MODE == 1) {
-      // lane r fetches the cache row of the unit's token r from the kept list, checked
-      int krow = 0;
-      if (lane < nt) {
-        const int v = v0 + lane;
-        const int t = (sel[v >> lp] << lp) + (v & (p - 1));
-        krow = a.kept[(size_t)ukv * vcap + t];
-        if (krow < 0 || krow >= flen) {
-          set_status(a.status, RKV_DEV_BAD_INDEX);
-          krow = 0;
+  for (int t0 = warp; t0 < nunits; t0 += 8 * upw) {
+    for (int j = 0; j < upw && t0 + 8 * j < nunits; ++j) {
+      const int t = t0 + 8 * j;
+      bf16* Kw = warea + (size_t)j * (2 * 16 * kRowPad);
+      bf16* Vw = Kw + 16 * kRowPad;
+      const int v0 = t * 16;
+      const int nt = min(16, ntok_all - v0);
+      // lanes 0..15 copy a K row, lanes 16..31 the V row of the same token, 16 bytes each
+      const int half = (lane >> 4) & 1, c16 = lane & 15;
+      const bf16* cache = half ? a.v_cache : a.k_cache;
+      bf16* dst = (half ? Vw : Kw) + c16 * 8;
+      if constexpr (MODE == 2) {
+        // lane r looks up (and checks) the block of the unit's token r in the page table
+        int kblk = 0;
+        if (lane < nt) {
+          const int v = v0 + lane;
+          kblk = paged_block(a.pm, u, (sel[v >> lp] << lp) + (v & (p - 1)), a.status);
+        }
+        for (int r = 0; r < nt; ++r) {
+          const int v = v0 + r;
+          const int blk = __shfl_sync(0xffffffffu, kblk, r);
+          const size_t row =
+              paged_row(a.pm, blk, a.n_kv, g, (sel[v >> lp] << lp) + (v & (p - 1)));
+          cp_async16(dst + r * kRowPad, cache + row * kHeadDim + c16 * 8);
+        }
+      } else if constexpr (MODE == 1) {
+        // lane r fetches the cache row of the unit's token r from the kept list, checked
+        int krow = 0;
+        if (lane < nt) {
+          const int v = v0 + lane;
+          const int tk = (sel[v >> lp] << lp) + (v & (p - 1));
+          krow = a.kept[(size_t)ukv * vcap + tk];
+          if (krow < 0 || krow >= flen) {
+            set_status(a.status, RKV_DEV_BAD_INDEX);
+            krow = 0;
+          }
+        }
+        for (int r = 0; r < nt; ++r) {
+          const size_t tok = (size_t)__shfl_sync(0xffffffffu, krow, r);
+          cp_async16(dst + r * kRowPad, cache + (cache_base + tok) * kHeadDim + c16 * 8);
+        }
+      } else {
+        for (int r = 0; r < nt; ++r) {
+          const int v = v0 + r;
+          const size_t tok = ((size_t)sel[v >> lp] << lp) + (v & (p - 1));
+          cp_async16(dst + r * kRowPad, cache + (cache_base + tok) * kHeadDim + c16 * 8);
         }
       }
-      for (int r = 0; r < nt; ++r) {
-        const size_t tok = (size_t)__shfl_sync(0xffffffffu, krow, r);
-        cp_async16(dst + r * kRowPad, cache + (cache_base + tok) * kHeadDim + c16 * 8);
-      }
-    } else {
-      for (int r = 0; r < nt; ++r) {
-        const int v = v0 + r;
-        const size_t tok = ((size_t)sel[v >> lp] << lp) + (v & (p - 1));
-        cp_async16(dst + r * kRowPad, cache + (cache_base + tok) * kHeadDim + c16 * 8);
-      }
+      // V rows past the unit's tokens meet P = 0: make them zero, not stale bits (0 * NaN)
+      for (int i = lane; i < (16 - nt) * 16; i += 32)
+        *reinterpret_cast<uint4*>(Vw + (nt + (i >> 4)) * kRowPad + (i & 15) * 8) =
+            make_uint4(0u, 0u, 0u, 0u);
     }
     cp_async_commit();
-    // V rows past the unit's tokens meet P = 0: make them zero, not stale bits (0 * NaN)
-    for (int i = lane; i < (16 - nt) * 16; i += 32)
-      *reinterpret_cast<uint4*>(Vw + (nt + (i >> 4)) * kRowPad + (i & 15) * 8) =
-          make_uint4(0u, 0u, 0u, 0u);
     cp_async_wait_all();
     __syncwarp();
-    at.step16(Kw, Vw, 0, nt, a.scale_log2);
-    __syncwarp();  // the next unit refills this warp's rows
+    for (int j = 0; j < upw && t0 + 8 * j < nunits; ++j) {
+      const bf16* Kw = warea + (size_t)j * (2 * 16 * kRowPad);
+      at.step16(Kw, Kw + 16 * kRowPad, 0, min(16, ntok_all - (t0 + 8 * j) * 16), a.scale_log2);
+    }
+    __syncwarp();  // the next batch refills this warp's rows
   }
-  __syncthreads();
-
-  CombineSmem<G>* cs = reinterpret_cast<CombineSmem<G>*>(smem);
-  warp_deposit<G>(at, cs);
+  __syncwarp();
+  warp_deposit_own<G>(at, warp_state<G>(stages, warp, wstride));
   __syncthreads();
   // output pair (h, c): merge the 8 warps' partial states, each thread forming head h's factors
   for (int i = tid; i < G * kHeadDim / 2; i += kDecodeThreads) {
     const int h = i >> 6, c = (i & 63) * 2;
+    float mw[8];
     float mm = -1e30f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) mm = fmaxf(mm, cs->m[w][h]);
+    for (int w = 0; w < 8; ++w) {
+      mw[w] = warp_state<G>(stages, w, wstride)[h];
+      mm = fmaxf(mm, mw[w]);
+    }
     float ll = 0.f, o0 = 0.f, o1 = 0.f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-      const float f = fast_exp2(cs->m[w][h] - mm);
-      const float2 x = *reinterpret_cast<const float2*>(&cs->o[w][h][c]);
-      ll = fmaf(cs->l[w][h], f, ll);
+      const float* st = warp_state<G>(stages, w, wstride);
+      const float f = fast_exp2(mw[w] - mm);
+      const float2 x = *reinterpret_cast<const float2*>(st + 2 * G + h * kORow + c);
+      ll = fmaf(st[G + h], f, ll);
       o0 = fmaf(f, x.x, o0);
       o1 = fmaf(f, x.y, o1);
     }
     const float inv = ll > 0.f ? 1.f / ll : 0.f;
     *reinterpret_cast<uint32_t*>(a.out + ((size_t)u * hq + g * G + h) * kHeadDim + c) =
         pack_bf16x2(o0 * inv, o1 * inv);
+  }
+  if constexpr (MODE != 0) {
+    if (appended && tid == 0 && atomicAdd(&a.ap.acount[u], 1) == a.n_kv - 1) {
+      a.ap.acount[u] = 0;
+      const_cast<int32_t*>(a.len)[u] = len0 + 1;
+      if constexpr (MODE == 1) const_cast<int32_t*>(a.full_len)[u] = arow + 1;
+    }
   }
 }
 
@@ -572,13 +763,22 @@ static cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+size_t hybrid_counter_bytes(int n) { return align_up((size_t)(n > 0 ? n : 0) * 4, 256); }
+
 cudaError_t launch_hybrid(const HybridArgsAll& a, cudaStream_t s) {
   const HybridArgs& plain = a;
   const HybridArgsMT& mt = a;
   HybridArgsPaged pg;
   static_cast<HybridArgs&>(pg) = plain;
   pg.pm = a.pm;
-  const size_t smem = hybrid_smem_bytes(a.gqa, a.page_cap, a.budget, a.page);
+  pg.ap = a.ap;
+  HybridArgsApp app;
+  static_cast<HybridArgs&>(app) = plain;
+  app.ap = a.ap;
+  // one CTA per (unit, KV head); the wide layout when they all fit one per SM
+  const size_t wbytes = wide_smem_bytes(a.channels, a.page_cap, a.budget);
+  const bool wide = wbytes != 0 && (long long)a.n * a.n_kv <= device_sm_count();
+  const size_t smem = wide ? wbytes : hybrid_smem_bytes(a.gqa, a.page_cap, a.budget, a.page);
   const dim3 grid(a.n * a.n_kv), block(kDecodeThreads);
   cudaError_t e = cudaSuccess;
   switch (a.gqa) {
@@ -594,6 +794,11 @@ cudaError_t launch_hybrid(const HybridArgsAll& a, cudaStream_t s) {
       e = ensure_dyn_smem((const void*)k, smem);                                             \
       if (e != cudaSuccess) return e;                                                        \
       e = launch_pdl(k, grid, block, smem, s, mt);                                           \
+    } else if (a.ap.new_k) {                                                                 \
+      auto* k = hybrid_decode_kernel<GG, 3, HybridArgsApp>;                                  \
+      e = ensure_dyn_smem((const void*)k, smem);                                             \
+      if (e != cudaSuccess) return e;                                                        \
+      e = launch_pdl(k, grid, block, smem, s, app);                                          \
     } else {                                                                                 \
       auto* k = hybrid_decode_kernel<GG, 0, HybridArgs>;                                     \
       e = ensure_dyn_smem((const void*)k, smem);                                             \
@@ -613,54 +818,6 @@ cudaError_t launch_hybrid(const HybridArgsAll& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// ==========================================================================================
-// Decode-token append: one CTA per unit writes the new row of every KV head and folds it into
-// the page summary it lands in, then bumps len[u]. With a kept list (RocketKV-MT) the row goes to
-// row full_len[u] of the full cache, its position is appended to the kept list, and both
-// counters advance.
-// ==========================================================================================
-__global__ void append_kernel(AppendArgs a) {
-  const int u = blockIdx.x, c = threadIdx.x;  // 128 threads: one channel each
-  pdl_wait();     // the previous decode step may still be reading the cache and the length
-  pdl_trigger();  // the decode after this append may be scheduled now; it waits for our writes
-  const int len = a.len[u];
-  const int row = a.kept ? a.full_len[u] : len;  // cache row receiving the token
-  const int pg = len / a.page;
-  const bool fits = len >= 0 && len < a.vcap && pg < a.page_cap && row >= 0 && row < a.cap;
-  if (fits) {
-    const int blk = a.pm.table ? paged_block(a.pm, u, len, a.status) : 0;
-    for (int g = 0; g < a.n_kv; ++g) {
-      const size_t ukv = (size_t)u * a.n_kv + g;
-      const bf16 kval = a.new_k[ukv * kHeadDim + c];
-      const size_t dst = a.pm.table ? paged_row(a.pm, blk, a.n_kv, g, len) : ukv * a.cap + row;
-      a.k_cache[dst * kHeadDim + c] = kval;
-      a.v_cache[dst * kHeadDim + c] = a.new_v[ukv * kHeadDim + c];
-      if (a.kept && c == 0) a.kept[ukv * a.vcap + len] = row;
-      const size_t si = (ukv * kHeadDim + c) * a.page_cap + pg;
-      if (len % a.page == 0) {
-        a.kmin[si] = kval;
-        a.kmax[si] = kval;
-      } else {
-        const float kf = __bfloat162float(kval);
-        if (kf < __bfloat162float(a.kmin[si])) a.kmin[si] = kval;
-        if (kf > __bfloat162float(a.kmax[si])) a.kmax[si] = kval;
-      }
-    }
-  }
-  __syncthreads();
-  if (c == 0) {
-    if (fits) {
-      a.len[u] = len + 1;
-      if (a.kept) a.full_len[u] = row + 1;
-    } else {
-      set_status(a.status, RKV_DEV_LEN_OVER_CAP);
-    }
-  }
-}
-
-cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
-  return launch_pdl(append_kernel, dim3(a.n), dim3(kHeadDim), 0, s, a);
-}
 
 // ==========================================================================================
 // Page summaries: CTA = (unit, KV head) x 32 pages. Reads rows coalesced (16 threads per

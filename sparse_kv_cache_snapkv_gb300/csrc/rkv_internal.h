@@ -40,12 +40,28 @@ struct HybridArgs {
 };
 static_assert(sizeof(HybridArgs) <= 128, "plain-decode parameters must fit in 128 bytes");
 
+// A decode step that first appends this step's token (new K / V rows [n][n_kv][128]) to every
+// (unit, KV head): acount [n] counts the unit's KV-head CTAs that have read the unit's length;
+// the last one advances it (zero at first use, back to zero after every launch).
+struct AppendFields {
+  const bf16* new_k;
+  const bf16* new_v;
+  int32_t* acount;
+};
+
+// Plain cache, with the append folded in.
+struct HybridArgsApp : HybridArgs {
+  AppendFields ap;
+};
+
 // RocketKV-MT: the sequence is kept[ukv][0 .. len-1], rows of the full cache (k_cache, cap rows,
-// valid below full_len[u]); vcap (the kept list's capacity) bounds len.
+// valid below full_len[u]); vcap (the kept list's capacity) bounds len. An appended token goes to
+// row full_len[u] of the full cache and to the end of the kept list.
 struct HybridArgsMT : HybridArgs {
   const int32_t* kept;
   const int32_t* full_len;
   int vcap;
+  AppendFields ap;  // new_k == nullptr: no append
 };
 
 // Paged K/V cache: k_cache / v_cache are pools [num_blocks][n_kv][block][128]; token t of unit u
@@ -58,28 +74,12 @@ struct PagedMap {
 
 struct HybridArgsPaged : HybridArgs {
   PagedMap pm;
+  AppendFields ap;  // new_k == nullptr: no append
 };
 
 // Launch-side view of every decode variant (only the fields of the chosen one are read).
 struct HybridArgsAll : HybridArgsMT {
   PagedMap pm;
-};
-
-// Appends token `len` of every unit. With `kept` set, the row goes to row full_len[u] of the
-// full cache and kept[ukv][len] = full_len[u]; both counters advance.
-struct AppendArgs {
-  const bf16* new_k;
-  const bf16* new_v;
-  bf16* k_cache;
-  bf16* v_cache;
-  int32_t* len;
-  bf16* kmin;
-  bf16* kmax;
-  int32_t* kept;
-  int32_t* full_len;
-  PagedMap pm;  // table == nullptr: not paged
-  int n, n_kv, cap, vcap, page_cap, page;
-  uint32_t* status;
 };
 
 // Summaries of the sequence of `len` tokens: cache rows, or with `kept` set the rows
@@ -144,8 +144,8 @@ DenseArgs dense_args(const void* q, const void* k, const void* v, const int32_t*
                      int n_kv, int gqa, int max_len, float scale, void* out, void* scratch);
 
 size_t hybrid_smem_bytes(int gqa, int page_cap, int budget, int page);
+size_t hybrid_counter_bytes(int n);  // the append counters after the status word
 cudaError_t launch_hybrid(const HybridArgsAll& a, cudaStream_t s);
-cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_summaries(const SummaryArgs& a, cudaStream_t s);
 cudaError_t launch_dense(const DenseArgs& a, cudaStream_t s);
 
@@ -173,7 +173,10 @@ struct SnapArgs {
   int page, page_cap;
   int pool_avg;     // 1: average pooling over the clipped window instead of max pooling
   int kept_stride;  // entries between units' kept lists (>= keep)
+  int scores_only;  // 1: stop after the score passes (no pooling, selection or gather)
   uint32_t* status;
+  uint64_t wait_limit_ns;  // 0: the default bound of every mbarrier wait (1 s)
+  int test_skip_tile;      // testing only (rkv_testing_scores_wait_timeout)
 };
 
 void snapkv_plan(int n, int n_kv, int gqa, int max_len, int window, int* nsplit,

@@ -131,6 +131,8 @@ struct ScoreParams {
   const float* nlse;  // [units][RP]: merged, negated log2-sum-exp of every row (pass 2)
   float* scores;   // [units][max_len - window]
   uint32_t* status;
+  uint64_t wait_limit_ns;  // bound of every mbarrier wait
+  int test_skip_tile;      // testing only: CTA 0 never loads its first K tile of pass 1
 };
 
 template <int RB>
@@ -197,6 +199,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const int W = p.window;
   const int R = p.gqa * W;
   const int items = p.units * p.nsplit;
+  const uint64_t lim = p.wait_limit_ns;
 
   if (tid == 0) {
     for (int i = 0; i < kKStages; ++i) {
@@ -232,7 +235,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const ItemInfo itm = score_item<PASS>(p, i);
         if (itm.ntiles == 0) continue;
         const int qb = QB == 2 ? (ic & 1) : 0;
-        if (ic >= QB && !mbar_wait(&qempty[qb], (uint32_t)(((ic / QB) - 1) & 1))) {
+        if (ic >= QB && !mbar_wait(&qempty[qb], (uint32_t)(((ic / QB) - 1) & 1), lim)) {
           aborted = true;
           break;
         }
@@ -246,10 +249,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const int krow0 = (itm.ukv / p.kv_div) * p.max_len;
         for (int t = 0; t < itm.ntiles; ++t, ++it) {
           const int s = it % kKStages;
-          if (it >= kKStages && !mbar_wait(&empty[s], (uint32_t)(((it / kKStages) - 1) & 1))) {
+          if (it >= kKStages && !mbar_wait(&empty[s], (uint32_t)(((it / kKStages) - 1) & 1), lim)) {
             aborted = true;
             break;
           }
+          // (testing: the first tile of CTA 0 is never loaded, so every wait on it runs out)
+          if (PASS == 1 && p.test_skip_tile && blockIdx.x == 0 && it == 0) continue;
           uint8_t* dst = ks + (size_t)s * kTileBytes;
           mbar_arrive_expect_tx(&full[s], (uint32_t)kTileBytes);
           const int y = krow0 + (itm.tile0 + t) * kTileTok;
@@ -261,7 +266,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       if (aborted) {
         set_status(p.status, RKV_DEV_WAIT_TIMEOUT);
         for (int j = max(0, it - kKStages); j < it; ++j)  // let issued loads land
-          mbar_wait(&full[j % kKStages], (uint32_t)((j / kKStages) & 1));
+          mbar_wait(&full[j % kKStages], (uint32_t)((j / kKStages) & 1), lim);
       }
     }
   } else if (warp == 1) {
@@ -272,18 +277,18 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const ItemInfo itm = score_item<PASS>(p, i);
         if (itm.ntiles == 0) continue;
         const int qb = QB == 2 ? (ic & 1) : 0;
-        if (!mbar_wait(&qfull[qb], (uint32_t)((ic / QB) & 1))) {
+        if (!mbar_wait(&qfull[qb], (uint32_t)((ic / QB) & 1), lim)) {
           aborted = true;
           break;
         }
         const uint32_t qbase = smem_addr(qs + (size_t)qb * SM::q_bytes);
         for (int t = 0; t < itm.ntiles; ++t, ++it) {
           const int s = it % kKStages, b = it & 1;
-          if (!mbar_wait(&full[s], (uint32_t)((it / kKStages) & 1))) {
+          if (!mbar_wait(&full[s], (uint32_t)((it / kKStages) & 1), lim)) {
             aborted = true;
             break;
           }
-          if (it >= 2 && !mbar_wait(&tempty[b], (uint32_t)(((it >> 1) - 1) & 1))) {
+          if (it >= 2 && !mbar_wait(&tempty[b], (uint32_t)(((it >> 1) - 1) & 1), lim)) {
             aborted = true;
             break;
           }
@@ -346,7 +351,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         for (int t = 0; t < itm.ntiles; ++t, ++it) {
           const int b = it & 1;
           if (aborted) continue;
-          if (!mbar_wait(&tfull[b], (uint32_t)((it >> 1) & 1))) {
+          if (!mbar_wait(&tfull[b], (uint32_t)((it >> 1) & 1), lim)) {
             aborted = true;
             continue;
           }
@@ -416,7 +421,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         // so that a timeout in one warp can never leave the others waiting at the barrier.
         for (int t = 0; t < itm.ntiles; ++t, ++it) {
           const int b = it & 1;
-          if (!aborted && !mbar_wait(&tfull[b], (uint32_t)((it >> 1) & 1))) aborted = true;
+          if (!aborted && !mbar_wait(&tfull[b], (uint32_t)((it >> 1) & 1), lim)) aborted = true;
           float acc = 0.f;
           if (!aborted) {
             tc_fence_after();
@@ -543,6 +548,203 @@ __global__ void __launch_bounds__(1024) select_kernel(SnapArgs a) {
   if (got != want && threadIdx.x == 0) set_status(a.status, RKV_DEV_SELECT_FAILED);
   for (int j = threadIdx.x; j < W; j += blockDim.x) kept[want + j] = L - W + j;
   if (g == 0 && threadIdx.x == 0) a.out_len[u] = a.keep;
+}
+
+// ------------------------------------------------------------------------------------------
+// pooling + top-k selection for long prompts: a cluster of kSelCluster CTAs per (unit, KV head)
+// ------------------------------------------------------------------------------------------
+// CTA c of the cluster owns the positions [c * span, (c + 1) * span) of the unit's n = L - W
+// scores: it loads them with the pooling radius on each side, pools them (max, or the mean of
+// the clipped window in 32.32 fixed point, as the other paths) into ordered keys in shared
+// memory, and takes part in an MSB-first radix select over the whole unit (11, 11, 10 bits):
+// every CTA builds a histogram of its keys, a cluster barrier publishes them, and every CTA
+// reads all kSelCluster histograms through distributed shared memory and finds the same digit.
+// The kept positions (ties -> lower position) are then written in ascending order from the
+// CTAs' (above, equal) counts, exchanged the same way, and a block scan inside each CTA.
+constexpr int kSelCluster = 8;
+constexpr int kSelCThreads = 1024;
+constexpr int kSelCBins = 2048;
+constexpr int kSelCMaxSpan = 20480;   // positions per CTA (beyond: the one-CTA select)
+constexpr int kSelCMaxRadius = 255;   // pooling radius (beyond: the one-CTA select)
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+// 32-bit word at `local` (a shared address of this CTA) in the shared memory of CTA `rank`.
+__device__ __forceinline__ uint32_t ld_peer_u32(const void* local, uint32_t rank) {
+  uint32_t addr, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(addr) : "r"(smem_addr(local)), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+struct SelCSmem {  // after the dynamic key / score arrays
+  uint32_t hist[kSelCBins];
+  unsigned long long tmp[33];
+  uint32_t cnt[2];  // this CTA's (above, equal) counts of the final threshold
+  int found[3];     // digit, keys above it, keys in its bin
+};
+
+size_t select_cluster_smem_bytes(int span, int r) {
+  return align_up((size_t)(span + 2 * r) * 4, 16) + (size_t)span * 4 + sizeof(SelCSmem);
+}
+
+__global__ void __launch_bounds__(kSelCThreads, 1) select_cluster_kernel(SnapArgs a, int span) {
+  extern __shared__ __align__(16) unsigned char smem_sel[];
+  const int ukv = blockIdx.y;
+  const uint32_t cr = cluster_rank();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int u = ukv / a.n_kv, g = ukv - u * a.n_kv;
+  const int W = a.window;
+  const int L = a.seq_lens[u];
+  int32_t* kept = a.kept_idx + (size_t)ukv * a.kept_stride;
+  // every CTA of the cluster sees the same L: the early exits are taken by all or by none
+  if (L <= W || L > a.max_len) {
+    if (cr == 0) {
+      for (int i = tid; i < a.keep; i += blockDim.x) kept[i] = -1;
+      if (g == 0 && tid == 0) a.out_len[u] = 0;
+    }
+    return;
+  }
+  if (L <= a.keep) {
+    if (cr == 0) {
+      for (int i = tid; i < a.keep; i += blockDim.x) kept[i] = i < L ? i : -1;
+      if (g == 0 && tid == 0) a.out_len[u] = L;
+    }
+    return;
+  }
+  const int n = L - W;
+  const int ks = a.kernel_size > 0 ? a.kernel_size : adaptive_kernel(L);
+  const int r = ks / 2;
+  const int beg = min(n, (int)cr * span), end = min(n, beg + span);
+  const int cnt_here = end - beg;
+  const int rpad = (a.kernel_size > 0 ? a.kernel_size : 31) / 2;  // the launch's halo
+  float* buf = reinterpret_cast<float*>(smem_sel);                  // positions beg-rpad ..
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_sel + align_up((size_t)(span + 2 * rpad) * 4, 16));
+  SelCSmem& sm = *reinterpret_cast<SelCSmem*>(reinterpret_cast<unsigned char*>(keys) + (size_t)span * 4);
+  const float* in = a.scores + (size_t)ukv * (a.max_len - W);
+
+  // ---- load this CTA's scores with the pooling halo, then pool into ordered keys ----------
+  for (int j = tid; j < cnt_here + 2 * r; j += blockDim.x) {
+    const int i = beg - r + j;
+    buf[j] = (i >= 0 && i < n) ? in[i] : -INFINITY;
+  }
+  __syncthreads();
+  for (int q = tid; q < cnt_here; q += blockDim.x) {
+    const int i = beg + q;
+    float m;
+    if (a.pool_avg) {
+      const int lo = max(0, i - r), hi = min(n - 1, i + r);
+      long long sum = 0;
+      for (int j = lo; j <= hi; ++j) sum += to_fixed(buf[j - beg + r]);
+      m = fixed_mean(sum, hi - lo + 1);
+    } else {
+      m = buf[q + r];
+      for (int j = 0; j <= 2 * r; ++j) m = fmaxf(m, buf[q + j]);  // -inf outside [0, n)
+    }
+    keys[q] = ordered_key(m);
+  }
+
+  // ---- radix select over the cluster ---------------------------------------------------------
+  const int want = a.keep - W;
+  uint32_t prefix = 0u, mask = 0u;
+  int remaining = want;
+  bool inclusive = false;
+  int start = 32;
+  while (start > 0 && !inclusive) {
+    const int nb = start >= 11 ? 11 : start;
+    const int shift = start - nb;
+    const uint32_t dmask = (1u << nb) - 1u;
+    for (int b = tid; b < kSelCBins; b += blockDim.x) sm.hist[b] = 0u;
+    __syncthreads();
+    // pooled scores share few leading bits, so many keys of a warp fall in one bin: one atomic
+    // per distinct bin and warp (its lanes' count)
+    for (int q0 = 0; q0 < cnt_here; q0 += blockDim.x) {
+      const int q = q0 + tid;
+      const uint32_t k = q < cnt_here ? keys[q] : 0u;
+      const bool in = q < cnt_here && (k & mask) == prefix;
+      const uint32_t act = __ballot_sync(0xffffffffu, in);
+      if (in) {
+        const uint32_t bin = (k >> shift) & dmask;
+        const uint32_t peers = __match_any_sync(act, bin);
+        if (lane == __ffs(peers) - 1) atomicAdd(&sm.hist[bin], (uint32_t)__popc(peers));
+      }
+    }
+    cluster_sync_all();  // every CTA's histogram is complete
+    // thread t: bins 2047 - 2t and 2046 - 2t (descending), summed over the cluster
+    uint32_t c0 = 0u, c1 = 0u;
+    for (uint32_t c = 0; c < (uint32_t)kSelCluster; ++c) {
+      c0 += ld_peer_u32(&sm.hist[kSelCBins - 1 - 2 * tid], c);
+      c1 += ld_peer_u32(&sm.hist[kSelCBins - 2 - 2 * tid], c);
+    }
+    const unsigned long long tot = (unsigned long long)c0 + c1;
+    const unsigned long long before = block_excl_scan64(tot, sm.tmp);
+    if (before < (unsigned long long)remaining && before + tot >= (unsigned long long)remaining) {
+      const bool first = before + c0 >= (unsigned long long)remaining;
+      sm.found[0] = first ? kSelCBins - 1 - 2 * tid : kSelCBins - 2 - 2 * tid;
+      sm.found[1] = (int)(first ? before : before + c0);
+      sm.found[2] = (int)(first ? c0 : c1);
+    }
+    __syncthreads();
+    const uint32_t digit = (uint32_t)sm.found[0];
+    prefix |= (digit & dmask) << shift;
+    mask |= dmask << shift;
+    remaining -= sm.found[1];
+    if (sm.found[2] == remaining) inclusive = true;
+    start = shift;
+    cluster_sync_all();  // no CTA clears its histogram while another still reads it
+  }
+
+  // ---- compaction in position order ----------------------------------------------------------
+  // taken: (key & mask) > prefix, or == prefix: all of them when inclusive, else the first
+  // `remaining` by position over the whole unit
+  const int per = (cnt_here + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int q0 = min(cnt_here, tid * per), q1 = min(cnt_here, q0 + per);
+  uint32_t gt = 0, eq = 0;
+  for (int q = q0; q < q1; ++q) {
+    const uint32_t k = keys[q] & mask;
+    gt += k > prefix ? 1u : 0u;
+    eq += k == prefix ? 1u : 0u;
+  }
+  const unsigned long long mine = ((unsigned long long)gt << 32) | eq;
+  const unsigned long long bef = block_excl_scan64(mine, sm.tmp);
+  if (tid == (int)blockDim.x - 1) {
+    sm.cnt[0] = (uint32_t)((bef + mine) >> 32);
+    sm.cnt[1] = (uint32_t)((bef + mine) & 0xffffffffull);
+  }
+  cluster_sync_all();
+  uint32_t gt_cl = 0, eq_cl = 0;  // earlier CTAs of the cluster
+  for (uint32_t c = 0; c < cr; ++c) {
+    gt_cl += ld_peer_u32(&sm.cnt[0], c);
+    eq_cl += ld_peer_u32(&sm.cnt[1], c);
+  }
+  const int need_eq = inclusive ? 0x7fffffff : remaining;
+  int gt_before = (int)gt_cl + (int)(bef >> 32);
+  int eq_before = (int)eq_cl + (int)(bef & 0xffffffffull);
+  for (int q = q0; q < q1; ++q) {
+    const uint32_t k = keys[q] & mask;
+    bool take = k > prefix;
+    if (k == prefix) {
+      take = eq_before < need_eq;
+      ++eq_before;
+    }
+    if (take) {
+      const int pos = gt_before + min(eq_before - (k == prefix ? 1 : 0), need_eq);
+      if (pos < want) kept[pos] = beg + q;
+    }
+    if (k > prefix) ++gt_before;
+  }
+  if (cr == 0) {
+    for (int j = tid; j < W; j += blockDim.x) kept[want + j] = L - W + j;
+    if (g == 0 && tid == 0) a.out_len[u] = a.keep;
+  }
+  cluster_sync_all();  // peers may still read this CTA's counts
 }
 
 // ------------------------------------------------------------------------------------------
@@ -1131,6 +1333,8 @@ cudaError_t launch_snapkv(const SnapArgs& a, cudaStream_t s) {
   sp.nlse = a.nlse;
   sp.scores = a.scores;
   sp.status = a.status;
+  sp.wait_limit_ns = a.wait_limit_ns ? a.wait_limit_ns : kWaitLimitNs;
+  sp.test_skip_tile = a.test_skip_tile;
   cudaError_t e;
   sp.reverse = 0;
   e = a.rows_pad == 128 ? launch_pass<1, 1>(km, qm, sp, s) : launch_pass<1, 2>(km, qm, sp, s);
@@ -1140,15 +1344,40 @@ cudaError_t launch_snapkv(const SnapArgs& a, cudaStream_t s) {
   sp.reverse = 1;
   e = a.rows_pad == 128 ? launch_pass<2, 1>(km, qm, sp, s) : launch_pass<2, 2>(km, qm, sp, s);
   if (e != cudaSuccess) return e;
+  if (a.scores_only) return cudaSuccess;
   // the whole-unit shared-memory select applies when every unit fits and the pooling kernel is
   // 2^k - 1 (the adaptive sizes 7 / 15 / 31 all are)
   const bool pow2_kernel =
       a.pool_avg || a.kernel_size <= 0 || ((a.kernel_size + 1) & a.kernel_size) == 0;
-  if (a.max_len - a.window <= kSelMaxN && pow2_kernel) {
+  const int nmax = a.max_len - a.window;
+  const int span = ((nmax + kSelCluster - 1) / kSelCluster + 3) & ~3;
+  const int rpad = (a.kernel_size > 0 ? a.kernel_size : 31) / 2;
+  if (nmax <= kSelMaxN && pow2_kernel) {
     const size_t smem = select_fast_smem_bytes();
     e = ensure_dyn_smem((const void*)select_fast_kernel, smem);
     if (e != cudaSuccess) return e;
     select_fast_kernel<<<units, kSelThreads, smem, s>>>(a);
+  } else if (span <= kSelCMaxSpan && rpad <= kSelCMaxRadius &&
+             (long long)units * kSelCluster * 2 <= device_sm_count()) {
+    // long prompts and few units (one CTA per unit would leave most SMs idle): a cluster of
+    // CTAs per (unit, KV head). With more units the one-CTA select measured faster.
+    const size_t smem = select_cluster_smem_bytes(span, rpad);
+    e = ensure_dyn_smem((const void*)select_cluster_kernel, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kSelCluster, units);
+    cfg.blockDim = dim3(kSelCThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kSelCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, select_cluster_kernel, a, span);
+    if (e != cudaSuccess) return e;
   } else {
     select_kernel<<<units, 1024, 0, s>>>(a);
   }

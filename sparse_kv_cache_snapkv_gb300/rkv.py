@@ -33,6 +33,7 @@ SYMBOLS = [
     "rkv_snapkv_per_head_workspace_bytes", "rkv_snapkv_compress_per_head",
     "rkv_snapkv_compress_paged", "rkv_build_page_summaries_paged", "rkv_hybrid_decode_paged",
     "rkv_snapkv_compress_summarized", "rkv_snapkv_compress_avg_pool", "rkv_snapkv_select",
+    "rkv_snapkv_scores", "rkv_testing_scores_wait_timeout",
 ]
 
 
@@ -72,6 +73,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
                                  vp, vp, i32, vp, vp, vp, vp, sz, vp], i32),
         "rkv_snapkv_compress_avg_pool": ([vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                           i32, f32, vp, vp, i32, vp, vp, vp, vp, sz, vp], i32),
+        "rkv_testing_scores_wait_timeout": ([vp, vp, vp, i32, i32, i32, i32, i32, i32, f32,
+                                             vp, ctypes.c_uint64, vp, sz, vp], i32),
+        "rkv_snapkv_scores": ([vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, vp, sz, vp],
+                              i32),
         "rkv_snapkv_select": ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, vp, i32,
                                vp, vp, vp, sz, vp], i32),
         "rkv_summaries_workspace_bytes": ([], sz),
@@ -247,6 +252,39 @@ def rkv_snapkv_select(k, seq_lens, q_win, kernel_size: int, keep: int, scale: fl
         keep, float(scale), _ptr(kept_idx), kept_idx.shape[2], _ptr(out_len), _ptr(scores_out),
         _ptr(ws), ws.numel(), _stream(stream))
     _check("rkv_snapkv_select", code)
+    return ws
+
+
+def rkv_snapkv_scores(k, seq_lens, q_win, scale: float, scores_out, ws=None, stream=None):
+    """Stage-1 window scores only (no pooling, selection or gather) into
+    scores_out [n][n_kv][max_len - window] fp32; see include/rkv.h."""
+    _bf16(k, "k"), _bf16(q_win, "q_win"), _i32(seq_lens, "seq_lens")
+    n, n_kv, max_len, d = k.shape
+    hq, window = q_win.shape[1], q_win.shape[2]
+    gqa = _group(hq, n_kv)
+    if ws is None:
+        ws = workspace(rkv_snapkv_workspace_bytes(n, n_kv, gqa, max_len, window), k.device)
+    code = load().rkv_snapkv_scores(
+        _ptr(k), _ptr(seq_lens), _ptr(q_win), n, n_kv, gqa, d, max_len, window, float(scale),
+        _ptr(scores_out), _ptr(ws), ws.numel(), _stream(stream))
+    _check("rkv_snapkv_scores", code)
+    return ws
+
+
+def rkv_testing_scores_wait_timeout(k, seq_lens, q_win, scale: float, scores_out,
+                                    wait_limit_ns: int, ws=None, stream=None):
+    """Test hook (include/rkv_testing.h): the score passes with one K tile of block 0 never
+    loaded, so that its bounded waits run out after wait_limit_ns."""
+    _bf16(k, "k"), _bf16(q_win, "q_win"), _i32(seq_lens, "seq_lens")
+    n, n_kv, max_len, d = k.shape
+    hq, window = q_win.shape[1], q_win.shape[2]
+    gqa = _group(hq, n_kv)
+    if ws is None:
+        ws = workspace(rkv_snapkv_workspace_bytes(n, n_kv, gqa, max_len, window), k.device)
+    code = load().rkv_testing_scores_wait_timeout(
+        _ptr(k), _ptr(seq_lens), _ptr(q_win), n, n_kv, gqa, d, max_len, window, float(scale),
+        _ptr(scores_out), int(wait_limit_ns), _ptr(ws), ws.numel(), _stream(stream))
+    _check("rkv_testing_scores_wait_timeout", code)
     return ws
 
 

@@ -1,5 +1,5 @@
 """Host-side checks of the C ABI: the library builds, loads and exports every symbol that
-include/rkv.h declares; the planner matches the oracle; invalid arguments are rejected on the host
+include/*.h declares; the planner matches the oracle; invalid arguments are rejected on the host
 before any launch. No GPU needed."""
 import ctypes
 import os
@@ -20,9 +20,13 @@ def lib():
 
 
 def _declared():
-    src = open(os.path.join(ROOT, "include", "rkv.h")).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(rkv_[a-z0-9_]+)\s*\(", src)))
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for hdr in sorted(os.listdir(inc)):
+        if hdr.endswith(".h"):
+            src = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, hdr)).read(), flags=re.S)
+            names |= set(re.findall(r"\b(rkv_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
 
 
 def test_exports_every_declared_symbol(lib):
@@ -158,6 +162,33 @@ def test_select_only_validation(lib):
     assert lib.rkv_snapkv_select(vp, vp, vp, 1, 2, 4, 64, 4096, 32, 7, 256, 0.1, vp, 256, vp,
                                  None, vp, big, None) == 2                              # head_dim
     assert lib.rkv_snapkv_select(*head, 256, 0.1, vp, 256, vp, None, vp, 64, None) == 3  # ws
+
+
+def test_scores_only_validation(lib):
+    vp = FAKE
+    big = 1 << 30
+    # (k, seq_lens, q_win, n, n_kv, gqa, head_dim, max_len, window, scale, scores_out, ws, ...)
+    assert lib.rkv_snapkv_scores(vp, vp, vp, 1, 2, 4, 128, 4096, 32, 0.1, None, vp, big,
+                                 None) == 1                                   # scores required
+    assert lib.rkv_snapkv_scores(vp, vp, vp, 1, 2, 4, 128, 32, 32, 0.1, vp, vp, big,
+                                 None) == 1                                   # max_len <= window
+    assert lib.rkv_snapkv_scores(vp, vp, vp, 1, 2, 4, 128, 4096, 32, 0.0, vp, vp, big,
+                                 None) == 1                                   # scale
+    assert lib.rkv_snapkv_scores(vp, vp, vp, 1, 2, 4, 64, 4096, 32, 0.1, vp, vp, big,
+                                 None) == 2                                   # head_dim
+    assert lib.rkv_snapkv_scores(vp, vp, vp, 1, 2, 16, 128, 4096, 32, 0.1, vp, vp, big,
+                                 None) == 2                                   # G * W > 256
+    assert lib.rkv_snapkv_scores(vp, vp, vp, 1, 2, 4, 128, 4096, 32, 0.1, vp, vp, 64,
+                                 None) == 3                                   # workspace
+
+
+def test_wait_timeout_hook_validation(lib):
+    vp = FAKE
+    big = 1 << 30
+    args = (vp, vp, vp, 1, 2, 4, 128, 4096, 32, 0.1, vp)
+    assert lib.rkv_testing_scores_wait_timeout(*args, 10, vp, big, None) == 1        # too short
+    assert lib.rkv_testing_scores_wait_timeout(*args, 2 * 10**9, vp, big, None) == 1  # too long
+    assert lib.rkv_testing_scores_wait_timeout(*args, 10**6, vp, 64, None) == 3       # ws
 
 
 def test_mt_validation_rejects_before_launch(lib):

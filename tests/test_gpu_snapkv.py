@@ -281,3 +281,25 @@ def test_snapkv_outlier_channels_128k_sample():
     res = _run(rkv, x, 32, 31, 16384)
     for g in range(2):
         _check_unit(x, 0, g, 4, 32, 31, 16384, *res, tag=f"g{g}")
+
+
+def test_snapkv_scores_only_matches_oracle():
+    # the score passes alone: ragged lengths (one not tile-aligned), G * W = 128 and 256; the
+    # entries past a unit's L - W stay untouched
+    rkv = _lib()
+    for window, lens in ((32, [3001, 700]), (64, [5000, 1999])):
+        wl, x = _inputs(2, 2, 4, lens, window, seed=150 + window, needles=2)
+        n, n_kv, max_len, _ = x["k"].shape
+        scores = torch.full((n, n_kv, max_len - window), -3.0, dtype=torch.float32,
+                            device="cuda")
+        ws = rkv.rkv_snapkv_scores(x["k"], x["seq_lens"], x["q_win"], 1.0 / math.sqrt(D), scores)
+        rkv.rkv_check_status(ws)
+        for u, L in enumerate(lens):
+            for g in range(n_kv):
+                k = _f64(x["k"][u, g, :L])
+                q = _f64(x["q_win"][u, g * 4:(g + 1) * 4])
+                ref = O.window_scores(k, q, 1.0 / math.sqrt(D))
+                gs = scores[u, g, :L - window].cpu().numpy().astype(np.float64)
+                err = np.abs(gs - ref)
+                assert (err <= SCORE_REL * np.abs(ref) + 1e-30).all(), f"W {window} unit {u}"
+                assert (scores[u, g, L - window:] == -3.0).all(), f"W {window} unit {u} tail"
