@@ -18,6 +18,7 @@ exchange step); rank 0 prints the JSON line with the max time over ranks.
 from __future__ import annotations
 
 import argparse
+import atexit
 import json
 import math
 import multiprocessing as mp
@@ -52,6 +53,9 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=2000)
     ap.add_argument("--layers", type=int, default=0,
                     help="run the workload with this many layers (smaller profiling cases)")
+    ap.add_argument("--decode-sets", type=int, default=0,
+                    help="copies of the compact cache the decode steps rotate through (0: as "
+                         "many as keep each step's rows out of L2, see decode_sets; 1: none)")
     ap.add_argument("--ctx", type=int, default=0,
                     help="prompt length of every sequence (e.g. 131072: the 128K end of the "
                          "metric at the default workload's budget)")
@@ -93,17 +97,25 @@ class ClockSampler:
         self.proc = None
         self.path = None
 
+    MAX_S = 900  # the sampler ends by itself after this long, whatever happens to this process
+
     def start(self):
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                ["timeout", str(self.MAX_S), "nvidia-smi", f"--id={self.gpu}",
+                 f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
+            # a bench that fails inside the timed region must not leave the sampler running
+            atexit.register(self._kill)
         except Exception:
             self.proc = None
+
+    def _kill(self):
+        if self.proc is not None and self.proc.poll() is None:
+            self.proc.kill()
 
     def stop(self):
         if self.proc is None:
@@ -246,8 +258,10 @@ def workload_config(wl, keep):
             "channels": wl.channels, "keep": keep, "decode_steps_per_step": wl.decode_steps,
             "append": wl.append, "needles": wl.needles,
             "l2": "inputs larger than L2: prompt K/V %.2f GB per step, compact cache + summaries "
-                  "%.2f GB" % (2 * wl.n * wl.n_kv * wl.max_len * 256 / 1e9,
-                               (wl.n * wl.n_kv * (keep or 0) * 512 * 1.25) / 1e9),
+                  "%.2f GB; without appends the decode steps rotate through copies of the "
+                  "compact cache so that each step reads from HBM (see decode_sets)"
+                  % (2 * wl.n * wl.n_kv * wl.max_len * 256 / 1e9,
+                     (wl.n * wl.n_kv * (keep or 0) * 512 * 1.25) / 1e9),
             "parallelism": "replicas"}
 
 
@@ -284,6 +298,13 @@ def run_ours(args):
     hp.step()
     torch.cuda.synchronize()
     hp.check_status()
+    # Cold-L2 decode: every layer is batched into one launch, so consecutive steps would find
+    # the rows they re-read in L2; rotating copies of the compact cache (enough that one step's
+    # rows are evicted before they come round again) makes each step read from HBM, as it would
+    # in a model, where the other layers' work runs between two steps of a layer.
+    sets = args.decode_sets or decode_sets(wl, hp)
+    if sets > 1 and not wl.append:
+        hp.rotate_decode_sets(sets)
 
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
@@ -372,6 +393,7 @@ def run_ours(args):
         "decode_hbm_gbs": round(dec_gbs, 1), "decode_frac_of_peak": round(dec_gbs / hbm_peak, 4),
         "compress_gbs": round(comp_gbs, 1), "compress_tflops": round(comp_tflops, 2),
         "compress_frac_of_peak_hbm": round(comp_gbs / hbm_peak, 4),
+        "decode_cache_sets": len(getattr(hp, "sets", [None])),
     }
 
     # dense decode over the full prompt (the full-KV baseline), one launch over all units
@@ -412,6 +434,15 @@ def run_ours(args):
                 "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
                 "breakdown": breakdown, "impl": "ours"}
         print(json.dumps(line), flush=True)
+
+
+def decode_sets(wl, hp, l2_bytes=L2_BYTES):
+    """Copies of the compact cache the decode steps rotate through: enough that 4 x L2 of other
+    decode traffic passes between two reads of a copy, at most 8; 1 with appends."""
+    if wl.append:
+        return 1
+    per_step = hp.decode_bytes_per_launch()
+    return int(max(1, min(8, math.ceil(4 * l2_bytes / max(per_step, 1)))))
 
 
 def _oracle_worker_init_env():
@@ -496,6 +527,10 @@ def _e2e(hp, host_in, wl, stream, world, steps):
         hp.step()
         host_out.copy_(hp.out, non_blocking=True)
 
+    # every pass decodes from the cache its own compression wrote (no rotated copies here: the
+    # host copies dominate this leg anyway)
+    sets, hp.sets = getattr(hp, "sets", None), None
+
     with torch.cuda.stream(stream):
         # untimed warm-up passes: the first transfers from freshly pinned memory run slower
         for _ in range(E2E_WARMUP):
@@ -509,6 +544,7 @@ def _e2e(hp, host_in, wl, stream, world, steps):
         b.record(stream)
         torch.cuda.synchronize()
     hp.check_status()
+    hp.sets = sets
     ms = a.elapsed_time(b)
     ms = max_over_ranks(ms, world)
     return {"value": round(steps * wl.decode_steps * world / (ms / 1e3), 2), "unit": UNIT,

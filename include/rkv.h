@@ -366,12 +366,13 @@ rkv_status rkv_dense_decode(const void* q, const void* k, const void* v, const i
  * (every GPU that loads the library holds it until the process exits).
  *
  * It exists for callers that cannot call cudaMalloc to build a workspace: code that is only
- * handed its input and output tensors (a plugin boundary, say), a host whose device memory
- * belongs entirely to its own pool, or a region being recorded into a CUDA graph. The caller
- * still passes inputs and outputs; nothing is allocated or freed by this call.
+ * handed its input and output tensors (a plugin boundary, say), or a host whose device memory
+ * belongs entirely to its own pool. The caller still passes inputs and outputs; nothing is
+ * allocated or freed by this call.
  *
  *  - Limit: 256 B + the partials of rkv_dense_decode_workspace_bytes(n, n_kv, gqa, max_len) must
- *    fit in 8 MiB; otherwise RKV_ERR_TOO_LARGE is returned and nothing is launched.
+ *    fit in 8 MiB; otherwise RKV_ERR_TOO_LARGE is returned and nothing is launched (the sizes
+ *    are checked before the pointers).
  *  - Set-up: the first call on each device looks up the device address of the array (with that
  *    device current). Make that first call before any stream capture.
  *  - All calls share the one array, which keeps the last call's contents. Each call clears the

@@ -3,8 +3,8 @@
 //
 // Who needs it: code that may only hand over the tensors it already owns and must not allocate
 // device memory while it runs -- for example a plugin boundary that passes just input and output
-// pointers, a host that has handed all device memory to its own pool, or a region that is being
-// recorded into a CUDA graph. Such a caller cannot call cudaMalloc to build a workspace.
+// pointers, or a host that has handed all device memory to its own pool. Such a caller cannot
+// call cudaMalloc to build a workspace.
 //
 // Cost: every GPU that loads the library keeps kNoAllocScratchBytes of device memory for this
 // array until the process exits.

@@ -1358,9 +1358,11 @@ cudaError_t launch_snapkv(const SnapArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     select_fast_kernel<<<units, kSelThreads, smem, s>>>(a);
   } else if (span <= kSelCMaxSpan && rpad <= kSelCMaxRadius &&
-             (long long)units * kSelCluster * 2 <= device_sm_count()) {
+             (long long)units * kSelCluster <= 4LL * device_sm_count()) {
     // long prompts and few units (one CTA per unit would leave most SMs idle): a cluster of
-    // CTAs per (unit, KV head). With more units the one-CTA select measured faster.
+    // CTAs per (unit, KV head). Measured at 128K prompts: 8 units 55 against 307 us, 64 units
+    // 272 against 311 us; with 128 units (ragged serving batch) the one-CTA select is faster
+    // (164 against 340 us).
     const size_t smem = select_cluster_smem_bytes(span, rpad);
     e = ensure_dyn_smem((const void*)select_cluster_kernel, smem);
     if (e != cudaSuccess) return e;

@@ -72,12 +72,27 @@ class HotPath:
             rkv.rkv_build_page_summaries(self.k_out, self.length, self.page, self.kmin,
                                          self.kmax, ws=self.ws_sum)
 
+    def rotate_decode_sets(self, sets: int):
+        """Give the decode `sets` copies of the compact cache and its summaries; step t reads copy
+        t % sets. All copies hold what the compression wrote (call after a compression; the
+        compression rewrites copy 0 with the same values). With every layer batched into one
+        launch, consecutive steps would otherwise re-read one small set of rows that stays in L2;
+        in a model the other layers' work runs in between, so each step reads its rows from HBM.
+        Only for workloads without appends (an appended token would reach one copy only)."""
+        assert not self.wl.append, "decode sets are for workloads without appends"
+        self.sets = [(self.k_out, self.v_out, self.kmin, self.kmax)]
+        for _ in range(1, sets):
+            self.sets.append(tuple(t.clone() for t in self.sets[0]))
+
     def decode(self, t: int):
         nk = self.new_k[t] if self.new_k is not None else None
         nv = self.new_v[t] if self.new_v is not None else None
-        rkv.rkv_hybrid_decode(self.dec_q[t], self.k_out, self.v_out, self.length, self.kmin,
-                              self.kmax, self.wl.budget, self.page, self.channels, self.scale,
-                              self.out[t], new_k=nk, new_v=nv, ws=self.ws_dec)
+        sets = getattr(self, "sets", None)
+        k, v, kmin, kmax = (sets[t % len(sets)] if sets else
+                            (self.k_out, self.v_out, self.kmin, self.kmax))
+        rkv.rkv_hybrid_decode(self.dec_q[t], k, v, self.length, kmin, kmax, self.wl.budget,
+                              self.page, self.channels, self.scale, self.out[t], new_k=nk,
+                              new_v=nv, ws=self.ws_dec)
 
     def step(self):
         self.compress()

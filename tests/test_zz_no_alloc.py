@@ -1,7 +1,7 @@
 """The allocation-free dense decode (rkv_dense_decode_noalloc) against the workspace version.
 
-Callers such as a plugin that is handed only its input and output tensors, or code recording a
-CUDA graph, cannot call cudaMalloc for a workspace; this entry point keeps its scratch in a
+Callers such as a plugin that is handed only its input and output tensors, or a host whose device
+memory all belongs to its own pool, cannot call cudaMalloc for a workspace; this entry point keeps its scratch in a
 fixed device array inside the library instead. The test calls it twice in a row through the C
 ABI (different queries each time, so nothing may leak from the first call into the second) and
 checks each output against rkv_dense_decode's bit for bit: both run the same kernels with the
