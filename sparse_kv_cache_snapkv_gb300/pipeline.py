@@ -108,10 +108,9 @@ class HotPath:
     def launches_per_step(self) -> int:
         """Kernel launches of one step: compression = score pass 1, LSE merge, score pass 2,
         select, gather (which also builds the page summaries unless fuse_summaries is off: then
-        one summaries launch more); then one decode launch per step (two with appends: the
-        append kernel and the decode)."""
-        per_decode = 2 if self.wl.append else 1
-        return 5 + (0 if self.fuse_summaries else 1) + per_decode * self.dec_q.shape[0]
+        one summaries launch more); then one decode launch per step (an append is done inside
+        the decode launch)."""
+        return 5 + (0 if self.fuse_summaries else 1) + self.dec_q.shape[0]
 
     def decode_bytes_per_launch(self) -> int:
         """Algorithmic HBM bytes of one hybrid decode launch (all units), budget-implied:
