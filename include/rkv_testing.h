@@ -32,6 +32,18 @@ rkv_status rkv_testing_scores_wait_timeout(const void* k, const int32_t* seq_len
                                            float* scores_out, uint64_t wait_limit_ns, void* ws,
                                            size_t ws_bytes, void* stream);
 
+/* Shared-memory layout of every later rkv_hybrid_decode call in this process, so that a test
+ * can run each on the same inputs (the results do not depend on it; one CTA per (unit, KV head)
+ * either way):
+ *   0  automatic (the default): the wide layout -- every kept channel's summary row staged at
+ *      once, every selected token's K / V rows staged per warp at once -- when there are no more
+ *      (unit, KV head) pairs than SMs and it fits in shared memory, else the ordinary one;
+ *   1  always the ordinary layout;
+ *   2  the wide layout wherever it fits, whatever the number of units.
+ * Returns RKV_ERR_INVALID_ARG (and changes nothing) for any other value. Not synchronised with
+ * decode calls running on other host threads. */
+rkv_status rkv_testing_decode_layout(int layout);
+
 #ifdef __cplusplus
 }
 #endif

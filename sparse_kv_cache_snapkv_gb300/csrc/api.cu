@@ -309,6 +309,10 @@ rkv_status rkv_testing_scores_wait_timeout(const void* k, const int32_t* seq_len
                      wait_limit_ns, 1);
 }
 
+rkv_status rkv_testing_decode_layout(int layout) {
+  return rkv::set_decode_layout(layout) == 0 ? RKV_OK : RKV_ERR_INVALID_ARG;
+}
+
 rkv_status rkv_snapkv_compress_summarized(const void* k, const void* v,
                                           const int32_t* seq_lens, const void* q_win, int n,
                                           int n_kv, int gqa, int head_dim, int max_len,

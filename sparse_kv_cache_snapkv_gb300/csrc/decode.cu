@@ -20,6 +20,7 @@
 // heads of a KV group are the rows of the A operand (padded to 16 with zeros); each warp takes 16
 // tokens at a time: S = Q K^T (16 MMAs), an online softmax on the accumulator fragments, and
 // O += P V (16 MMAs) with P re-packed from the accumulators as the next A operand.
+#include <atomic>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -277,13 +278,18 @@ __device__ __forceinline__ void group_sync(int group) {
 // ==========================================================================================
 // Hybrid sparse decode: one CTA of 8 warps per (unit, KV head).
 // ==========================================================================================
+// The selected pages: the S = B / 2 / p of a sparse step, or every page of a dense one (a
+// sequence of at most B tokens), never more than page_cap.
+inline int sel_entries(int page_cap, int budget, int page) {
+  const int dense_pages = (budget + page - 1) / page;
+  return page_cap < dense_pages ? page_cap : dense_pages;
+}
+
 size_t hybrid_smem_bytes(int gqa, int page_cap, int budget, int page) {
   (void)gqa;
-  (void)budget;
-  (void)page;
-  size_t b = (size_t)kDecStages * kStageBytes;  // K/V stages (also the warp combine)
-  b += align_up((size_t)page_cap * 4, 16);       // approximate scores
-  b += align_up((size_t)page_cap * 4, 16);       // selected pages
+  size_t b = (size_t)kDecStages * kStageBytes;                       // K/V stages, warp states
+  b += align_up((size_t)page_cap * 4, 16);                            // approximate scores
+  b += align_up((size_t)sel_entries(page_cap, budget, page) * 4, 16);  // selected pages
   return b;
 }
 
@@ -763,6 +769,14 @@ static cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Layout policy of the hybrid decode (rkv_testing_decode_layout); 0: automatic.
+static std::atomic<int> g_decode_layout{0};
+int set_decode_layout(int layout) {
+  if (layout < 0 || layout > 2) return -1;
+  g_decode_layout.store(layout);
+  return 0;
+}
+
 size_t hybrid_counter_bytes(int n) { return align_up((size_t)(n > 0 ? n : 0) * 4, 256); }
 
 cudaError_t launch_hybrid(const HybridArgsAll& a, cudaStream_t s) {
@@ -775,9 +789,12 @@ cudaError_t launch_hybrid(const HybridArgsAll& a, cudaStream_t s) {
   HybridArgsApp app;
   static_cast<HybridArgs&>(app) = plain;
   app.ap = a.ap;
-  // one CTA per (unit, KV head); the wide layout when they all fit one per SM
+  // one CTA per (unit, KV head); the wide layout when they all fit one per SM (or as the test
+  // hook asks: 1 never, 2 wherever it fits)
+  const int layout = g_decode_layout.load();
   const size_t wbytes = wide_smem_bytes(a.channels, a.page_cap, a.budget);
-  const bool wide = wbytes != 0 && (long long)a.n * a.n_kv <= device_sm_count();
+  const bool wide = wbytes != 0 && layout != 1 &&
+                    (layout == 2 || (long long)a.n * a.n_kv <= device_sm_count());
   const size_t smem = wide ? wbytes : hybrid_smem_bytes(a.gqa, a.page_cap, a.budget, a.page);
   const dim3 grid(a.n * a.n_kv), block(kDecodeThreads);
   cudaError_t e = cudaSuccess;

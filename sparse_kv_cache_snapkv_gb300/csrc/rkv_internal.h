@@ -144,6 +144,10 @@ DenseArgs dense_args(const void* q, const void* k, const void* v, const int32_t*
                      int n_kv, int gqa, int max_len, float scale, void* out, void* scratch);
 
 size_t hybrid_smem_bytes(int gqa, int page_cap, int budget, int page);
+// Shared-memory layout of later hybrid decode launches in this process
+// (rkv_testing_decode_layout): 0 automatic, 1 always the ordinary layout, 2 the wide layout
+// wherever it fits. Returns -1 for any other value.
+int set_decode_layout(int layout);
 size_t hybrid_counter_bytes(int n);  // the append counters after the status word
 cudaError_t launch_hybrid(const HybridArgsAll& a, cudaStream_t s);
 cudaError_t launch_summaries(const SummaryArgs& a, cudaStream_t s);

@@ -33,7 +33,7 @@ SYMBOLS = [
     "rkv_snapkv_per_head_workspace_bytes", "rkv_snapkv_compress_per_head",
     "rkv_snapkv_compress_paged", "rkv_build_page_summaries_paged", "rkv_hybrid_decode_paged",
     "rkv_snapkv_compress_summarized", "rkv_snapkv_compress_avg_pool", "rkv_snapkv_select",
-    "rkv_snapkv_scores", "rkv_testing_scores_wait_timeout",
+    "rkv_snapkv_scores", "rkv_testing_scores_wait_timeout", "rkv_testing_decode_layout",
 ]
 
 
@@ -77,6 +77,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
                                              vp, ctypes.c_uint64, vp, sz, vp], i32),
         "rkv_snapkv_scores": ([vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, vp, sz, vp],
                               i32),
+        "rkv_testing_decode_layout": ([i32], i32),
         "rkv_snapkv_select": ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, vp, i32,
                                vp, vp, vp, sz, vp], i32),
         "rkv_summaries_workspace_bytes": ([], sz),
@@ -286,6 +287,12 @@ def rkv_testing_scores_wait_timeout(k, seq_lens, q_win, scale: float, scores_out
         _ptr(scores_out), int(wait_limit_ns), _ptr(ws), ws.numel(), _stream(stream))
     _check("rkv_testing_scores_wait_timeout", code)
     return ws
+
+
+def rkv_testing_decode_layout(layout: int) -> None:
+    """Test hook (include/rkv_testing.h): the hybrid decode's shared-memory layout for later
+    calls in this process (0 automatic, 1 ordinary, 2 wide wherever it fits)."""
+    _check("rkv_testing_decode_layout", load().rkv_testing_decode_layout(int(layout)))
 
 
 def rkv_snapkv_per_head_workspace_bytes(n: int, n_kv: int, gqa: int, max_len: int,

@@ -191,6 +191,14 @@ def test_wait_timeout_hook_validation(lib):
     assert lib.rkv_testing_scores_wait_timeout(*args, 10**6, vp, 64, None) == 3       # ws
 
 
+def test_decode_layout_hook(lib):
+    # include/rkv_testing.h: 0..2 accepted, anything else rejected; back to automatic after
+    for bad in (-1, 3, 1 << 20):
+        assert lib.rkv_testing_decode_layout(bad) == 1  # RKV_ERR_INVALID_ARG
+    for ok in (1, 2, 0):
+        assert lib.rkv_testing_decode_layout(ok) == 0
+
+
 def test_mt_validation_rejects_before_launch(lib):
     vp = FAKE
     # (q, new_k, new_v, k_full, v_full, full_len, kept_idx, kept_len, kmin, kmax)
