@@ -45,8 +45,8 @@ def test_dense_decode_noalloc_rejects_oversize():
     from sparse_kv_cache_snapkv_gb300 import rkv
     lib = rkv.load()
     # 512 units x 64 query heads: the split partials alone need 16 MiB, beyond the fixed 8 MiB.
-    # The size is checked before the pointers, so null pointers still get the size verdict (and
-    # nothing could be launched on them if the order of the checks ever changed).
+    # The size is checked before the pointers, so null pointers still get the size check's
+    # answer (and nothing could be launched on them if the order of the checks ever changed).
     assert lib.rkv_dense_decode_workspace_bytes(512, 8, 8, 1024) > (8 << 20)
     code = lib.rkv_dense_decode_noalloc(None, None, None, None, 512, 8, 8, 128, 1024, 0.1,
                                         None, None)
