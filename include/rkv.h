@@ -247,6 +247,9 @@ size_t rkv_hybrid_decode_workspace_bytes(int n, int n_kv, int gqa, int page_cap,
  *   sel_channels NULL or [n][n_kv][channels] int32 (ascending; -1 on the dense path)
  *   sel_pages NULL or [n][n_kv][(budget/2)/page] int32 (ascending; -1 where unused)
  *   approx_scores NULL or [n][n_kv][page_cap] fp32 (pages >= ceil(len_u/page) untouched)
+ * A decode CTA keeps one fp32 score per page of page_cap in shared memory: page_cap may be up to
+ * 31,168 (fewer when budget/page is large: 27,136 at budget/page = 4096); beyond that the call
+ * returns RKV_ERR_UNSUPPORTED. The same limit holds for the RocketKV-MT and paged variants.
  */
 rkv_status rkv_hybrid_decode(const void* q, const void* new_k, const void* new_v,
                              void* k_cache, void* v_cache, int32_t* len, void* kmin, void* kmax,

@@ -431,7 +431,7 @@ static rkv_status hybrid_impl(const void* q, const void* new_k, const void* new_
       channels < 1 || channels > kHeadDim || !(scale > 0.f) || !std::isfinite(scale))
     return RKV_ERR_INVALID_ARG;
   const size_t smem = hybrid_smem_bytes(gqa, page_cap, budget, page);
-  if (smem > 200 * 1024) return RKV_ERR_UNSUPPORTED;
+  if (smem > kDecodeSmemMax) return RKV_ERR_UNSUPPORTED;
   if (!ws || !aligned16(ws) ||
       ws_bytes < rkv_hybrid_decode_workspace_bytes(n, n_kv, gqa, page_cap, budget, page))
     return RKV_ERR_WORKSPACE;

@@ -143,7 +143,10 @@ int dense_check_pointers(const void* q, const void* k, const void* v, const int3
 DenseArgs dense_args(const void* q, const void* k, const void* v, const int32_t* len, int n,
                      int n_kv, int gqa, int max_len, float scale, void* out, void* scratch);
 
+// Dynamic shared memory of a decode CTA (ordinary layout), and its ceiling: the 227 KB a CTA
+// may have less the kernel's static shared memory (about 29 KB), with a margin.
 size_t hybrid_smem_bytes(int gqa, int page_cap, int budget, int page);
+constexpr size_t kDecodeSmemMax = 190 * 1024;
 // Shared-memory layout of later hybrid decode launches in this process
 // (rkv_testing_decode_layout): 0 automatic, 1 always the ordinary layout, 2 the wide layout
 // wherever it fits. Returns -1 for any other value.

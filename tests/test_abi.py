@@ -81,6 +81,12 @@ def test_validation_rejects_before_launch(lib):
                                  4, 32, 0.1, vp, None, None, None, vp, 256, None) == 1
     assert lib.rkv_hybrid_decode(*common, 1, 1, 4, 128, 64, 16, 256, 4, 32, 0.1, vp, None, None,
                                  None, vp, 8, None) == 3
+    # page_cap past the decode CTA's shared memory (190 KB: 31,168 pages at budget / page = 64)
+    # is unsupported; at the limit the call gets as far as the workspace check (no workspace given)
+    assert lib.rkv_hybrid_decode(*common, 1, 1, 4, 128, 64, 31176, 256, 4, 32, 0.1, vp, None,
+                                 None, None, vp, 0, None) == 2
+    assert lib.rkv_hybrid_decode(*common, 1, 1, 4, 128, 64, 31168, 256, 4, 32, 0.1, vp, None,
+                                 None, None, vp, 0, None) == 3
     assert lib.rkv_hybrid_decode(vp, vp, None, vp, vp, vp, vp, vp, 1, 1, 4, 128, 64, 16, 256, 4,
                                  32, 0.1, vp, None, None, None, vp, 256, None) == 1  # new_v missing
     misaligned = ctypes.c_void_p((1 << 20) + 8)
