@@ -53,6 +53,6 @@ def test_layout_append_steps(layout):
 
 
 def test_layout_more_units_than_sms(layout):
-    # 160 (unit, KV head) pairs on a 152-SM part: more than one wave, in either layout
+    # 160 (unit, KV head) pairs, more than the SMs: the wide layout runs here only when forced
     T._hybrid_case(80, 2, 4, [600 + 7 * i for i in range(80)], 1200, 256, 4, 32, seed=73,
                    steps=1)
