@@ -42,8 +42,8 @@ def run():
         gp = sel[0, g].cpu().numpy()
         parity.check_selection(gp, ref["scores"], len(ref["pages"]), "smoke pages")
         toks = np.concatenate([np.arange(p * page, min(L, (p + 1) * page)) for p in gp])
-        parity.check_output(out[0, g * gqa:(g + 1) * gqa].double().cpu().numpy(),
-                            O.attention(qh, kk[0, g][toks], vv[0, g][toks], scale), "smoke out")
+        parity.check_attention(out[0, g * gqa:(g + 1) * gqa].double().cpu().numpy(), qh,
+                               kk[0, g][toks], vv[0, g][toks], scale, "smoke out")
     # stage 1 on a small prompt: tensor-core window scores, pooling, top-k, gather with the page
     # summaries of the compact cache
     W, keep, kernel, Lp = 32, 1024, 7, 3001

@@ -63,13 +63,14 @@ def _check_decode_step(rkv, hp, wl, t, samples, caches, new_tokens=False):
                               hp.page, hp.channels, hp.scale)
         tag = f"step {t} unit {u} kv {g} len {L}"
         if ref["pages"] is None:
-            parity.check_output(_f64(out[u, g * wl.gqa:(g + 1) * wl.gqa]), ref["out"], tag)
+            parity.check_attention(_f64(out[u, g * wl.gqa:(g + 1) * wl.gqa]), qh, st["k"][:L],
+                                   st["v"][:L], hp.scale, tag)
             continue
         gp = sel[u, g].cpu().numpy()
         parity.check_selection(gp, ref["scores"], len(ref["pages"]), tag)
         toks = np.concatenate([np.arange(p * hp.page, min(L, (p + 1) * hp.page)) for p in gp])
-        parity.check_output(_f64(out[u, g * wl.gqa:(g + 1) * wl.gqa]),
-                            O.attention(qh, st["k"][toks], st["v"][toks], hp.scale), tag)
+        parity.check_attention(_f64(out[u, g * wl.gqa:(g + 1) * wl.gqa]), qh, st["k"][toks],
+                               st["v"][toks], hp.scale, tag)
 
 
 def _cache_state(kc, vc, page, page_cap, cap):

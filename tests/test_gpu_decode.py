@@ -116,7 +116,8 @@ def _hybrid_case(n, n_kv, gqa, lens, cap, budget, page, channels, seed, steps=2,
                 if ref["channels"] is None:
                     assert (sel_c[u, g] == -1).all(), tag
                     assert (sel_p[u, g] == -1).all(), tag
-                    parity.check_output(_f64(out[u, g * gqa:(g + 1) * gqa]), ref["out"], tag)
+                    parity.check_attention(_f64(out[u, g * gqa:(g + 1) * gqa]), qh, kk[u, g][:L],
+                                           vv[u, g][:L], scale, tag)
                     continue
                 mag = np.abs(qh).sum(axis=0)
                 parity.check_selection(sel_c[u, g].cpu().numpy(), mag, channels,
@@ -136,8 +137,8 @@ def _hybrid_case(n, n_kv, gqa, lens, cap, budget, page, channels, seed, steps=2,
                 assert np.all(np.diff(gp[:nsel]) > 0), f"{tag} pages not ascending"
                 toks = np.concatenate([np.arange(pg * page, min(L, (pg + 1) * page))
                                        for pg in gp[:nsel]])
-                ref_out = O.attention(qh, kk[u, g][toks], vv[u, g][toks], scale)
-                parity.check_output(_f64(out[u, g * gqa:(g + 1) * gqa]), ref_out, tag)
+                parity.check_attention(_f64(out[u, g * gqa:(g + 1) * gqa]), qh, kk[u, g][toks],
+                                       vv[u, g][toks], scale, tag)
 
 
 def test_hybrid_config1_shape():
@@ -187,7 +188,11 @@ def test_hybrid_page1_all_channels_is_exact_group_topk():
                                                   0.1)
         true = _f64(k[0, g])[:L] @ qh.sum(axis=0)
         parity.check_selection(sel_p[0, g].cpu().numpy(), true, B // 2, "exact top-k")
-        parity.check_output(_f64(out[0, g * gqa:(g + 1) * gqa]), ref_out, "exact top-k out")
+        toks = np.sort(np.asarray(ref_tok, dtype=np.int64))
+        parity.check_attention(_f64(out[0, g * gqa:(g + 1) * gqa]), qh, _f64(k[0, g])[toks],
+                               _f64(v[0, g])[toks], 0.1, "exact top-k out")
+        assert np.allclose(O.attention(qh, _f64(k[0, g])[toks], _f64(v[0, g])[toks], 0.1),
+                           ref_out, rtol=1e-12, atol=1e-12), "group_topk_attention's tokens"
 
 
 def test_hybrid_append_steps():
@@ -234,14 +239,15 @@ def test_hybrid_append_steps():
                                       page, C, scale)
                 tag = f"append step {step} unit {u} kv {g} len {L}"
                 if ref["pages"] is None:
-                    parity.check_output(_f64(out[u, g * gqa:(g + 1) * gqa]), ref["out"], tag)
+                    parity.check_attention(_f64(out[u, g * gqa:(g + 1) * gqa]), qh,
+                                           kk[u, g][:L], vv[u, g][:L], scale, tag)
                     continue
                 gp = sel_p[u, g].cpu().numpy()
                 parity.check_selection(gp, ref["scores"], len(ref["pages"]), tag)
                 toks = np.concatenate([np.arange(pg * page, min(L, (pg + 1) * page))
                                        for pg in gp])
-                ref_out = O.attention(qh, kk[u, g][toks], vv[u, g][toks], scale)
-                parity.check_output(_f64(out[u, g * gqa:(g + 1) * gqa]), ref_out, tag)
+                parity.check_attention(_f64(out[u, g * gqa:(g + 1) * gqa]), qh, kk[u, g][toks],
+                                       vv[u, g][toks], scale, tag)
     assert lens_t.cpu().tolist() == cur
     for u in range(n):
         for g in range(n_kv):
@@ -267,8 +273,8 @@ def test_dense_decode_ragged(gqa):
     for u, L in enumerate(lens):
         for g in range(n_kv):
             qh = qq[u, g * gqa:(g + 1) * gqa]
-            ref = O.dense_decode(qh, kk[u, g], vv[u, g], L, 0.0884)
-            parity.check_output(_f64(out[u, g * gqa:(g + 1) * gqa]), ref, f"dense {u} {g}")
+            parity.check_attention(_f64(out[u, g * gqa:(g + 1) * gqa]), qh, kk[u, g][:L],
+                                   vv[u, g][:L], 0.0884, f"dense {u} {g}")
 
 
 def test_device_status_len_over_cap():
@@ -336,8 +342,8 @@ def test_hybrid_page_select_crowded_equal_scores():
         ref_a = O.approx_scores(qh.sum(axis=0), gch, rmin, rmax)
         parity.check_selection(gp, ref_a, S, f"kv {g} pages")
         toks = np.concatenate([np.arange(pg * page, (pg + 1) * page) for pg in gp])
-        parity.check_output(_f64(out[0, g * gqa:(g + 1) * gqa]),
-                            O.attention(qh, kk[0, g][toks], vv[0, g][toks], scale), f"kv {g}")
+        parity.check_attention(_f64(out[0, g * gqa:(g + 1) * gqa]), qh, kk[0, g][toks],
+                               vv[0, g][toks], scale, f"kv {g}")
 
 
 def test_hybrid_exact_ties_take_lowest_pages_and_channels():
@@ -361,5 +367,5 @@ def test_hybrid_exact_ties_take_lowest_pages_and_channels():
     rkv.rkv_check_status(ws)
     assert sel_c[0, 0].tolist() == list(range(C))
     assert sel_p[0, 0].tolist() == list(range(B // 2 // page))
-    ref = O.attention(_f64(q[0]), _f64(k[0, 0, :128]), _f64(v[0, 0, :128]), 0.1)
-    parity.check_output(_f64(out[0]), ref, "all-ties output")
+    parity.check_attention(_f64(out[0]), _f64(q[0]), _f64(k[0, 0, :128]), _f64(v[0, 0, :128]),
+                           0.1, "all-ties output")

@@ -150,13 +150,14 @@ def test_mt_against_oracle():
                                  st["scale"])
         tag = f"unit {u} kv {g}"
         if ref["pages"] is None:
-            parity.check_output(_f64(out[u, g * gqa:(g + 1) * gqa]), ref["out"], tag)
+            parity.check_attention(_f64(out[u, g * gqa:(g + 1) * gqa]), qh, kf[kept[:n1]],
+                                   vf[kept[:n1]], st["scale"], tag)
             continue
         gp = selp[u, g].cpu().numpy()
         parity.check_selection(gp, ref["scores"], len(ref["pages"]), tag)
         rows = np.concatenate([kept[p * PAGE:min(n1, (p + 1) * PAGE)] for p in gp])
-        parity.check_output(_f64(out[u, g * gqa:(g + 1) * gqa]),
-                            O.attention(qh, kf[rows], vf[rows], st["scale"]), tag)
+        parity.check_attention(_f64(out[u, g * gqa:(g + 1) * gqa]), qh, kf[rows], vf[rows],
+                               st["scale"], tag)
 
 
 def test_mt_bad_kept_index_sets_status():
@@ -280,5 +281,5 @@ def test_mt_second_turn_refilter():
             gp = selp[u, g].cpu().numpy()
             parity.check_selection(gp, ref["scores"], len(ref["pages"]), tag)
             rows = np.concatenate([kl[p * PAGE:min(n1 + 1, (p + 1) * PAGE)] for p in gp])
-            parity.check_output(_f64(out[u, g * gqa:(g + 1) * gqa]),
-                                O.attention(qh, kf[rows], vf[rows], scale), tag)
+            parity.check_attention(_f64(out[u, g * gqa:(g + 1) * gqa]), qh, kf[rows], vf[rows],
+                                   scale, tag)

@@ -216,7 +216,7 @@ def test_paged_against_oracle(block):
             gout = _f64(out[u, g * G:(g + 1) * G])
             if ref["channels"] is None:
                 assert (sel_p[u, g] == -1).all(), tag
-                parity.check_output(gout, ref["out"], tag)
+                parity.check_attention(gout, qh, kc[:L], vc[:L], scale, tag)
                 continue
             parity.check_selection(sel_c[u, g].cpu().numpy(), np.abs(qh).sum(axis=0), CHANNELS,
                                    f"{tag} channels")
@@ -231,7 +231,7 @@ def test_paged_against_oracle(block):
             parity.check_selection(gp[:nsel], ref_a, nsel, f"{tag} pages")
             toks = np.concatenate([np.arange(pg * PAGE, min(L, (pg + 1) * PAGE))
                                    for pg in gp[:nsel]])
-            parity.check_output(gout, O.attention(qh, kc[toks], vc[toks], scale), tag)
+            parity.check_attention(gout, qh, kc[toks], vc[toks], scale, tag)
 
 
 def test_paged_bad_table_entry_sets_status():
