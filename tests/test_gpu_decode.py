@@ -128,7 +128,7 @@ def _hybrid_case(n, n_kv, gqa, lens, cap, budget, page, channels, seed, steps=2,
                 ref_a = O.approx_scores(q_g, gch, rmin, rmax)
                 P = rmin.shape[1]
                 magn = parity.approx_magnitude(q_g, gch, rmin, rmax)
-                parity.check_approx(approx[u, g, :P].cpu().numpy(), ref_a, magn,
+                parity.check_approx(approx[u, g, :P].cpu().numpy(), ref_a, magn, len(gch),
                                     f"{tag} approx")
                 nsel = min(S, P)
                 gp = sel_p[u, g].cpu().numpy()

@@ -225,7 +225,8 @@ def test_paged_against_oracle(block):
             ref_a = O.approx_scores(q_g, gch, rmin, rmax)
             P = rmin.shape[1]
             parity.check_approx(approx[u, g, :P].cpu().numpy(), ref_a,
-                                parity.approx_magnitude(q_g, gch, rmin, rmax), f"{tag} approx")
+                                parity.approx_magnitude(q_g, gch, rmin, rmax), len(gch),
+                                f"{tag} approx")
             gp = sel_p[u, g].cpu().numpy()
             nsel = min(S_pages, P)
             parity.check_selection(gp[:nsel], ref_a, nsel, f"{tag} pages")
