@@ -421,7 +421,10 @@ def run_ours(args):
                "kind": "oracle",
                "sample": oracle_sample_text(wl, units, cores, n_samples) +
                          f"; per-unit mean {tc:.3f} s compress, {td * 1e3:.2f} ms per decode step",
-               "sample_s": round(sum(r[0] for r in res), 2)}
+               "sample_s": round(sum(r[0] for r in res), 2),
+               # the same per-unit times with every unit on one core, one after another
+               "value_1core": round(wl.decode_steps / oracle_full_step_s(wl, units, 1, tc, td),
+                                    4)}
 
     launches = hp.launches_per_step() * args.steps
     if rank == 0:
